@@ -1,0 +1,289 @@
+"""Benchmark of the routed-MoE layer with Q2_K experts on GB300.
+
+Headline workload: one DeepSeek-V4-Flash-shaped layer, decode batch 1
+(x[1,4096] bf16, 256 Q2_K experts of 4096->2048->4096, top-6, bf16 shared
+expert of width 2048).  One step = one full layer (router, selection, route,
+routed and shared SwiGLU experts, combine) over one token.  Inputs larger
+than L2: the timed steps rotate over independently generated layers, as a
+decode pass does, so no step finds the previous step's weights in L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--extra] [--layers R]
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+for _p in (ROOT, os.path.join(ROOT, "gen")):
+    if _p not in sys.path:
+        sys.path.insert(0, _p)
+
+import dsgen  # noqa: E402
+
+METRIC = "MoE-layer tokens/s, decode B=1/32 & prefill 4096; % of HBM / bf16 roofline"
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFS = 1900.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": HBM_FALLBACK_GBS, "bf16_tflops": BF16_FALLBACK_TFS}, "fallback"
+
+
+def algorithmic_bytes(cfg, n_experts_used: int, T: int) -> int:
+    """Bytes the layer must move: each used expert once, the shared expert,
+    the router, x in and out."""
+    shared = 3 * cfg.Fs * cfg.D * 2
+    router = cfg.E * cfg.D * (2 if cfg.router_dtype == "bf16" else 4)
+    xio = T * cfg.D * (2 if cfg.x_dtype == "bf16" else 4) + T * cfg.D * 4
+    return n_experts_used * cfg.expert_bytes + shared + router + xio
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- GPU arm --
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import bit_quantized_routed_router_gb300 as ds
+    from bit_quantized_routed_router_gb300 import build as libbuild
+    from bit_quantized_routed_router_gb300 import synthetic
+
+    if rank == 0 or not os.path.exists(ds.LIB_PATH):
+        libbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = dsgen.DECODE1
+    sh = synthetic.shape_of(cfg)
+    R = args.layers
+    layers = [synthetic.build_layer(cfg, layer=r, device=dev) for r in range(R)]
+    xs = [synthetic.build_x(cfg, layer=r, device=dev) for r in range(R)]
+    out = torch.empty((1, cfg.D), dtype=torch.float32, device=dev)
+    ws = torch.empty(ds.workspace_bytes(sh, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+
+    # used experts per layer (for the algorithmic bytes): read back the route once
+    n_used = []
+    for r in range(R):
+        counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+        ds.layer(sh, layers[r], xs[r], out, ws, debug={"counts": counts}, stream=s)
+        n_used.append(int((counts > 0).sum().item()))
+    ds.sync_status(s)
+    bytes_per_step = statistics.mean(algorithmic_bytes(cfg, u, 1) for u in n_used)
+
+    def step(i):
+        r = i % R
+        ds.layer(sh, layers[r], xs[r], out, ws, stream=s)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    clocks = Clocks(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    ds.sync_status(s)
+    t = torch.tensor([ms], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_per_step = ms_max / args.steps
+    value = world * args.steps * cfg.T / (ms_max / 1e3)
+
+    # end to end through the host-buffer entry point: x H2D, layer, out D2H per step
+    xh = [x.cpu().pin_memory() for x in xs]
+    oh = torch.empty((1, cfg.D), dtype=torch.float32).pin_memory()
+    ws_h = torch.empty(ds.workspace_bytes(sh, 1), dtype=torch.uint8, device=dev)
+    for i in range(args.warmup):
+        ds.layer_hostio(sh, layers[i % R], xh[i % R], oh, ws_h, stream=s)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        ds.layer_hostio(sh, layers[i % R], xh[i % R], oh, ws_h, stream=s)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    te = torch.tensor([e2e_ms], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_value = world * args.steps * cfg.T / (float(te.item()) / 1e3)
+
+    pk, pk_kind = peaks()
+    hbm = float(pk.get("hbm_gbs", HBM_FALLBACK_GBS))
+    achieved = bytes_per_step / (ms_per_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Philox generator; weights N(0,0.02) packed to Q2_K)",
+        "config": {"workload": cfg.name, "T": cfg.T, "n_embd": cfg.D, "n_expert": cfg.E,
+                   "top_k": cfg.k, "n_ff": cfg.F, "n_ff_shared": cfg.Fs,
+                   "expert_format": "Q2_K 84 B / 256 weights", "shared_dtype": "bf16",
+                   "l2": f"inputs larger than L2: steps rotate over {R} independently generated "
+                         f"layers ({R * (cfg.E * cfg.expert_bytes) / 1e9:.1f} GB of experts)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "ds_moe_layer decode step (all kernels)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": pk_kind,
+                     "traffic": None, "algorithmic_bytes": bytes_per_step},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.D * 2,
+                "d2h_bytes_per_step": cfg.T * cfg.D * 4},
+        "gpu_launches": args.steps * LAUNCHES_PER_DECODE_STEP,
+        "clocks": clk,
+    }
+    return line
+
+
+LAUNCHES_PER_DECODE_STEP = 5  # router, select+route, gate/up, down, combine
+
+
+# ------------------------------------------------------------ oracle (CPU) --
+
+def oracle_sample(n_tokens: int, budget_s: float = 20.0):
+    """Time the fp64 oracle on decode-B=1 steps (one token each).  Expert
+    regeneration and packing are input preparation and are not timed."""
+    sys.path.insert(0, os.path.join(ROOT, "oracle"))
+    import oracle
+
+    cfg = dsgen.DECODE1
+    lo = oracle.LayerOracle(cfg)
+    times, used_threads = [], 0
+    t_start = time.time()
+    for t in range(n_tokens):
+        x = oracle.as_f64(dsgen.host_x(cfg, [t])[:1], cfg.x_dtype)
+        ids0, _ = oracle.select(lo.logits(x), cfg.k)
+        experts = lo.experts(ids0)
+        t0 = time.perf_counter()
+        L = lo.logits(x)
+        ids, w = oracle.select(L, cfg.k)
+        oracle.moe_layer(x, experts, lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
+        times.append(time.perf_counter() - t0)
+        used_threads = max(used_threads, min(oracle.NTHREADS, len(set(ids.ravel())) + 1))
+        lo._experts.clear()
+        if time.time() - t_start > budget_s and len(times) >= 1:
+            break
+    tot = sum(times)
+    return {"value": len(times) / tot, "unit": "tokens/s", "cores": used_threads,
+            "kind": "oracle", "sample": f"{len(times)} decode-B=1 tokens of the same layer shape "
+                                        f"(fp64 C oracle, {tot:.1f} s of layer compute; expert "
+                                        f"regeneration untimed)"}
+
+
+def reference_arm(args, rank):
+    if rank != 0:
+        return None
+    cb = oracle_sample(max(args.steps, 1), budget_s=min(60.0, 20.0 * max(args.steps, 1)))
+    cfg = dsgen.DECODE1
+    return {"metric": METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / cb["value"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Philox generator)", "impl": "reference",
+            "config": {"workload": cfg.name, "T": 1},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=4, help="rotating layers (L2 defeat)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = reference_arm(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = gpu_arm(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = oracle_sample(3)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+"""Python binding of the ds_moe C ABI (``include/ds_moe.h``).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels
+of ``libds_moe.so``.  PyTorch supplies device memory and streams.  There is
+no fallback: if the library has not been built, importing the binding's
+functions raises.
+
+Names mirror the C entry points: ``q2k_bytes``, ``expert_bytes``,
+``quantize_q2k``, ``dequantize_q2k``, ``workspace_bytes``, ``layer``,
+``layer_hostio``, ``stack``, ``sync_status``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libds_moe.so")
+
+DS_OK, DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED = 0, -1, -2
+DS_ERR_CUDA, DS_ERR_TIMEOUT, DS_ERR_DEVICE_CHECK = -3, -4, -5
+DS_F32, DS_BF16 = 0, 1
+
+SYMBOLS = ["ds_moe_q2k_bytes", "ds_moe_expert_bytes", "ds_moe_quantize_q2k",
+           "ds_moe_dequantize_q2k", "ds_moe_workspace_bytes", "ds_moe_layer",
+           "ds_moe_layer_hostio", "ds_moe_stack", "ds_moe_sync_status", "ds_moe_version"]
+
+
+class DsMoeError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"ds_moe error {code}: {msg}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("n_embd", ctypes.c_int32), ("n_expert", ctypes.c_int32),
+                ("n_ff", ctypes.c_int32), ("n_ff_shared", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("x_dtype", ctypes.c_int32),
+                ("router_dtype", ctypes.c_int32), ("routed_scale", ctypes.c_float)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("shared_gate", ctypes.c_void_p), ("shared_up", ctypes.c_void_p),
+                ("shared_down", ctypes.c_void_p), ("experts_q2k", ctypes.c_void_p)]
+
+
+class Debug(ctypes.Structure):
+    _fields_ = [("logits", ctypes.c_void_p), ("ids", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("counts", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
+                ("perm", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libds_moe.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() "
+                               "(or python bit_quantized_routed_router_gb300/build.py)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, sz, cp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_char_p
+        L.ds_moe_q2k_bytes.restype = sz
+        L.ds_moe_q2k_bytes.argtypes = [i64, i64]
+        L.ds_moe_expert_bytes.restype = sz
+        L.ds_moe_expert_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        for f in (L.ds_moe_quantize_q2k, L.ds_moe_dequantize_q2k):
+            f.restype = ctypes.c_int
+            f.argtypes = [vp, i64, i64, vp, vp, cp, sz]
+        L.ds_moe_workspace_bytes.restype = ctypes.c_int
+        L.ds_moe_workspace_bytes.argtypes = [ctypes.POINTER(Shape), i64, ctypes.POINTER(sz), cp, sz]
+        L.ds_moe_layer.restype = ctypes.c_int
+        L.ds_moe_layer.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64, vp, vp,
+                                   sz, ctypes.POINTER(Debug), vp, cp, sz]
+        L.ds_moe_layer_hostio.restype = ctypes.c_int
+        L.ds_moe_layer_hostio.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64,
+                                          vp, vp, sz, vp, cp, sz]
+        L.ds_moe_stack.restype = ctypes.c_int
+        L.ds_moe_stack.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), ctypes.c_int32,
+                                   vp, i64, ctypes.c_float, vp, sz, vp, cp, sz]
+        L.ds_moe_sync_status.restype = ctypes.c_int
+        L.ds_moe_sync_status.argtypes = [vp, cp, sz]
+        L.ds_moe_version.restype = ctypes.c_char_p
+        L.ds_moe_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _call(fn, *args):
+    err = ctypes.create_string_buffer(512)
+    rc = fn(*args, err, 512)
+    if rc != DS_OK:
+        raise DsMoeError(rc, err.value.decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+@dataclass
+class MoEShape:
+    n_embd: int
+    n_expert: int
+    n_ff: int
+    n_ff_shared: int
+    top_k: int
+    x_dtype: int = DS_BF16
+    router_dtype: int = DS_BF16
+    routed_scale: float = 1.0
+
+    def c(self) -> Shape:
+        return Shape(self.n_embd, self.n_expert, self.n_ff, self.n_ff_shared, self.top_k,
+                     self.x_dtype, self.router_dtype, self.routed_scale)
+
+
+@dataclass
+class MoEWeights:
+    """Device tensors of one layer (see include/ds_moe.h for layouts)."""
+    router_w: object
+    experts_q2k: object
+    router_bias: object = None
+    shared_gate: object = None
+    shared_up: object = None
+    shared_down: object = None
+
+    def c(self) -> Weights:
+        return Weights(_ptr(self.router_w), _ptr(self.router_bias), _ptr(self.shared_gate),
+                       _ptr(self.shared_up), _ptr(self.shared_down), _ptr(self.experts_q2k))
+
+
+def version() -> str:
+    return lib().ds_moe_version().decode()
+
+
+def q2k_bytes(rows: int, in_dim: int) -> int:
+    return lib().ds_moe_q2k_bytes(rows, in_dim)
+
+
+def expert_bytes(n_embd: int, n_ff: int) -> int:
+    return lib().ds_moe_expert_bytes(n_embd, n_ff)
+
+
+def quantize_q2k(w, out, stream=None):
+    """w: fp32 device tensor [rows][in_dim]; out: uint8 device tensor of q2k_bytes."""
+    rows, in_dim = w.shape
+    _call(lib().ds_moe_quantize_q2k, w.data_ptr(), rows, in_dim, out.data_ptr(), _stream(stream))
+
+
+def dequantize_q2k(q, rows, in_dim, out, stream=None):
+    _call(lib().ds_moe_dequantize_q2k, q.data_ptr(), rows, in_dim, out.data_ptr(), _stream(stream))
+
+
+def workspace_bytes(shape: MoEShape, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    _call(lib().ds_moe_workspace_bytes, ctypes.byref(shape.c()), T, ctypes.byref(n))
+    return n.value
+
+
+def layer(shape: MoEShape, weights: MoEWeights, x, out, workspace, debug: dict | None = None,
+          stream=None, T: int | None = None):
+    """out[T][D] fp32 = MoE layer of x[T][D] (device tensors)."""
+    T = x.shape[0] if T is None else T
+    dbg = None
+    if debug is not None:
+        dbg = ctypes.byref(Debug(*[_ptr(debug.get(n)) for n in
+                                   ("logits", "ids", "w", "counts", "offsets", "perm")]))
+    _call(lib().ds_moe_layer, ctypes.byref(shape.c()), ctypes.byref(weights.c()), x.data_ptr(), T,
+          out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), dbg,
+          _stream(stream))
+
+
+def layer_hostio(shape: MoEShape, weights: MoEWeights, x_host, out_host, workspace, stream=None):
+    """Same as layer with x and out in (pinned) host memory; enqueues only."""
+    _call(lib().ds_moe_layer_hostio, ctypes.byref(shape.c()), ctypes.byref(weights.c()),
+          x_host.data_ptr(), x_host.shape[0], out_host.data_ptr(), workspace.data_ptr(),
+          workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def stack(shape: MoEShape, layers, x, workspace, eps: float = 1e-6, stream=None):
+    """x[T][D] fp32 residual, updated in place through len(layers) layers."""
+    arr = (Weights * len(layers))(*[w.c() for w in layers])
+    _call(lib().ds_moe_stack, ctypes.byref(shape.c()), arr, len(layers), x.data_ptr(), x.shape[0],
+          eps, workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def sync_status(stream=None):
+    """Synchronise the stream and raise on a recorded device-side error."""
+    _call(lib().ds_moe_sync_status, _stream(stream))

@@ -1,0 +1,320 @@
+// C-ABI entry points of the ds_moe library (declared in include/ds_moe.h):
+// argument validation, workspace layout, the per-device status word and the
+// dispatch of one routed MoE layer onto the kernels.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsm {
+
+__device__ unsigned g_status_word;
+
+unsigned *status_word() {
+  static std::mutex mu;
+  static unsigned *addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    addr[dev] = (unsigned *)p;
+  }
+  return addr[dev];
+}
+
+namespace {
+
+int fail(char *err, size_t errlen, int code, const char *fmt, ...) {
+  if (err && errlen) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(err, errlen, fmt, ap);
+    va_end(ap);
+  }
+  return code;
+}
+
+int cuda_fail(char *err, size_t errlen, cudaError_t e, const char *what) {
+  return fail(err, errlen, DS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_shape(const ds_moe_shape *s, char *err, size_t errlen, Shape *out) {
+  if (!s) return fail(err, errlen, DS_ERR_INVALID_ARG, "shape is NULL");
+  if (s->n_embd < 256 || s->n_embd > 8192 || s->n_embd % 256)
+    return fail(err, errlen, DS_ERR_UNSUPPORTED, "n_embd=%d: need a multiple of 256 in [256, 8192]",
+                s->n_embd);
+  if (s->n_expert < 1 || s->n_expert > 1024)
+    return fail(err, errlen, DS_ERR_UNSUPPORTED, "n_expert=%d: need 1..1024", s->n_expert);
+  if (s->n_ff < 128 || s->n_ff > 8192 || s->n_ff % 128)
+    return fail(err, errlen, DS_ERR_UNSUPPORTED, "n_ff=%d: need a multiple of 128 in [128, 8192]",
+                s->n_ff);
+  if (s->n_ff_shared < 0 || s->n_ff_shared > 8192 || s->n_ff_shared % 128)
+    return fail(err, errlen, DS_ERR_UNSUPPORTED,
+                "n_ff_shared=%d: need 0 or a multiple of 128 up to 8192", s->n_ff_shared);
+  if (s->top_k < 1 || s->top_k > 16 || s->top_k > s->n_expert)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "top_k=%d: need 1..min(n_expert, 16)", s->top_k);
+  if ((s->x_dtype != DS_F32 && s->x_dtype != DS_BF16) ||
+      (s->router_dtype != DS_F32 && s->router_dtype != DS_BF16))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "x_dtype/router_dtype must be DS_F32 or DS_BF16");
+  if (!isfinite(s->routed_scale))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "routed_scale is not finite");
+  *out = Shape{s->n_embd, s->n_expert, s->n_ff, s->n_ff_shared, s->top_k,
+               s->x_dtype, s->router_dtype, s->routed_scale};
+  return DS_OK;
+}
+
+constexpr size_t ALIGN = 256;
+size_t up(size_t v) { return (v + ALIGN - 1) / ALIGN * ALIGN; }
+
+// Workspace layout; with base == nullptr only the total is computed.
+size_t layout(const Shape &sh, int64_t T, char *base, Work *wk) {
+  const int64_t P = T * sh.k;
+  const int64_t n_chunks = (P + 1023) / 1024;
+  const int64_t xbytes = T * sh.D * (sh.x_dtype == DS_BF16 ? 2 : 4);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char *p = base ? base + off : nullptr;
+    off += up(bytes);
+    return p;
+  };
+  Work w{};
+  w.ctrl = (unsigned *)take(256);
+  w.logits = (float *)take(sizeof(float) * T * sh.E);
+  w.ids = (int32_t *)take(sizeof(int32_t) * P);
+  w.w = (float *)take(sizeof(float) * P);
+  w.counts = (int32_t *)take(sizeof(int32_t) * sh.E);
+  w.offsets = (int32_t *)take(sizeof(int32_t) * (sh.E + 1));
+  w.perm = (int32_t *)take(sizeof(int32_t) * P);
+  w.pos = (int32_t *)take(sizeof(int32_t) * P);
+  w.used = (int32_t *)take(sizeof(int32_t) * (sh.E + 1));
+  w.chunk = (int32_t *)take(sizeof(int32_t) * n_chunks * sh.E);
+  w.h = (float *)take(sizeof(float) * P * sh.F);
+  w.hs = (float *)take(sizeof(float) * T * std::max(sh.Fs, 1));
+  w.y = (float *)take(sizeof(float) * P * sh.D);
+  w.ys = (float *)take(sizeof(float) * T * sh.D);
+  w.xn = (uint16_t *)take(sizeof(uint16_t) * T * sh.D);
+  w.x_dev = take(xbytes);
+  w.out_dev = (float *)take(sizeof(float) * T * sh.D);
+  w.T = T;
+  w.n_chunks = n_chunks;
+  if (wk) *wk = w;
+  return off;
+}
+
+int check_weights(const Shape &sh, const ds_moe_weights *W, char *err, size_t errlen) {
+  if (!W) return fail(err, errlen, DS_ERR_INVALID_ARG, "weights is NULL");
+  if (!W->router_w || !W->experts_q2k)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "router_w and experts_q2k are required");
+  if (!aligned(W->router_w, 16) || !aligned(W->experts_q2k, 16))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "router_w / experts_q2k must be 16-byte aligned");
+  if (W->router_bias && !aligned(W->router_bias, 4))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "router_bias must be 4-byte aligned");
+  if (sh.Fs > 0) {
+    if (!W->shared_gate || !W->shared_up || !W->shared_down)
+      return fail(err, errlen, DS_ERR_INVALID_ARG, "shared expert weights required when n_ff_shared > 0");
+    if (!aligned(W->shared_gate, 16) || !aligned(W->shared_up, 16) || !aligned(W->shared_down, 16))
+      return fail(err, errlen, DS_ERR_INVALID_ARG, "shared expert weights must be 16-byte aligned");
+  }
+  return DS_OK;
+}
+
+// One layer on device buffers: route, expert FFNs, combine into out.
+int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *out, bool accumulate,
+              const Work &wk, const ds_moe_debug *dbg, cudaStream_t s, char *err, size_t errlen) {
+  cudaError_t e = cudaMemsetAsync(wk.ctrl, 0, 256, s);
+  if (e != cudaSuccess) return cuda_fail(err, errlen, e, "workspace control reset");
+  if ((e = launch_route(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
+  if ((e = launch_decode_ffn(sh, W, x, wk, s)) != cudaSuccess)
+    return cuda_fail(err, errlen, e, "expert FFN");
+  if ((e = launch_combine(sh, wk, out, accumulate, s)) != cudaSuccess)
+    return cuda_fail(err, errlen, e, "combine");
+  if (dbg) {
+    const int64_t P = wk.T * sh.k;
+    struct { void *dst; const void *src; size_t n; } cp[] = {
+        {dbg->logits, wk.logits, sizeof(float) * wk.T * sh.E},
+        {dbg->ids, wk.ids, sizeof(int32_t) * P},
+        {dbg->w, wk.w, sizeof(float) * P},
+        {dbg->counts, wk.counts, sizeof(int32_t) * sh.E},
+        {dbg->offsets, wk.offsets, sizeof(int32_t) * (sh.E + 1)},
+        {dbg->perm, wk.perm, sizeof(int32_t) * P},
+    };
+    for (auto &c : cp)
+      if (c.dst && c.n) {
+        e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(err, errlen, e, "debug copy");
+      }
+  }
+  return DS_OK;
+}
+
+}  // namespace
+}  // namespace dsm
+
+using namespace dsm;
+
+extern "C" {
+
+size_t ds_moe_q2k_bytes(int64_t rows, int64_t in_dim) {
+  if (rows < 0 || in_dim < 0) return 0;
+  return (size_t)rows * (size_t)((in_dim + QK - 1) / QK) * QB;
+}
+
+size_t ds_moe_expert_bytes(int32_t n_embd, int32_t n_ff) {
+  if (n_embd <= 0 || n_ff <= 0) return 0;
+  return 2 * ds_moe_q2k_bytes(n_ff, n_embd) + ds_moe_q2k_bytes(n_embd, n_ff);
+}
+
+int ds_moe_quantize_q2k(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, void *stream,
+                        char *err, size_t errlen) {
+  if (rows < 0 || in_dim < 0) return fail(err, errlen, DS_ERR_INVALID_ARG, "negative size");
+  if (rows == 0 || in_dim == 0) return DS_OK;
+  if (!w || !out) return fail(err, errlen, DS_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(w, 4) || !aligned(out, 4))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "w and out must be 4-byte aligned");
+  if (!status_word()) return fail(err, errlen, DS_ERR_CUDA, "no CUDA device");
+  cudaError_t e = launch_quantize(w, rows, in_dim, out, (cudaStream_t)stream);
+  return e == cudaSuccess ? DS_OK : cuda_fail(err, errlen, e, "quantize");
+}
+
+int ds_moe_dequantize_q2k(const uint8_t *q, int64_t rows, int64_t in_dim, float *out, void *stream,
+                          char *err, size_t errlen) {
+  if (rows < 0 || in_dim < 0) return fail(err, errlen, DS_ERR_INVALID_ARG, "negative size");
+  if (rows == 0 || in_dim == 0) return DS_OK;
+  if (!q || !out) return fail(err, errlen, DS_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(out, 4)) return fail(err, errlen, DS_ERR_INVALID_ARG, "out must be 4-byte aligned");
+  cudaError_t e = launch_dequantize(q, rows, in_dim, out, (cudaStream_t)stream);
+  return e == cudaSuccess ? DS_OK : cuda_fail(err, errlen, e, "dequantize");
+}
+
+int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, char *err,
+                           size_t errlen) {
+  Shape sh{};
+  int rc = check_shape(shape, err, errlen, &sh);
+  if (rc) return rc;
+  if (!bytes) return fail(err, errlen, DS_ERR_INVALID_ARG, "bytes is NULL");
+  if (T < 0 || T > (1 << 24)) return fail(err, errlen, DS_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
+  *bytes = layout(sh, T, nullptr, nullptr);
+  return DS_OK;
+}
+
+int ds_moe_layer(const ds_moe_shape *shape, const ds_moe_weights *weights, const void *x, int64_t T,
+                 float *out, void *workspace, size_t workspace_bytes, const ds_moe_debug *dbg,
+                 void *stream, char *err, size_t errlen) {
+  Shape sh{};
+  int rc = check_shape(shape, err, errlen, &sh);
+  if (rc) return rc;
+  if ((rc = check_weights(sh, weights, err, errlen))) return rc;
+  if (T < 0 || T > (1 << 24)) return fail(err, errlen, DS_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
+  if (T == 0) return DS_OK;
+  if (!x || !out || !workspace) return fail(err, errlen, DS_ERR_INVALID_ARG, "x, out and workspace are required");
+  if (!aligned(x, 16) || !aligned(out, 16))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  if (!aligned(workspace, ALIGN))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = layout(sh, T, nullptr, nullptr);
+  if (workspace_bytes < need)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes",
+                workspace_bytes, need);
+  if (!status_word()) return fail(err, errlen, DS_ERR_CUDA, "no CUDA device");
+  Work wk;
+  layout(sh, T, (char *)workspace, &wk);
+  return run_layer(sh, *weights, x, out, false, wk, dbg, (cudaStream_t)stream, err, errlen);
+}
+
+int ds_moe_layer_hostio(const ds_moe_shape *shape, const ds_moe_weights *weights,
+                        const void *x_host, int64_t T, float *out_host, void *workspace,
+                        size_t workspace_bytes, void *stream, char *err, size_t errlen) {
+  Shape sh{};
+  int rc = check_shape(shape, err, errlen, &sh);
+  if (rc) return rc;
+  if ((rc = check_weights(sh, weights, err, errlen))) return rc;
+  if (T < 0 || T > (1 << 24)) return fail(err, errlen, DS_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
+  if (T == 0) return DS_OK;
+  if (!x_host || !out_host || !workspace)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "x_host, out_host and workspace are required");
+  if (!aligned(workspace, ALIGN))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = layout(sh, T, nullptr, nullptr);
+  if (workspace_bytes < need)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes",
+                workspace_bytes, need);
+  if (!status_word()) return fail(err, errlen, DS_ERR_CUDA, "no CUDA device");
+  Work wk;
+  layout(sh, T, (char *)workspace, &wk);
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t xbytes = (size_t)T * sh.D * (sh.x_dtype == DS_BF16 ? 2 : 4);
+  cudaError_t e = cudaMemcpyAsync(wk.x_dev, x_host, xbytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(err, errlen, e, "copy x to device");
+  rc = run_layer(sh, *weights, wk.x_dev, wk.out_dev, false, wk, nullptr, s, err, errlen);
+  if (rc) return rc;
+  e = cudaMemcpyAsync(out_host, wk.out_dev, sizeof(float) * T * sh.D, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? DS_OK : cuda_fail(err, errlen, e, "copy out to host");
+}
+
+int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_t n_layers,
+                 float *x, int64_t T, float eps, void *workspace, size_t workspace_bytes,
+                 void *stream, char *err, size_t errlen) {
+  Shape sh{};
+  int rc = check_shape(shape, err, errlen, &sh);
+  if (rc) return rc;
+  if (sh.x_dtype != DS_BF16)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "the stack feeds bf16 normalised inputs: x_dtype must be DS_BF16");
+  if (n_layers < 0 || (n_layers > 0 && !layers))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "bad layer array");
+  for (int l = 0; l < n_layers; ++l)
+    if ((rc = check_weights(sh, &layers[l], err, errlen))) return rc;
+  if (T < 0 || T > (1 << 24)) return fail(err, errlen, DS_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
+  if (T == 0 || n_layers == 0) return DS_OK;
+  if (!x || !workspace) return fail(err, errlen, DS_ERR_INVALID_ARG, "x and workspace are required");
+  if (!aligned(x, 16) || !aligned(workspace, ALIGN))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "x must be 16-byte and workspace 256-byte aligned");
+  if (!(eps > 0.0f) || !isfinite(eps)) return fail(err, errlen, DS_ERR_INVALID_ARG, "eps must be > 0");
+  const size_t need = layout(sh, T, nullptr, nullptr);
+  if (workspace_bytes < need)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes",
+                workspace_bytes, need);
+  if (!status_word()) return fail(err, errlen, DS_ERR_CUDA, "no CUDA device");
+  Work wk;
+  layout(sh, T, (char *)workspace, &wk);
+  cudaStream_t s = (cudaStream_t)stream;
+  for (int l = 0; l < n_layers; ++l) {
+    cudaError_t e = launch_rmsnorm_bf16(x, T, sh.D, eps, wk.xn, s);
+    if (e != cudaSuccess) return cuda_fail(err, errlen, e, "rmsnorm");
+    rc = run_layer(sh, layers[l], wk.xn, x, true, wk, nullptr, s, err, errlen);
+    if (rc) return rc;
+  }
+  return DS_OK;
+}
+
+int ds_moe_sync_status(void *stream, char *err, size_t errlen) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(err, errlen, e, "stream");
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(err, errlen, e, "read status word");
+  if (v) {
+    unsigned z = 0;
+    e = cudaMemcpyToSymbol(g_status_word, &z, sizeof z);
+    if (e != cudaSuccess) return cuda_fail(err, errlen, e, "clear status word");
+  }
+  if (v & ST_TIMEOUT) return fail(err, errlen, DS_ERR_TIMEOUT, "a device wait timed out (status 0x%x)", v);
+  if (v & ST_QUANT_INPUT)
+    return fail(err, errlen, DS_ERR_DEVICE_CHECK, "quantiser input not finite or |w| > 65504 (status 0x%x)", v);
+  if (v & ST_BAD_ID) return fail(err, errlen, DS_ERR_DEVICE_CHECK, "expert id out of range (status 0x%x)", v);
+  if (v) return fail(err, errlen, DS_ERR_DEVICE_CHECK, "device check failed (status 0x%x)", v);
+  return DS_OK;
+}
+
+const char *ds_moe_version(void) { return "ds_moe 0.1 (sm_103a)"; }
+
+}  // extern "C"

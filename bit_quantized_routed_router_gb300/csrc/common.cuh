@@ -1,0 +1,60 @@
+// Shared device helpers of the ds_moe CUDA library (sm_103a).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds_moe.h"
+
+namespace dsm {
+
+constexpr int QK = 256;      // weights per Q2_K super-block
+constexpr int QB = 84;       // bytes per Q2_K super-block
+constexpr int NUM_SMS = 152; // GB300
+
+// Sticky status bits (per device, read by ds_moe_sync_status).
+enum : unsigned {
+  ST_QUANT_INPUT = 1u << 0,   // non-finite / out-of-range quantiser input
+  ST_BAD_ID = 1u << 1,        // expert id outside [0, E)
+  ST_TIMEOUT = 1u << 2,       // a bounded device wait expired
+  ST_BAD_COUNT = 1u << 3,     // route counts inconsistent
+};
+
+// Status word address for the current device (set up once per device).
+unsigned *status_word();
+
+__device__ __forceinline__ void flag(unsigned *st, unsigned bit) { atomicOr(st, bit); }
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ float fp16_to_f32(uint16_t h) {
+  return __half2float(__ushort_as_half(h));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+// ----------------------------------------------------------------------------
+// Host-side launch helpers
+// ----------------------------------------------------------------------------
+
+struct Shape {
+  int D, E, F, Fs, k;
+  int x_dtype, router_dtype;
+  float routed_scale;
+  int64_t nb_D() const { return (D + QK - 1) / QK; }
+  int64_t nb_F() const { return (F + QK - 1) / QK; }
+  int64_t gate_bytes() const { return (int64_t)F * nb_D() * QB; }
+  int64_t down_bytes() const { return (int64_t)D * nb_F() * QB; }
+  int64_t expert_bytes() const { return 2 * gate_bytes() + down_bytes(); }
+};
+
+}  // namespace dsm

@@ -1,0 +1,53 @@
+// Internal launchers of the ds_moe library (not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dsm {
+
+// Device views of the per-call workspace (all device pointers).
+struct Work {
+  float *logits;     // [T][E]
+  int32_t *ids;      // [T][k]
+  float *w;          // [T][k]
+  int32_t *counts;   // [E]
+  int32_t *offsets;  // [E+1]
+  int32_t *perm;     // [T*k]
+  int32_t *pos;      // [T*k]
+  int32_t *used;     // [E+1]: used[0..n) ascending experts with tokens, used[E] = n
+  int32_t *chunk;    // [n_chunks][E] per-chunk histogram (large T)
+  unsigned *ctrl;    // control words (zeroed at the start of every call)
+  float *h;          // [T*k][F] routed SwiGLU activations, perm order
+  float *hs;         // [T][Fs] shared-expert activations
+  float *y;          // [T*k][D] routed expert outputs, perm order
+  float *ys;         // [T][D] shared-expert output
+  uint16_t *xn;      // [T][D] bf16 normalised input (stack)
+  void *x_dev;       // [T][D] device copy of host x (hostio)
+  float *out_dev;    // [T][D] device out (hostio)
+  int64_t T;
+  int64_t n_chunks;
+};
+
+cudaError_t launch_quantize(const float *w, int64_t rows, int64_t in_dim, uint8_t *out,
+                            cudaStream_t s);
+cudaError_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t in_dim, float *out,
+                              cudaStream_t s);
+
+// Router logits, top-k selection and the expert route (histogram, scan,
+// stable permutation, used-expert list).
+cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
+                         cudaStream_t s);
+
+// Decode path: grouped dequantising GEMVs and the combine.
+cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const void *x,
+                              const Work &wk, cudaStream_t s);
+cudaError_t launch_combine(const Shape &sh, const Work &wk, float *out, bool accumulate,
+                           cudaStream_t s);
+
+// Stack helper: bf16(x / sqrt(mean(x^2) + eps)).
+cudaError_t launch_rmsnorm_bf16(const float *x, int64_t T, int D, float eps, uint16_t *out,
+                                cudaStream_t s);
+
+}  // namespace dsm

@@ -1,0 +1,174 @@
+/* ds_moe: one routed mixture-of-experts layer with 2-bit (Q2_K) routed
+ * experts, computed on one GB300 (sm_103a) GPU.
+ *
+ * The layer ("Understanding Dwarf Star", 5.3.2 "The MoE Architecture" and
+ * 5.3.7 "The MoE Kernel in Metal"):
+ *     logits  = x W_router^T (+ bias)                      router, fp32
+ *     ids, w  = top-k of logits, w = softmax over the k     selection
+ *     y_e(x)  = W_down,e ( SiLU(W_gate,e x) * (W_up,e x) )  SwiGLU expert
+ *     out     = y_shared(x) + sum_j w_j y_{ids_j}(x)        combine, fp32
+ * with the routed expert matrices stored as Q2_K super-blocks ("Understanding
+ * Dwarf Star", 3.3.3 "Q2_K: 2.625 Bits Per Element"): 84 bytes per 256
+ * weights along each matrix's input dimension.  Shapes of the DeepSeek V4
+ * Flash layer: n_embd 4096, 256 experts, top-6, one shared expert, expert
+ * width 2048 ("Understanding Dwarf Star", 2.4.3 shape table).
+ *
+ * Conventions (the pages' C engine style: int status, 0 = ok, negative =
+ * error, plus a caller-supplied error buffer; caller-owned scratch):
+ *   - Every pointer is a DEVICE pointer unless the argument says "host".
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous on that stream unless stated.
+ *   - The library allocates no device memory: the caller owns every buffer,
+ *     including the workspace, and nothing is retained after a call returns.
+ *   - Argument errors are detected on the host before any launch and return
+ *     DS_ERR_INVALID_ARG (or DS_ERR_UNSUPPORTED) with a message in err.
+ *     Errors a kernel detects (a non-finite weight given to the quantiser,
+ *     a corrupted id, a timed-out wait) are recorded in a per-device sticky
+ *     status word, read and cleared by ds_moe_sync_status.
+ *   - err may be NULL; otherwise up to errlen bytes (NUL-terminated) are
+ *     written on failure.
+ *   - Calls are thread-safe as long as concurrent calls use distinct
+ *     workspaces and outputs.
+ *
+ * Q2_K super-block (84 bytes, 256 weights):
+ *   bytes [0,16)   sub-block s (16 weights each): scale sc_s in the low
+ *                  nibble, min m_s in the high nibble
+ *   bytes [16,80)  2-bit codes; weight j at byte 16 + j/4, bits 2*(j%4)
+ *   bytes [80,82)  d, fp16 little-endian;  bytes [82,84) dmin, fp16
+ *   weight j = d*sc_s*q_j - dmin*m_s  (s = j/16)
+ * A row of in_dim weights uses ceil(in_dim/256) blocks (zero-padded).
+ * Packed expert e = gate [n_ff rows][n_embd] | up [n_ff][n_embd] |
+ * down [n_embd rows][n_ff], each row-major in blocks; experts are contiguous
+ * in expert order, each ds_moe_expert_bytes() long; base 16-byte aligned.
+ */
+#ifndef DS_MOE_H
+#define DS_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DS_OK = 0,
+  DS_ERR_INVALID_ARG = -1,  /* bad pointer, size, alignment or workspace    */
+  DS_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. odd n_embd)  */
+  DS_ERR_CUDA = -3,         /* a CUDA runtime call failed                    */
+  DS_ERR_TIMEOUT = -4,      /* a device wait hit its iteration limit         */
+  DS_ERR_DEVICE_CHECK = -5  /* a kernel found invalid data                   */
+} ds_status;
+
+typedef enum { DS_F32 = 0, DS_BF16 = 1 } ds_dtype;
+
+typedef struct {
+  int32_t n_embd;       /* D: model width, multiple of 256, <= 8192          */
+  int32_t n_expert;     /* E: routed experts, 1..1024                        */
+  int32_t n_ff;         /* F: expert width, multiple of 128, <= 8192         */
+  int32_t n_ff_shared;  /* Fs: shared expert width, 0 = none, mult. of 128, <= 8192 */
+  int32_t top_k;        /* k: 1..min(E, 16)                                  */
+  int32_t x_dtype;      /* ds_dtype of x                                     */
+  int32_t router_dtype; /* ds_dtype of router_w                              */
+  float routed_scale;   /* multiplies the k routing weights (1.0 default)    */
+} ds_moe_shape;
+
+typedef struct {
+  const void *router_w;       /* [E][D] router_dtype, row-major                 */
+  const float *router_bias;   /* [E] fp32 added to the logits, or NULL          */
+  const uint16_t *shared_gate; /* [Fs][D] bf16 bits (NULL when Fs == 0)        */
+  const uint16_t *shared_up;   /* [Fs][D] bf16 bits                             */
+  const uint16_t *shared_down; /* [D][Fs] bf16 bits                             */
+  const uint8_t *experts_q2k; /* [E] packed experts, 16-byte aligned           */
+} ds_moe_weights;
+
+/* Optional debug outputs of ds_moe_layer (device pointers; NULL fields and a
+ * NULL struct are skipped).  All are written in the same stream order. */
+typedef struct {
+  float *logits;    /* [T][E] router logits incl. bias (fp32)                 */
+  int32_t *ids;     /* [T][k] selected experts, descending logit order        */
+  float *w;         /* [T][k] routing weights (after routed_scale)            */
+  int32_t *counts;  /* [E] tokens per expert                                  */
+  int32_t *offsets; /* [E+1] exclusive scan of counts                         */
+  int32_t *perm;    /* [T*k] pair t*k+j at position offsets[e]+rank, stable   */
+} ds_moe_debug;
+
+/* Bytes of a Q2_K matrix of `rows` rows of `in_dim` weights:
+ * rows * ceil(in_dim/256) * 84 ("Understanding Dwarf Star", 3.3.3).
+ * Returns 0 for negative sizes. */
+size_t ds_moe_q2k_bytes(int64_t rows, int64_t in_dim);
+
+/* Bytes of one packed routed expert (gate, up and down; "The sparsity that
+ * pays for everything else in DwarfStar", "Where the parameters actually
+ * are": gate, up and down per expert). */
+size_t ds_moe_expert_bytes(int32_t n_embd, int32_t n_ff);
+
+/* Quantise an fp32 matrix w [rows][in_dim] (row-major, device) to Q2_K
+ * blocks in out (ds_moe_q2k_bytes(rows, in_dim) bytes, device, 4-byte
+ * aligned).  The encoding picks, per super-block, the smallest fp16 dmin and
+ * d and the smallest 4-bit mins and scales whose four evenly spaced levels
+ * cover each 16-weight sub-block, then rounds each weight to its nearest
+ * level, ties upward ("Understanding Dwarf Star", 2.3.5: Q2_K levels are
+ * evenly spaced between the block's min and max; 3.3.3 block layout).  Every
+ * decision is exact, so the bytes are a pure function of the inputs.
+ * Non-finite inputs or |w| > 65504 set DS_ERR_DEVICE_CHECK in the status
+ * word and produce an all-zero block. */
+int ds_moe_quantize_q2k(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, void *stream,
+                        char *err, size_t errlen);
+
+/* Dequantise Q2_K blocks q [rows][ceil(in_dim/256)*84] to fp32
+ * out [rows][in_dim]: out = fp32(d*sc*q - dmin*m), i.e. the exact value
+ * rounded once ("Understanding Dwarf Star", 2.8.1: weights are rebuilt from
+ * the stored scales and mins).  A test and inspection aid. */
+int ds_moe_dequantize_q2k(const uint8_t *q, int64_t rows, int64_t in_dim, float *out, void *stream,
+                          char *err, size_t errlen);
+
+/* Workspace bytes ds_moe_layer needs for T tokens of this shape (host call,
+ * synchronous).  The workspace must be 256-byte aligned. */
+int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, char *err,
+                           size_t errlen);
+
+/* One routed MoE layer on T tokens (the equations at the top of this file).
+ *   x    [T][D] x_dtype (device), 16-byte aligned
+ *   out  [T][D] fp32 (device), 16-byte aligned; fully overwritten
+ *   workspace: ds_moe_workspace_bytes bytes, 256-byte aligned, caller-owned;
+ *        its contents need no initialisation and are scratch after return
+ *   dbg  optional debug outputs (NULL to skip)
+ * Tokens are independent: row t of out depends only on row t of x.
+ * T == 0 is a no-op.  Decode-sized batches (T <= 64) use the fused
+ * dequantising GEMV path; larger batches use the grouped tensor-core path. */
+int ds_moe_layer(const ds_moe_shape *shape, const ds_moe_weights *weights, const void *x, int64_t T,
+                 float *out, void *workspace, size_t workspace_bytes, const ds_moe_debug *dbg,
+                 void *stream, char *err, size_t errlen);
+
+/* ds_moe_layer with x and out in HOST memory (pinned for best speed): the
+ * host-to-device copy of x and the device-to-host copy of out are issued on
+ * `stream` around the layer, using the workspace for the device copies
+ * (ds_moe_workspace_bytes covers them).  Returns after enqueueing; the caller
+ * synchronises the stream before reading out. */
+int ds_moe_layer_hostio(const ds_moe_shape *shape, const ds_moe_weights *weights,
+                        const void *x_host, int64_t T, float *out_host, void *workspace,
+                        size_t workspace_bytes, void *stream, char *err, size_t errlen);
+
+/* A stack of n_layers blocks, each  x <- x + layer_l(bf16(RMSNorm(x)))  with
+ * RMSNorm(x) = x / sqrt(mean(x^2) + eps) and unit gain (pages: every layer
+ * applies RMSNorm and a residual connection).  x [T][D] fp32 (device) is the
+ * residual stream, updated in place.  layers: host array of n_layers weight
+ * sets; shape->x_dtype must be DS_BF16.  Workspace as for ds_moe_layer. */
+int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_t n_layers,
+                 float *x, int64_t T, float eps, void *workspace, size_t workspace_bytes,
+                 void *stream, char *err, size_t errlen);
+
+/* Synchronise `stream`, then read and clear this device's sticky status
+ * word.  Returns DS_OK, DS_ERR_TIMEOUT or DS_ERR_DEVICE_CHECK (with a message
+ * naming the check), or DS_ERR_CUDA if the stream itself failed. */
+int ds_moe_sync_status(void *stream, char *err, size_t errlen);
+
+/* Library version string (static storage). */
+const char *ds_moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS_MOE_H */

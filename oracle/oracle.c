@@ -103,8 +103,8 @@ static int d_ok(double h, const void *c) {
 /* ----------------------------------------------------------- Q2_K block --- */
 
 /* Quantise one super-block of 256 values ([UDS] 3.3.3, reading above).
- * Returns 0, or -1 when a value is not finite or too large for an fp16
- * scale. */
+ * Returns 0, or -1 when a value is not finite or |v| > 65504 (the largest
+ * fp16: the encoding's domain, so that every scale fits in fp16). */
 static int q2k_quantize_block(const double *x, uint8_t *out) {
   double lo[16], hi[16], neg_lo[16], b[16];
   int m[16], sc[16];
@@ -112,7 +112,7 @@ static int q2k_quantize_block(const double *x, uint8_t *out) {
     double mn = 0.0, mx = -INFINITY;
     for (int j = 0; j < 16; ++j) {
       double v = x[16 * s + j];
-      if (!isfinite(v)) return -1;
+      if (!(fabs(v) <= 65504.0)) return -1; /* also rejects NaN and infinities */
       if (v < mn) mn = v;
       if (v > mx) mx = v;
     }

@@ -1,0 +1,335 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Bit-exact: Q2_K bytes, dequantised weights, expert ids (and their order),
+per-expert counts, offsets and the permutation.  Floats: max|err| <= tol *
+rms(out_oracle) with tol = 2e-3 on the decode path and 5e-3 on the
+prefill path; the oracle's routing weights and logits are compared at the
+same scale.  Tokens are resampled (oracle-side) until no two of their top
+k+1 logits lie within 1e-4, so the selection has one answer at fp32.
+"""
+import numpy as np
+import pytest
+
+import dsgen
+import oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import bit_quantized_routed_router_gb300 as ds  # noqa: E402
+from bit_quantized_routed_router_gb300 import synthetic  # noqa: E402
+
+DECODE_TOL = 2e-3
+PREFILL_TOL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_quantized_routed_router_gb300 import build
+    build.build()
+    yield
+
+
+def gpu_quantize(w_np):
+    w = torch.from_numpy(np.ascontiguousarray(w_np, np.float32)).cuda()
+    out = torch.zeros(ds.q2k_bytes(*w.shape), dtype=torch.uint8, device="cuda")
+    ds.quantize_q2k(w, out)
+    ds.sync_status()
+    return out.cpu().numpy().reshape(w.shape[0], -1)
+
+
+def run_layer(cfg, W, x, scale=1.0):
+    T = x.shape[0]
+    sh = synthetic.shape_of(cfg)
+    sh.routed_scale = scale
+    ws = torch.empty(ds.workspace_bytes(sh, T), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, cfg.D), dtype=torch.float32, device="cuda")
+    P = T * cfg.k
+    dbg = {"logits": torch.empty((T, cfg.E), dtype=torch.float32, device="cuda"),
+           "ids": torch.empty((T, cfg.k), dtype=torch.int32, device="cuda"),
+           "w": torch.empty((T, cfg.k), dtype=torch.float32, device="cuda"),
+           "counts": torch.empty(cfg.E, dtype=torch.int32, device="cuda"),
+           "offsets": torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda"),
+           "perm": torch.empty(P, dtype=torch.int32, device="cuda")}
+    ds.layer(sh, W, x, out, ws, debug=dbg)
+    ds.sync_status()
+    return out.cpu().numpy(), {k: v.cpu().numpy() for k, v in dbg.items()}
+
+
+def check_route(dbg, ids_ref, E, rows=None):
+    """ids (and order) for the given rows; counts/offsets/perm over the batch."""
+    ids = dbg["ids"] if rows is None else dbg["ids"][rows]
+    assert np.array_equal(ids, ids_ref)
+
+
+def check_route_full(dbg, ids_ref, E):
+    assert np.array_equal(dbg["ids"], ids_ref)
+    counts, offsets, perm, _ = oracle.route(ids_ref, E)
+    assert np.array_equal(dbg["counts"], counts)
+    assert np.array_equal(dbg["offsets"], offsets)
+    assert np.array_equal(dbg["perm"], perm)
+
+
+def check_close(got, ref, tol, what="out"):
+    rms = np.sqrt(np.mean(ref ** 2))
+    err = np.max(np.abs(got.astype(np.float64) - ref))
+    assert err <= tol * rms, f"{what}: max|err| {err:.3e} > {tol} * rms {rms:.3e}"
+    print(f"{what}: max|err|/rms = {err / rms:.3e}")
+    return err / rms
+
+
+# ------------------------------------------------------------- quantiser --
+
+@pytest.mark.parametrize("rows,in_dim,scale", [(3, 256, 0.02), (5, 128, 1.0), (4, 300, 5.0),
+                                               (64, 1024, 0.02), (2, 256, 1e4), (2, 512, 1e-30)])
+def test_quantize_bit_exact_random(rows, in_dim, scale):
+    rng = np.random.default_rng(rows * 1000 + in_dim)
+    x = (rng.normal(size=(rows, in_dim)) * scale).astype(np.float32)
+    x[0, :16] = np.abs(x[0, :16])
+    if rows > 1:
+        x[1, 16:32] = 0.0
+        x[1, 32:48] = -np.abs(x[1, 32:48])
+    assert np.array_equal(gpu_quantize(x), oracle.quantize(x))
+
+
+def test_quantize_domain_edges():
+    x = np.zeros((3, 256), np.float32)
+    x[0, 0], x[0, 1] = 65504.0, -65504.0
+    x[1, 7] = 1e-45   # fp32 subnormal
+    x[2, :] = np.linspace(-3.0, 7.0, 256)
+    assert np.array_equal(gpu_quantize(x), oracle.quantize(x))
+    bad = np.zeros((1, 256), np.float32)
+    bad[0, 9] = 65505.0
+    with pytest.raises(ValueError):
+        oracle.quantize(bad)
+    with pytest.raises(ds.DsMoeError):
+        gpu_quantize(bad)
+
+
+def test_quantize_bit_exact_generated_expert():
+    cfg = dsgen.DECODE1
+    g, u, d = dsgen.host_expert_f32(cfg, 17)
+    for m in (g, d):
+        assert np.array_equal(gpu_quantize(m), oracle.quantize(m))
+
+
+def test_quantize_nonfinite_sets_status():
+    x = np.zeros((2, 256), np.float32)
+    x[1, 5] = np.inf
+    w = torch.from_numpy(x).cuda()
+    out = torch.full((ds.q2k_bytes(2, 256),), 7, dtype=torch.uint8, device="cuda")
+    ds.quantize_q2k(w, out)
+    with pytest.raises(ds.DsMoeError) as ei:
+        ds.sync_status()
+    assert ei.value.code == ds.DS_ERR_DEVICE_CHECK
+    o = out.cpu().numpy()
+    assert not o[84:].any()          # the bad block is zeroed
+    assert np.array_equal(o[:84], oracle.quantize(x[:1]).ravel())
+    ds.sync_status()                 # the status word was cleared
+
+
+def test_dequantize_bit_exact():
+    rng = np.random.default_rng(3)
+    x = (rng.normal(size=(16, 512)) * 0.02).astype(np.float32)
+    q = oracle.quantize(x)
+    blocks = rng.integers(0, 256, (4, 3 * 84)).astype(np.uint8)
+    for r in range(4):
+        for b in range(3):
+            for o in (80, 82):  # finite d and dmin, some subnormal
+                v = int(rng.integers(0, 0x7BFF))
+                blocks[r, 84 * b + o], blocks[r, 84 * b + o + 1] = v & 0xFF, v >> 8
+    for qq, rows, in_dim in ((q, 16, 512), (blocks, 4, 700)):
+        ref = oracle.dequantize(qq, rows, in_dim).astype(np.float32)  # fp32 of the exact value
+        out = torch.empty((rows, in_dim), dtype=torch.float32, device="cuda")
+        ds.dequantize_q2k(torch.from_numpy(qq).cuda(), rows, in_dim, out)
+        ds.sync_status()
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+# ----------------------------------------------------------------- layers --
+
+def oracle_case(cfg, layer=0):
+    lo = oracle.LayerOracle(cfg, layer)
+    att = oracle.resample_attempts(cfg, lo)
+    x = oracle.as_f64(dsgen.host_x(cfg, att, layer), cfg.x_dtype)
+    return lo, att, x
+
+
+def layer_parity(cfg, tol, scale=1.0):
+    lo, att, x64 = oracle_case(cfg)
+    W = synthetic.build_layer(cfg)
+    x = synthetic.build_x(cfg, att)
+    out, dbg = run_layer(cfg, W, x, scale)
+    L = lo.logits(x64)
+    ids, w = oracle.select(L, cfg.k, scale)
+    check_route_full(dbg, ids, cfg.E)
+    res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
+    check_close(dbg["logits"], L, 1e-5, "logits")
+    assert np.max(np.abs(dbg["w"] - w)) <= 1e-5
+    return check_close(out, res, tol)
+
+
+def test_tiny_layer_parity():
+    layer_parity(dsgen.TINY, DECODE_TOL)
+
+
+@pytest.mark.parametrize("variant", ["k_eq_E", "one_expert", "shared", "scale1.5", "T33", "T1"])
+def test_tiny_variants(variant):
+    from dataclasses import replace
+    c = dsgen.TINY
+    scale = 1.0
+    if variant == "k_eq_E":
+        c = replace(c, k=16)
+    elif variant == "one_expert":
+        c = replace(c, E=1, k=1)
+    elif variant == "shared":
+        c = replace(c, Fs=128, shared_sigma=0.02)
+    elif variant == "scale1.5":
+        scale = 1.5
+    elif variant == "T33":
+        c = replace(c, T=33, k=3)
+    elif variant == "T1":
+        c = replace(c, T=1)
+    layer_parity(c, DECODE_TOL, scale)
+
+
+def test_tiny_prefill_sized_batch():
+    """A batch beyond the decode size takes the large-batch route kernels."""
+    from dataclasses import replace
+    c = replace(dsgen.TINY, T=700, k=2)
+    layer_parity(c, PREFILL_TOL)
+
+
+@pytest.fixture(scope="module")
+def decode1():
+    cfg = dsgen.DECODE1
+    lo, att, x64 = oracle_case(cfg)
+    return cfg, lo, att, x64, synthetic.build_layer(cfg)
+
+
+def test_decode_b1_parity(decode1):
+    cfg, lo, att, x64, W = decode1
+    out, dbg = run_layer(cfg, W, synthetic.build_x(cfg, att))
+    (res, ids, w, L) = lo.forward(x64)
+    check_route_full(dbg, ids, cfg.E)
+    check_close(dbg["logits"], L, 1e-5, "logits")
+    check_close(out, res, DECODE_TOL)
+
+
+def test_decode_hostio_matches_device(decode1):
+    cfg, lo, att, x64, W = decode1
+    x = synthetic.build_x(cfg, att)
+    out_dev, _ = run_layer(cfg, W, x)
+    sh = synthetic.shape_of(cfg)
+    ws = torch.empty(ds.workspace_bytes(sh, 1), dtype=torch.uint8, device="cuda")
+    xh = x.cpu().pin_memory()
+    oh = torch.empty((1, cfg.D), dtype=torch.float32).pin_memory()
+    ds.layer_hostio(sh, W, xh, oh, ws)
+    ds.sync_status()
+    assert np.array_equal(oh.numpy(), out_dev)
+
+
+def test_decode32_zipf_parity():
+    cfg = dsgen.DECODE32_ZIPF
+    layer_parity(cfg, DECODE_TOL)
+
+
+def test_batch_invariance_decode(decode1):
+    """A token computed alone equals the same token inside a decode batch, bit for bit."""
+    cfg, lo, att, x64, W = decode1
+    from dataclasses import replace
+    c8 = replace(cfg, T=8)
+    xb = synthetic.build_x(c8)
+    out_b, _ = run_layer(c8, W, xb)
+    for t in (0, 5):
+        out_1, _ = run_layer(cfg, W, xb[t:t + 1].contiguous())
+        assert np.array_equal(out_1[0], out_b[t])
+
+
+def test_prefill_parity_sampled():
+    cfg = dsgen.PREFILL
+    lo = oracle.LayerOracle(cfg)
+    att = oracle.resample_attempts(cfg, lo)
+    W = synthetic.build_layer(cfg)
+    out, dbg = run_layer(cfg, W, synthetic.build_x(cfg, att))
+    x64 = oracle.as_f64(dsgen.host_x(cfg, att), cfg.x_dtype)
+    L = lo.logits(x64)
+    ids, w = oracle.select(L, cfg.k)
+    check_route_full(dbg, ids, cfg.E)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(cfg.T, 6, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, cfg.T - 1]]))
+    res = oracle.moe_layer(x64[rows], lo.experts(ids[rows]), lo.shared, ids[rows], w[rows], cfg.D,
+                           cfg.E, cfg.F, cfg.Fs)
+    check_close(out[rows], res, PREFILL_TOL)
+
+
+def test_zero_tokens_is_noop(decode1):
+    cfg, lo, att, x64, W = decode1
+    sh = synthetic.shape_of(cfg)
+    out = torch.full((1, cfg.D), 3.0, device="cuda")
+    ws = torch.empty(ds.workspace_bytes(sh, 1), dtype=torch.uint8, device="cuda")
+    ds.layer(sh, W, synthetic.build_x(cfg, att), out, ws, T=0)
+    ds.sync_status()
+    assert torch.all(out == 3.0)
+
+
+def _stack_oracle(cfg, n_layers):
+    """Oracle residual after each of n_layers stack steps (own residual; fp32
+    between layers).  Returns the input and the residual after each layer."""
+    from dataclasses import replace
+    x0 = dsgen.host_x(replace(cfg, x_dtype="f32"))
+    xr, outs = x0.copy(), []
+    for l in range(n_layers):
+        lo = oracle.LayerOracle(cfg, l)
+        r64 = oracle.as_f64(oracle.rmsnorm_bf16(xr), "bf16")
+        if np.any(oracle.min_top_gap(lo.logits(r64), cfg.k) < oracle.GAP):
+            pytest.skip("near-tie in a stack layer's input for this seed")
+        (res, _, _, _) = lo.forward(r64)
+        xr = (xr.astype(np.float64) + res).astype(np.float32)
+        outs.append(xr.copy())
+    return x0, outs
+
+
+def test_stack_parity_by_depth():
+    """The stack  x <- x + layer(bf16(RMSNorm(x)))  at full width, T=8.
+    Depth 1 must meet the decode tolerance on the update.  Each later layer
+    re-rounds its normalised input to bf16, so residual differences at the
+    1e-5 level flip a few bf16 roundings and the difference grows with depth;
+    the bound used is 2e-3 * depth * rms(update)."""
+    cfg = dsgen.STACK
+    n_layers = 3
+    x0, outs = _stack_oracle(cfg, n_layers)
+    Ws = [synthetic.build_layer(cfg, l) for l in range(n_layers)]
+    sh = synthetic.shape_of(cfg)
+    ws = torch.empty(ds.workspace_bytes(sh, cfg.T), dtype=torch.uint8, device="cuda")
+    for depth in range(1, n_layers + 1):
+        x = torch.from_numpy(x0).cuda()
+        ds.stack(sh, Ws[:depth], x, ws)
+        ds.sync_status()
+        upd = x.cpu().numpy().astype(np.float64) - x0
+        r = check_close(upd, outs[depth - 1].astype(np.float64) - x0, DECODE_TOL * depth,
+                        f"stack update at depth {depth}")
+        print(f"stack depth {depth}: max|err|/rms = {r:.2e}")
+
+
+def test_stack_equals_layer_by_layer():
+    """ds_moe_stack is bit-identical to RMSNorm + ds_moe_layer + residual add
+    issued one layer at a time (here 4 layers)."""
+    from dataclasses import replace
+    cfg = dsgen.STACK
+    Ws = [synthetic.build_layer(cfg, l) for l in range(4)]
+    sh = synthetic.shape_of(cfg)
+    ws = torch.empty(ds.workspace_bytes(sh, cfg.T), dtype=torch.uint8, device="cuda")
+    x0 = torch.from_numpy(dsgen.host_x(replace(cfg, x_dtype="f32"))).cuda()
+    xa = x0.clone()
+    ds.stack(sh, Ws, xa, ws)
+    xb = x0.clone()
+    for W in Ws:
+        xb_in = xb.clone()
+        ds.stack(sh, [W], xb, ws)
+        assert not torch.equal(xb, xb_in)
+    ds.sync_status()
+    assert torch.equal(xa, xb)

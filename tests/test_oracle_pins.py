@@ -236,11 +236,17 @@ def test_quantizer_zero_pads_short_rows():
     assert oracle.dequantize(q, 4, 128).shape == (4, 128)
 
 
-def test_quantizer_rejects_non_finite():
+def test_quantizer_rejects_non_finite_and_out_of_domain():
+    for bad in (np.nan, np.inf, -np.inf, 65505.0, -70000.0):
+        x = np.zeros((1, 256), np.float32)
+        x[0, 3] = bad
+        with pytest.raises(ValueError):
+            oracle.quantize(x)
     x = np.zeros((1, 256), np.float32)
-    x[0, 3] = np.nan
-    with pytest.raises(ValueError):
-        oracle.quantize(x)
+    x[0, 3] = -65504.0  # the largest fp16 magnitude is inside the domain
+    q = oracle.quantize(x)
+    # dmin = fp16 >= 65504/15 = 4368, m = 15: the low level is -65520 (half-step bound holds)
+    assert oracle.dequantize(q, 1, 256)[0, 3] == -65520.0
 
 
 # ---------------------------------------------------------------- routing --
