@@ -24,7 +24,8 @@ DS_F32, DS_BF16 = 0, 1
 
 SYMBOLS = ["ds_moe_q2k_bytes", "ds_moe_expert_bytes", "ds_moe_quantize_q2k",
            "ds_moe_dequantize_q2k", "ds_moe_workspace_bytes", "ds_moe_layer",
-           "ds_moe_layer_hostio", "ds_moe_stack", "ds_moe_sync_status", "ds_moe_version"]
+           "ds_moe_layer_hostio", "ds_moe_stack", "ds_moe_sync_status", "ds_moe_version",
+           "ds_moe_layer_noalloc"]
 
 
 class DsMoeError(RuntimeError):
@@ -82,6 +83,9 @@ def lib():
         L.ds_moe_stack.restype = ctypes.c_int
         L.ds_moe_stack.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), ctypes.c_int32,
                                    vp, i64, ctypes.c_float, vp, sz, vp, cp, sz]
+        L.ds_moe_layer_noalloc.restype = ctypes.c_int
+        L.ds_moe_layer_noalloc.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64,
+                                           vp, vp, cp, sz]
         L.ds_moe_sync_status.restype = ctypes.c_int
         L.ds_moe_sync_status.argtypes = [vp, cp, sz]
         L.ds_moe_version.restype = ctypes.c_char_p
@@ -185,6 +189,14 @@ def layer_hostio(shape: MoEShape, weights: MoEWeights, x_host, out_host, workspa
     _call(lib().ds_moe_layer_hostio, ctypes.byref(shape.c()), ctypes.byref(weights.c()),
           x_host.data_ptr(), x_host.shape[0], out_host.data_ptr(), workspace.data_ptr(),
           workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def layer_noalloc(shape: MoEShape, weights: MoEWeights, x, out, stream=None, T: int | None = None):
+    """layer() without a workspace: the library's static device scratch is used
+    (for callers that cannot allocate; at most 8 MiB of scratch, serialise calls)."""
+    T = x.shape[0] if T is None else T
+    _call(lib().ds_moe_layer_noalloc, ctypes.byref(shape.c()), ctypes.byref(weights.c()),
+          x.data_ptr(), T, out.data_ptr(), _stream(stream))
 
 
 def stack(shape: MoEShape, layers, x, workspace, eps: float = 1e-6, stream=None):

@@ -159,6 +159,25 @@ int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_
                  float *x, int64_t T, float eps, void *workspace, size_t workspace_bytes,
                  void *stream, char *err, size_t errlen);
 
+/* ds_moe_layer for callers that cannot allocate device memory where they
+ * call the layer -- for example code being captured into a CUDA graph, where
+ * allocation calls are not allowed, or a plugin whose host program owns all
+ * device memory through its own allocator.  It takes no workspace: its
+ * scratch is a static 8 MiB device array inside this library, allocated on
+ * each GPU when the library is loaded there and held until the process
+ * exits.  The pages have no counterpart to this entry point.
+ *   x, T, out, stream, err: as for ds_moe_layer (no debug outputs).
+ *   Rejects, with DS_ERR_INVALID_ARG and a message, any T whose
+ *   ds_moe_workspace_bytes exceeds 8 MiB (about 40 tokens at the 4096/256/6/
+ *   2048 shape).  Allocates nothing: no cudaMalloc, no cudaFree.
+ *   The first call on a device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   Every call reuses the same array and leaves its contents behind; the
+ *   call clears what must start at zero.  Calls that overlap on the GPU
+ *   (other streams or threads) race on the array: serialise them. */
+int ds_moe_layer_noalloc(const ds_moe_shape *shape, const ds_moe_weights *weights, const void *x,
+                         int64_t T, float *out, void *stream, char *err, size_t errlen);
+
 /* Synchronise `stream`, then read and clear this device's sticky status
  * word.  Returns DS_OK, DS_ERR_TIMEOUT or DS_ERR_DEVICE_CHECK (with a message
  * naming the check), or DS_ERR_CUDA if the stream itself failed. */

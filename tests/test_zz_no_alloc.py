@@ -1,0 +1,76 @@
+"""ds_moe_layer_noalloc: the layer for callers that cannot allocate device
+memory where they run it (a stream being captured into a CUDA graph, a plugin
+whose host program owns all device memory).  Its scratch is a static device
+array inside the library, so the caller passes only inputs and outputs.
+
+The check: its output matches ds_moe_layer (caller workspace) within the
+decode tolerance, on two calls in a row (the second with another batch, so
+contents left in the shared array by the first call must not matter), and a
+batch too large for the static array is refused with a clear error.
+
+This file is collected last on purpose; it also passes on its own in a fresh
+process.
+"""
+import numpy as np
+import pytest
+
+import dsgen
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import bit_quantized_routed_router_gb300 as ds  # noqa: E402
+from bit_quantized_routed_router_gb300 import synthetic  # noqa: E402
+
+TOL = 2e-3  # the decode tolerance used by the parity tests
+
+
+@pytest.fixture(scope="module")
+def layer():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_quantized_routed_router_gb300 import build
+    build.build()
+    cfg = dsgen.DECODE1
+    return cfg, synthetic.build_layer(cfg)
+
+
+def with_workspace(cfg, W, x):
+    sh = synthetic.shape_of(cfg)
+    ws = torch.empty(ds.workspace_bytes(sh, x.shape[0]), dtype=torch.uint8, device="cuda")
+    out = torch.empty((x.shape[0], cfg.D), dtype=torch.float32, device="cuda")
+    ds.layer(sh, W, x, out, ws)
+    ds.sync_status()
+    return out.cpu().numpy()
+
+
+def test_noalloc_matches_workspace_entry_point_twice(layer):
+    cfg, W = layer
+    sh = synthetic.shape_of(cfg)
+    from dataclasses import replace
+    for T, seed_layer in ((8, 0), (1, 3)):  # two calls in a row, different batches
+        c = replace(cfg, T=T)
+        x = synthetic.build_x(c, layer=seed_layer)
+        ref = with_workspace(c, W, x)
+        out = torch.full((T, cfg.D), float("nan"), dtype=torch.float32, device="cuda")
+        ds.layer_noalloc(sh, W, x, out)
+        ds.sync_status()
+        got = out.cpu().numpy()
+        rms = float(np.sqrt(np.mean(ref.astype(np.float64) ** 2)))
+        err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+        assert np.isfinite(got).all()
+        assert err <= TOL * rms, f"T={T}: max|err| {err:.3e} > {TOL} * rms {rms:.3e}"
+
+
+def test_noalloc_refuses_batches_beyond_its_scratch(layer):
+    cfg, W = layer
+    sh = synthetic.shape_of(cfg)
+    T = 64  # needs ~12.6 MB of scratch at this shape; the static array holds 8 MiB
+    assert ds.workspace_bytes(sh, T) > 8 << 20
+    x = torch.zeros((T, cfg.D), dtype=torch.int16, device="cuda")
+    out = torch.zeros((T, cfg.D), dtype=torch.float32, device="cuda")
+    with pytest.raises(ds.DsMoeError) as ei:
+        ds.layer_noalloc(sh, W, x, out)
+    assert ei.value.code == ds.DS_ERR_INVALID_ARG
+    assert "static scratch" in str(ei.value)
+    ds.sync_status()
