@@ -131,13 +131,19 @@ int check_weights(const Shape &sh, const ds_moe_weights *W, char *err, size_t er
 // One layer on device buffers: route, expert FFNs, combine into out.
 int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *out, bool accumulate,
               const Work &wk, const ds_moe_debug *dbg, cudaStream_t s, char *err, size_t errlen) {
-  cudaError_t e = cudaMemsetAsync(wk.ctrl, 0, 256, s);
-  if (e != cudaSuccess) return cuda_fail(err, errlen, e, "workspace control reset");
-  if ((e = launch_route(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
-  if ((e = launch_decode_ffn(sh, W, x, wk, s)) != cudaSuccess)
-    return cuda_fail(err, errlen, e, "expert FFN");
-  if ((e = launch_combine(sh, wk, out, accumulate, s)) != cudaSuccess)
-    return cuda_fail(err, errlen, e, "combine");
+  cudaError_t e;
+  if (fused_decode_supported(sh, wk.T)) {
+    if ((e = launch_decode_fused(sh, W, x, wk, out, accumulate, s)) != cudaSuccess)
+      return cuda_fail(err, errlen, e, "fused decode layer");
+  } else {
+    if ((e = cudaMemsetAsync(wk.ctrl, 0, 256, s)) != cudaSuccess)
+      return cuda_fail(err, errlen, e, "workspace control reset");
+    if ((e = launch_route(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
+    if ((e = launch_decode_ffn(sh, W, x, wk, s)) != cudaSuccess)
+      return cuda_fail(err, errlen, e, "expert FFN");
+    if ((e = launch_combine(sh, wk, out, accumulate, s)) != cudaSuccess)
+      return cuda_fail(err, errlen, e, "combine");
+  }
   if (dbg) {
     const int64_t P = wk.T * sh.k;
     struct { void *dst; const void *src; size_t n; } cp[] = {

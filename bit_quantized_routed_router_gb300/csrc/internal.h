@@ -43,6 +43,11 @@ cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x
 // Decode path: grouped dequantising GEMVs and the combine.
 cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const void *x,
                               const Work &wk, cudaStream_t s);
+// Decode path for T <= 8: the whole layer in one persistent kernel (writes or
+// accumulates into out, and fills the route arrays of the workspace).
+bool fused_decode_supported(const Shape &sh, int64_t T);
+cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const void *x,
+                                const Work &wk, float *out, bool accumulate, cudaStream_t s);
 cudaError_t launch_combine(const Shape &sh, const Work &wk, float *out, bool accumulate,
                            cudaStream_t s);
 

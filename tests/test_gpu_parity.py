@@ -195,6 +195,24 @@ def test_tiny_variants(variant):
     layer_parity(c, DECODE_TOL, scale)
 
 
+def _small(T, Fs, k=2, E=16, dtype="f32"):
+    from dataclasses import replace
+    return replace(dsgen.TINY, name=f"small D=1024 F=1024 T={T} Fs={Fs} k={k} E={E} {dtype}", T=T,
+                   D=1024, F=1024, E=E, k=k, Fs=Fs, shared_sigma=0.02, x_dtype=dtype,
+                   router_dtype=dtype)
+
+
+@pytest.mark.parametrize("T,Fs,k,E,dtype", [(1, 0, 2, 16, "f32"), (2, 256, 2, 16, "f32"),
+                                            (1, 512, 6, 16, "bf16"), (1, 0, 16, 16, "f32"),
+                                            (2, 1024, 4, 40, "bf16"), (1, 128, 1, 3, "f32"),
+                                            (3, 256, 2, 16, "f32"), (8, 0, 16, 16, "f32")])
+def test_small_decode_variants(T, Fs, k, E, dtype):
+    """Decode-sized batches at a reduced width: the single-kernel path (T <= 2
+    here) and the grouped path, including k = E, one expert per token, odd E
+    and no shared expert."""
+    layer_parity(_small(T, Fs, k, E, dtype), DECODE_TOL)
+
+
 def test_tiny_prefill_sized_batch():
     """A batch beyond the decode size takes the large-batch route kernels."""
     from dataclasses import replace
@@ -237,14 +255,32 @@ def test_decode32_zipf_parity():
 
 
 def test_batch_invariance_decode(decode1):
-    """A token computed alone equals the same token inside a decode batch, bit for bit."""
+    """Within one path a token's result does not depend on its batch: tokens of
+    an 8-token batch equal the same tokens in a 3-token batch bit for bit
+    (grouped path), and the single-token path agrees with both at tolerance."""
     cfg, lo, att, x64, W = decode1
     from dataclasses import replace
     c8 = replace(cfg, T=8)
     xb = synthetic.build_x(c8)
     out_b, _ = run_layer(c8, W, xb)
+    out_3, _ = run_layer(replace(cfg, T=3), W, xb[2:5].contiguous())
+    assert np.array_equal(out_3, out_b[2:5])
     for t in (0, 5):
         out_1, _ = run_layer(cfg, W, xb[t:t + 1].contiguous())
+        check_close(out_1[0].astype(np.float64), out_b[t].astype(np.float64), DECODE_TOL,
+                    "single-token path vs batched path")
+
+
+def test_batch_invariance_single_kernel_path():
+    """Single-kernel path (T <= 2 at width 1024): a token alone equals itself
+    inside a 2-token batch, bit for bit."""
+    cfg = _small(2, 256, 2, 16, "bf16")
+    from dataclasses import replace
+    W = synthetic.build_layer(cfg)
+    xb = synthetic.build_x(cfg)
+    out_b, _ = run_layer(cfg, W, xb)
+    for t in (0, 1):
+        out_1, _ = run_layer(replace(cfg, T=1), W, xb[t:t + 1].contiguous())
         assert np.array_equal(out_1[0], out_b[t])
 
 
