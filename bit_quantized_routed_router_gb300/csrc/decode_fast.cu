@@ -1,0 +1,769 @@
+// Decode path for a few tokens (T*k <= 32, e.g. one token at 4096/256/6/2048):
+// three kernels chained with programmatic dependent launch (PDL).
+//
+// What it computes is the layer of "Understanding Dwarf Star" 5.3.2/5.3.7
+// (router -> top-k -> gate/up -> SiLU(gate)*up -> down -> weighted sum, plus
+// the always-active shared expert of 5.3.4), with the routed weights read as
+// Q2_K blocks (3.3.3) and dequantised on the fly (2.8.1-2.8.2).
+//
+//   K1 route_kernel   router logits (a quarter of a row per warp).
+//   K2 gateup_kernel  one warp per CTA waits for K1 and selects the top-k and
+//                     builds the route (each CTA its own copy; CTA 0 publishes
+//                     it), while the other warps start on the shared gate/up
+//                     quarter-rows (no route needed: they overlap K1 through
+//                     PDL); then one warp per routed gate/up row pair ->
+//                     h = SiLU(g) * u.
+//   K3 down_kernel    one warp per output row: shared down row, every used
+//                     expert's down row, and the combine
+//                     out = y_shared + sum_j w_j y_j (slot order j).
+//
+// Q2_K rows are read straight from global memory (every byte once; a lane's
+// 4-byte words of one 84-byte block), all loads of an item issued before any
+// use.  Dot products with Q2_K rows are exact integer sums: activations are
+// turned into 16-bit fixed point per 256-element block, X = rint(v / step),
+// step = 2^(e-15) with max |v| < 2^e, split in a signed high byte and an
+// unsigned low byte, and sum_j q_j X_j is formed with dp4a; per lane the
+// integers sum_s sc_s S_s and sum_s m_s sum(X) are accumulated exactly and
+// converted once: w.x = step * (d * sum sc S - dmin * sum m X).  The only
+// rounding beyond fp32 is that fixed point (|err| <= 2^-16 of the block's
+// largest |v| per element).
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dsm {
+namespace {
+
+constexpr int PMAXD = 32;          // token-expert pairs this path serves (one per lane)
+constexpr int NW2 = 12, NW3 = 12;  // warps per CTA of K2 and K3
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+
+enum { C_NUSED = 1 };  // control word: experts with tokens (written with the route)
+
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------- fixed point planes --
+// For a vector of nb blocks (nsb = 16 nb sub-blocks): nine planes of nsb words
+// (hi0..3, lo0..3, SX) then nb steps.  Word i of hi (lo) for sub-block sb
+// holds in byte c the high (low) byte of X_{16 sb + 4c + i}: the byte order of
+// (codes >> 2i) & 0x03030303.  Within a plane the words are stored in the
+// order lanes read them, so every vector load is conflict-free.
+// Lane map of a row of nb blocks (nb = 2 SPL): LPB = 16 / SPL lanes per block;
+// lane l takes block l / LPB, sub-blocks SPL (l % LPB) + i, i < SPL.
+template <int SPL>
+struct LaneMap {
+  static constexpr int LPB = 16 / SPL;
+  static constexpr int Q = SPL < 4 ? SPL : 4;
+  __device__ static __forceinline__ int off(int lane, int i) {
+    return (i / Q) * (32 * Q) + lane * Q + (i % Q);
+  }
+};
+
+// One block per half-warp (lanes 0-15 and 16-31 convert one block each);
+// lane & 15 holds sub-block s's 16 values.
+template <int SPL>
+__device__ __forceinline__ void digitize_block(const float v[16], int b, uint32_t *planes,
+                                              float *steps, int nsb) {
+  const int lane = threadIdx.x & 31, s = lane & 15;
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  int e = 0;
+  if (m > 0.f) frexpf(m, &e);  // m < 2^e
+  const float inv = m > 0.f ? ldexpf(1.0f, 15 - e) : 0.f;
+  uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+  int sx = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    int X = __float2int_rn(v[j] * inv);  // exact scaling by a power of two
+    X = max(-32767, min(32767, X));
+    sx += X;
+    const int i = j & 3, c = 8 * (j >> 2);
+    hi[i] |= ((uint32_t)(X >> 8) & 0xFFu) << c;
+    lo[i] |= ((uint32_t)X & 0xFFu) << c;
+  }
+  const int lr = b * LaneMap<SPL>::LPB + s / SPL;  // the lane that reads this sub-block
+  const int o = LaneMap<SPL>::off(lr, s % SPL);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    planes[i * nsb + o] = hi[i];
+    planes[(4 + i) * nsb + o] = lo[i];
+  }
+  planes[8 * nsb + o] = (uint32_t)sx;
+  if (s == 0) steps[b] = m > 0.f ? ldexpf(1.0f, e - 15) : 0.f;
+}
+
+template <int Q>
+__device__ __forceinline__ void lds_words(const uint32_t *p, uint32_t w[Q]) {
+  if (Q == 4) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if (Q == 2) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+    w[0] = p[0];
+  }
+}
+
+// This lane's words of one Q2_K row (global): SPL code words, the scale bytes
+// of its sub-blocks, and d/dmin.
+template <int SPL>
+struct RowPart {
+  uint32_t codes[SPL];
+  uint32_t scm[(SPL + 3) / 4];
+  uint32_t dd;
+};
+
+template <int SPL>
+__device__ __forceinline__ void load_row(const uint8_t *row, RowPart<SPL> &r) {
+  const int lane = threadIdx.x & 31;
+  constexpr int LPB = 16 / SPL;
+  const uint8_t *blk = row + (lane / LPB) * QB;
+  const int s0 = SPL * (lane % LPB);
+  const uint32_t *cw = reinterpret_cast<const uint32_t *>(blk + 16 + 4 * s0);
+#pragma unroll
+  for (int i = 0; i < SPL; ++i) r.codes[i] = __ldcs(cw + i);  // streamed once
+  if (SPL >= 4) {
+    const uint32_t *sw = reinterpret_cast<const uint32_t *>(blk + s0);
+#pragma unroll
+    for (int i = 0; i < (SPL + 3) / 4; ++i) r.scm[i] = __ldcs(sw + i);
+  } else {  // s0 is not 4-aligned: take the word holding the bytes
+    const uint32_t w = __ldcs(reinterpret_cast<const uint32_t *>(blk + (s0 & ~3)));
+    r.scm[0] = w >> (8 * (s0 & 3));
+  }
+  r.dd = __ldcs(reinterpret_cast<const uint32_t *>(blk + 80));
+}
+
+// sum over this lane's sub-blocks of (row) . (planes): exact integers, one
+// conversion per lane.
+template <int SPL>
+__device__ __forceinline__ float row_dot(const RowPart<SPL> &r, const uint32_t *planes,
+                                         const float *steps, int nsb) {
+  using M = LaneMap<SPL>;
+  constexpr int Q = M::Q;
+  const int lane = threadIdx.x & 31;
+  int accq = 0, accm = 0;
+#pragma unroll
+  for (int g = 0; g < SPL / Q; ++g) {
+    uint32_t hi[4][Q], lo[4][Q], sx[Q];
+    const int o = g * (32 * Q) + lane * Q;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      lds_words<Q>(planes + i * nsb + o, hi[i]);
+      lds_words<Q>(planes + (4 + i) * nsb + o, lo[i]);
+    }
+    lds_words<Q>(planes + 8 * nsb + o, sx);
+#pragma unroll
+    for (int k = 0; k < Q; ++k) {
+      const int sub = g * Q + k;
+      const uint32_t codes = r.codes[sub];
+      const int scm = (r.scm[sub >> 2] >> (8 * (sub & 3))) & 0xFF;
+      const uint32_t q0 = codes & 0x03030303u, q1 = (codes >> 2) & 0x03030303u;
+      const uint32_t q2 = (codes >> 4) & 0x03030303u, q3 = (codes >> 6) & 0x03030303u;
+      int sh = __dp4a((int)q0, (int)hi[0][k], 0);
+      sh = __dp4a((int)q1, (int)hi[1][k], sh);
+      sh = __dp4a((int)q2, (int)hi[2][k], sh);
+      sh = __dp4a((int)q3, (int)hi[3][k], sh);
+      unsigned sl = __dp4a(q0, lo[0][k], 0u);
+      sl = __dp4a(q1, lo[1][k], sl);
+      sl = __dp4a(q2, lo[2][k], sl);
+      sl = __dp4a(q3, lo[3][k], sl);
+      accq += (scm & 15) * (sh * 256 + (int)sl);  // sc_s * sum_j q_j X_j
+      accm += (scm >> 4) * (int)sx[k];            // m_s * sum_j X_j
+    }
+  }
+  const float d = fp16_to_f32((uint16_t)(r.dd & 0xFFFF)), dmin = fp16_to_f32((uint16_t)(r.dd >> 16));
+  return steps[lane / M::LPB] * fmaf(d, (float)accq, -dmin * (float)accm);
+}
+
+__device__ __forceinline__ void bf16x8(uint4 v, float f[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Butterfly sums of N independent values (all lanes end with the totals);
+// the N shuffles of a level are independent, so they pipeline.
+template <int N>
+__device__ __forceinline__ void warp_sum_n(float v[N]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+}
+
+__device__ __forceinline__ int shfl(int v, int l) { return __shfl_sync(0xffffffffu, v, l); }
+__device__ __forceinline__ float shflf(float v, int l) { return __shfl_sync(0xffffffffu, v, l); }
+
+struct Args {
+  int D, E, F, Fs, k, T;
+  float routed_scale;
+  const void *router_w;
+  int router_f32;
+  const float *bias;
+  const uint16_t *sg, *su, *sd;
+  const uint8_t *experts;
+  int64_t expert_bytes, gate_bytes;
+  const void *x;
+  int x_f32;
+  float *logits;
+  int32_t *ids;
+  float *w;
+  int32_t *counts, *offsets, *perm, *pos, *used;
+  float *h;    // [P][F] routed activations, perm order
+  float *pgu;  // [2][4][T][Fs] shared gate / up partial sums (per quarter of n_embd)
+  unsigned *ctrl;
+  float *out;
+  int accumulate;
+  unsigned *status;
+  int n_slots;
+};
+
+template <typename T>
+__device__ __forceinline__ void ld8(const T *p, float v[8]);
+template <>
+__device__ __forceinline__ void ld8<float>(const float *p, float v[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void ld8<uint16_t>(const uint16_t *p, float v[8]) {
+  bf16x8(__ldg(reinterpret_cast<const uint4 *>(p)), v);
+}
+
+// ===================================================================== K1 ==
+
+// Router logits: two expert rows per CTA, a quarter of n_embd per warp.
+template <typename TX, typename TW>
+__global__ void __launch_bounds__(256) route_kernel(const Args a) {
+  pdl_trigger();  // the gate/up kernel may start its route-free work now
+  __shared__ float part[8][4];  // [warp][token] partial logits
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // two expert rows per CTA, a quarter of n_embd per warp, loads issued up front
+  const int e = blockIdx.x * 2 + (warp >> 2), qd = warp & 3, len = a.D / 4, c0 = qd * len;
+  if (e < a.E) {
+    const TW *row = (const TW *)a.router_w + (int64_t)e * a.D + c0;
+    for (int t = 0; t < a.T; ++t) {
+      const TX *xr = (const TX *)a.x + (int64_t)t * a.D + c0;
+      float acc = 0.f;
+#pragma unroll 4
+      for (int d = 8 * lane; d < len; d += 256) {
+        float wv[8], xv[8];
+        ld8<TW>(row + d, wv);
+        ld8<TX>(xr + d, xv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = fmaf(xv[i], wv[i], acc);
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) part[warp][t] = acc;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 2 * a.T) {
+    const int r = threadIdx.x / a.T, t = threadIdx.x % a.T, ee = blockIdx.x * 2 + r;
+    if (ee < a.E) {
+      const float v = ((part[4 * r][t] + part[4 * r + 1][t]) + part[4 * r + 2][t]) + part[4 * r + 3][t];
+      a.logits[(int64_t)t * a.E + ee] = v + (a.bias ? a.bias[ee] : 0.f);
+    }
+  }
+}
+
+// The route as the warps of K2/K3 keep it in registers: lane p holds pair p,
+// lane u holds used expert u.
+struct RouteCache {
+  int nu, perm, used, base, cnt;
+  float w;
+};
+
+// Selection and route by one warp (T * k <= 32): top-k by logit, ties to the
+// lower index, weights = routed_scale * softmax over the selected logits; the
+// stable route puts pair p at #(pairs with a smaller expert, or the same
+// expert and a smaller p).  Returns the calling lane's RouteCache entries; with
+// publish, also writes ids, w, counts, offsets, perm, pos and used.
+__device__ RouteCache select_route_warp(const Args &a, bool publish) {
+  const int lane = threadIdx.x & 31, P = a.T * a.k;
+  int my_id = 0;     // lane p: expert of pair p
+  float my_lg = 0.f; // lane p: its logit
+  for (int t = 0; t < a.T; ++t) {
+    const float *L = a.logits + (int64_t)t * a.E;
+    float lv[32];
+#pragma unroll
+    for (int ii = 0; ii < 32; ++ii) lv[ii] = lane + 32 * ii < a.E ? __ldcg(L + lane + 32 * ii) : -INFINITY;
+    uint32_t taken = 0;
+    for (int j = 0; j < a.k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int ii = 0; ii < 32; ++ii) {
+        const int ee = lane + 32 * ii;
+        if (ee < a.E && !(taken & (1u << ii)) && (lv[ii] > bv || (lv[ii] == bv && ee < bi))) { bv = lv[ii]; bi = ee; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (bi < 0 || bi >= a.E) { if (lane == 0 && publish) flag(a.status, ST_BAD_ID); bi = 0; }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == t * a.k + j) { my_id = bi; my_lg = bv; }
+    }
+  }
+  // weights: softmax over each token's selected logits
+  const int tok = lane / max(a.k, 1), j0 = tok * a.k;
+  const float m0 = __shfl_sync(0xffffffffu, my_lg, min(j0, 31));
+  float ex = lane < P ? __expf(my_lg - m0) : 0.f;
+  float den = 0.f;
+  for (int j = 0; j < a.k; ++j) den += __shfl_sync(0xffffffffu, ex, min(j0 + j, 31));
+  const float my_w = lane < P ? a.routed_scale * (ex / den) : 0.f;
+  // ranks
+  int rank = 0, first = 1, ui = 0;
+  for (int q = 0; q < P; ++q) {
+    const int eq = __shfl_sync(0xffffffffu, my_id, q);
+    rank += (eq < my_id) || (eq == my_id && q < lane);
+    if (eq == my_id && q < lane) first = 0;
+  }
+  const unsigned firsts = __ballot_sync(0xffffffffu, lane < P && first);
+  for (int q = 0; q < P; ++q) {  // distinct experts below mine
+    const int eq = __shfl_sync(0xffffffffu, my_id, q);
+    ui += ((firsts >> q) & 1u) && eq < my_id;
+  }
+  RouteCache r;
+  r.nu = __popc(firsts);
+  // lane p learns perm[p]: the pair whose rank is p
+  int perm_p = 0;
+  for (int q = 0; q < P; ++q) {
+    const int rq = __shfl_sync(0xffffffffu, rank, q);
+    if (rq == lane) perm_p = q;
+  }
+  r.perm = perm_p;
+  r.w = my_w;
+  // lane u learns used[u], its first position and its pair count
+  int used_u = 0, base_u = 0, cnt_u = 0;
+  for (int q = 0; q < P; ++q) {
+    const int uq = __shfl_sync(0xffffffffu, ui, q), eq = __shfl_sync(0xffffffffu, my_id, q);
+    const int rq = __shfl_sync(0xffffffffu, rank, q);
+    if (((firsts >> q) & 1u) && uq == lane) { used_u = eq; base_u = rq; }
+  }
+  for (int q = 0; q < P; ++q) {
+    const int eq = __shfl_sync(0xffffffffu, my_id, q);  // every lane shuffles
+    cnt_u += (lane < r.nu && eq == used_u) ? 1 : 0;
+  }
+  r.used = used_u;
+  r.base = base_u;
+  r.cnt = cnt_u;
+  if (publish) {
+    if (lane < P) {
+      a.ids[lane] = my_id;
+      a.w[lane] = my_w;
+      a.perm[rank] = lane;
+      a.pos[lane] = rank;
+    }
+    if (lane < r.nu) a.used[lane] = used_u;
+    for (int e0 = 0; e0 <= a.E; e0 += 32) {  // warp-uniform trip count (shuffles inside)
+      const int e = e0 + lane;
+      int lt = 0, eqc = 0;
+      for (int q = 0; q < P; ++q) {
+        const int eq = __shfl_sync(0xffffffffu, my_id, q);
+        lt += eq < e;
+        eqc += eq == e;
+      }
+      if (e <= a.E) a.offsets[e] = lt;
+      if (e < a.E) a.counts[e] = eqc;
+    }
+    if (lane == 0) {
+      a.used[a.E] = r.nu;
+      a.ctrl[C_NUSED] = (unsigned)r.nu;
+    }
+  }
+  return r;
+}
+
+// Reads the route published in global memory; any entry out of range (which
+// a correct route never has) is replaced by a harmless value and flagged.
+__device__ __forceinline__ RouteCache load_route(const Args &a) {
+  const int lane = threadIdx.x & 31, P = a.T * a.k;
+  RouteCache r;
+  r.nu = (int)__ldcg((const int *)(a.ctrl + C_NUSED));
+  bool bad = r.nu < 0 || r.nu > P;
+  if (bad) r.nu = 0;
+  r.perm = lane < P ? __ldcg(a.perm + lane) : 0;
+  r.w = lane < P ? __ldcg(a.w + lane) : 0.f;
+  r.used = lane < r.nu ? __ldcg(a.used + lane) : 0;
+  if (r.used < 0 || r.used >= a.E) { bad = true; r.used = 0; }
+  r.base = lane < r.nu ? __ldcg(a.offsets + r.used) : 0;
+  r.cnt = lane < r.nu ? __ldcg(a.offsets + r.used + 1) - r.base : 0;
+  if (r.perm < 0 || r.perm >= P || r.base < 0 || r.cnt < 0 || r.base + r.cnt > P) {
+    bad = true;
+    r.perm = 0; r.base = 0; r.cnt = 0;
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) flag(a.status, ST_BAD_COUNT);
+    r.nu = 0;  // compute nothing routed rather than index with bad data
+  }
+  return r;
+}
+
+// ===================================================================== K2 ==
+
+template <int SPL>
+__global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
+  pdl_trigger();  // every CTA of this grid is resident: the down kernel may queue
+  extern __shared__ __align__(16) uint32_t xpl[];  // [T] planes + steps
+  __shared__ int s_rt[5][32];
+  __shared__ float s_w[32];
+  __shared__ volatile int s_ready;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = a.D / QK, nsb = a.D / 16, xw = 9 * nsb + nb;
+  if (threadIdx.x == 0) s_ready = 0;
+  for (int u = warp; u < (a.T * nb + 1) / 2; u += NW2) {
+    const int bi = min(2 * u + (lane >> 4), a.T * nb - 1);
+    const int t = bi / nb, b = bi % nb;
+    const int64_t e0 = (int64_t)t * a.D + QK * b + 16 * (lane & 15);
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      v[j] = a.x_f32 ? __ldg((const float *)a.x + e0 + j) : bf16_to_f32(__ldg((const uint16_t *)a.x + e0 + j));
+    digitize_block<SPL>(v, b, xpl + t * xw, reinterpret_cast<float *>(xpl + t * xw + 9 * nsb), nsb);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // every CTA selects and routes on its own (a few hundred logits); CTA 0
+    // also publishes the route for the down kernel and the debug outputs
+    pdl_wait();  // the router logits are complete and visible
+    const RouteCache r = select_route_warp(a, blockIdx.x == 0);
+    s_rt[0][lane] = r.perm; s_rt[1][lane] = r.used; s_rt[2][lane] = r.base; s_rt[3][lane] = r.cnt;
+    s_rt[4][lane] = r.nu;
+    s_w[lane] = r.w;
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) s_ready = 1;
+  }
+
+  const int n_sh = a.Fs > 0 ? 4 * a.Fs : 0;    // shared items: (row, quarter of n_embd)
+  const int n_items = n_sh + a.n_slots * a.F;  // then one per routed (slot, row)
+  const int gw = warp * gridDim.x + blockIdx.x, nwork = gridDim.x * NW2;
+  const int rb = nb * QB;
+  bool have_route = false;
+  RouteCache rc{0, 0, 0, 0, 0, 0.f};
+  // L2 prefetch (bulk-copy engine, lane 0) of item i's bytes; every lane calls
+  // it (the routed address comes from a shuffle)
+  auto prefetch = [&](int i) {
+    if (i >= n_items) return;
+    if (i < n_sh) {
+      if (lane == 0) {
+        const int f = i >> 2, q = i & 3, len = a.D / 4;
+        bulk_prefetch_l2(a.sg + (int64_t)f * a.D + q * len, (uint32_t)len * 2u);
+        bulk_prefetch_l2(a.su + (int64_t)f * a.D + q * len, (uint32_t)len * 2u);
+      }
+    } else if (have_route) {
+      const int r = i - n_sh, slot = r / a.F, f = r % a.F;
+      const int e = shfl(rc.used, min(slot, 31));
+      if (slot < rc.nu && lane == 0) {
+        const uint8_t *g = a.experts + (int64_t)e * a.expert_bytes + (int64_t)f * rb;
+        bulk_prefetch_l2(g, (uint32_t)rb);
+        bulk_prefetch_l2(g + a.gate_bytes, (uint32_t)rb);
+      }
+    }
+  };
+  prefetch(gw);
+  prefetch(gw + nwork);
+  for (int it = gw; it < n_items; it += nwork) {
+    if (it >= n_sh && !have_route) {
+      int ok = 1;
+      if (lane == 0) {  // bounded wait for this CTA's route
+        const uint64_t t0 = globaltimer_ns();
+        while (!s_ready) {
+          if (globaltimer_ns() - t0 > 2000000000ull) { flag(a.status, ST_TIMEOUT); ok = 0; break; }
+          __nanosleep(64);
+        }
+      }
+      if (!shfl(ok, 0)) return;
+      __syncwarp();
+      rc.perm = s_rt[0][lane]; rc.used = s_rt[1][lane]; rc.base = s_rt[2][lane]; rc.cnt = s_rt[3][lane];
+      rc.nu = s_rt[4][lane]; rc.w = s_w[lane];
+      have_route = true;
+      prefetch(it + nwork);  // routed items could not be prefetched before
+    }
+    prefetch(it + 2 * nwork);
+    if (it < n_sh) {
+      const int f = it >> 2, q = it & 3, len = a.D / 4, c0 = q * len;
+      const uint16_t *gr = a.sg + (int64_t)f * a.D + c0, *ur = a.su + (int64_t)f * a.D + c0;
+      float gu[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // gate[0..3], up[0..3] (T <= 4)
+#pragma unroll 4
+      for (int c = 8 * lane; c < len; c += 256) {
+        float gf[8], uf[8];
+        bf16x8(__ldcs(reinterpret_cast<const uint4 *>(gr + c)), gf);
+        bf16x8(__ldcs(reinterpret_cast<const uint4 *>(ur + c)), uf);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (t >= a.T) break;
+          float xf[8];
+          if (a.x_f32) ld8<float>((const float *)a.x + (int64_t)t * a.D + c0 + c, xf);
+          else ld8<uint16_t>((const uint16_t *)a.x + (int64_t)t * a.D + c0 + c, xf);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) { gu[t] = fmaf(gf[i], xf[i], gu[t]); gu[4 + t] = fmaf(uf[i], xf[i], gu[4 + t]); }
+        }
+      }
+      warp_sum_n<8>(gu);
+      if (lane < 2 * a.T) {  // lane = matrix * T + token
+        const int m = lane / a.T, t = lane % a.T;
+        a.pgu[((int64_t)(m * 4 + q) * a.T + t) * a.Fs + f] = gu[4 * m + t];
+      }
+      continue;
+    }
+    const int r = it - n_sh, slot = r / a.F, f = r % a.F;
+    if (slot >= rc.nu) continue;
+    const int e = shfl(rc.used, slot), base = shfl(rc.base, slot), n = shfl(rc.cnt, slot);
+    const uint8_t *grow = a.experts + (int64_t)e * a.expert_bytes + (int64_t)f * rb;
+    RowPart<SPL> gp, up;
+    load_row<SPL>(grow, gp);
+    load_row<SPL>(grow + a.gate_bytes, up);
+    for (int j = 0; j < n; ++j) {
+      const int t = shfl(rc.perm, base + j) / a.k;
+      const uint32_t *pl = xpl + t * xw;
+      const float *st = reinterpret_cast<const float *>(pl + 9 * nsb);
+      float gu[2] = {row_dot<SPL>(gp, pl, st, nsb), row_dot<SPL>(up, pl, st, nsb)};
+      warp_sum_n<2>(gu);
+      if (lane == 0) a.h[(int64_t)(base + j) * a.F + f] = silu(gu[0]) * gu[1];
+    }
+  }
+}
+
+// ===================================================================== K3 ==
+
+template <int SPL>
+__global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
+  pdl_wait();  // gate/up (and through it the route) complete and visible
+  extern __shared__ __align__(16) uint32_t hpl[];  // [P] planes + steps, then hs [T][Fs]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = a.F / QK, nsb = a.F / 16, hw = 9 * nsb + nb;
+  const int P = a.T * a.k;
+  float *hs = reinterpret_cast<float *>(hpl + P * hw);
+  const RouteCache rc = load_route(a);
+  // h of every pair in fixed point (perm order), and the shared activations
+  for (int u = warp; u < (P * nb + 1) / 2; u += NW3) {
+    const int bi = min(2 * u + (lane >> 4), P * nb - 1);
+    const int q = bi / nb, b = bi % nb;
+    const float4 *src = reinterpret_cast<const float4 *>(a.h + (int64_t)q * a.F + QK * b + 16 * (lane & 15));
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 f4 = __ldcg(src + j);
+      v[4 * j] = f4.x; v[4 * j + 1] = f4.y; v[4 * j + 2] = f4.z; v[4 * j + 3] = f4.w;
+    }
+    digitize_block<SPL>(v, b, hpl + q * hw, reinterpret_cast<float *>(hpl + q * hw + 9 * nsb), nsb);
+  }
+  {
+    // shared activations: hs = SiLU(sum of gate quarters) * (sum of up quarters),
+    // quarters summed in a fixed order; all loads of a thread issued first
+    constexpr int PER = 8;  // elements per thread and pass
+    for (int i0 = threadIdx.x; i0 < a.T * a.Fs; i0 += PER * blockDim.x) {
+      float g[PER][4], u[PER][4];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int i = i0 + k * blockDim.x;
+        const int t = i / max(a.Fs, 1), f = i % max(a.Fs, 1);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          g[k][q] = i < a.T * a.Fs ? __ldcg(a.pgu + ((int64_t)(0 * 4 + q) * a.T + t) * a.Fs + f) : 0.f;
+          u[k][q] = i < a.T * a.Fs ? __ldcg(a.pgu + ((int64_t)(1 * 4 + q) * a.T + t) * a.Fs + f) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int i = i0 + k * blockDim.x;
+        if (i < a.T * a.Fs)
+          hs[i] = silu(((g[k][0] + g[k][1]) + g[k][2]) + g[k][3]) * (((u[k][0] + u[k][1]) + u[k][2]) + u[k][3]);
+      }
+    }
+  }
+  __syncthreads();
+
+  const int gw = warp * gridDim.x + blockIdx.x, nwork = gridDim.x * NW3;
+  const int er = nb * QB;
+  // L2 prefetch of output row d's bytes: shared down row and every used expert's row
+  auto prefetch = [&](int d) {
+    if (d >= a.D) return;
+    const int e = shfl(rc.used, lane);
+    if (lane < rc.nu)
+      bulk_prefetch_l2(a.experts + (int64_t)e * a.expert_bytes + 2 * a.gate_bytes + (int64_t)d * er, (uint32_t)er);
+    if (lane == 31 && a.Fs > 0) bulk_prefetch_l2(a.sd + (int64_t)d * a.Fs, (uint32_t)a.Fs * 2u);
+  };
+  prefetch(gw);
+  prefetch(gw + nwork);
+  for (int d = gw; d < a.D; d += nwork) {
+    prefetch(d + 2 * nwork);
+    // shared down row (bf16) . hs
+    float ys[4] = {0.f, 0.f, 0.f, 0.f};
+    if (a.Fs > 0) {
+      const uint16_t *row = a.sd + (int64_t)d * a.Fs;
+#pragma unroll 8
+      for (int c = 8 * lane; c < a.Fs; c += 256) {
+        float wf[8];
+        bf16x8(__ldcs(reinterpret_cast<const uint4 *>(row + c)), wf);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (t >= a.T) break;
+          const float4 h0 = *reinterpret_cast<const float4 *>(hs + t * a.Fs + c);
+          const float4 h1 = *reinterpret_cast<const float4 *>(hs + t * a.Fs + c + 4);
+          ys[t] = fmaf(wf[0], h0.x, ys[t]); ys[t] = fmaf(wf[1], h0.y, ys[t]);
+          ys[t] = fmaf(wf[2], h0.z, ys[t]); ys[t] = fmaf(wf[3], h0.w, ys[t]);
+          ys[t] = fmaf(wf[4], h1.x, ys[t]); ys[t] = fmaf(wf[5], h1.y, ys[t]);
+          ys[t] = fmaf(wf[6], h1.z, ys[t]); ys[t] = fmaf(wf[7], h1.w, ys[t]);
+        }
+      }
+    }
+    // every used expert's down row . its pairs' h (T <= 4 pairs per expert)
+    float yreg = 0.f;  // lane p: y of pair p at this row
+    constexpr int BATCH = 6;
+    for (int u0 = 0; u0 < rc.nu; u0 += BATCH) {
+      RowPart<SPL> rp[BATCH];
+#pragma unroll
+      for (int v = 0; v < BATCH; ++v) {
+        const int e = shfl(rc.used, min(u0 + v, 31));
+        if (u0 + v < rc.nu)
+          load_row<SPL>(a.experts + (int64_t)e * a.expert_bytes + 2 * a.gate_bytes + (int64_t)d * er, rp[v]);
+      }
+      for (int j = 0; j < a.T; ++j) {  // j-th pair of every expert of the batch
+        float y[BATCH];
+#pragma unroll
+        for (int v = 0; v < BATCH; ++v) {
+          const int base = shfl(rc.base, min(u0 + v, 31)), n = shfl(rc.cnt, min(u0 + v, 31));
+          y[v] = 0.f;
+          if (u0 + v < rc.nu && j < n) {
+            const uint32_t *pl = hpl + (base + j) * hw;
+            y[v] = row_dot<SPL>(rp[v], pl, reinterpret_cast<const float *>(pl + 9 * nsb), nsb);
+          }
+        }
+        warp_sum_n<BATCH>(y);
+#pragma unroll
+        for (int v = 0; v < BATCH; ++v) {
+          const int base = shfl(rc.base, min(u0 + v, 31)), n = shfl(rc.cnt, min(u0 + v, 31));
+          const int pr = shfl(rc.perm, min(base + j, 31));
+          if (u0 + v < rc.nu && j < n && lane == pr) yreg = y[v];
+        }
+      }
+    }
+    {
+      float yst[4] = {ys[0], ys[1], ys[2], ys[3]};
+      warp_sum_n<4>(yst);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (t >= a.T) break;
+        float acc = yst[t];  // y_shared (0 without a shared expert)
+        for (int j = 0; j < a.k; ++j) {
+          const int p = t * a.k + j;
+          acc = fmaf(shflf(rc.w, p), shflf(yreg, p), acc);
+        }
+        if (lane == 0) {
+          float *o = a.out + (int64_t)t * a.D + d;
+          *o = a.accumulate ? *o + acc : acc;
+        }
+      }
+    }
+  }
+}
+
+size_t k2_smem(int T, int D) { return 4 * (size_t)T * (9 * (D / 16) + D / QK); }
+size_t k3_smem(int T, int k, int F, int Fs) {
+  return 4 * ((size_t)T * k * (9 * (F / 16) + F / QK) + (size_t)T * Fs);
+}
+
+template <typename K>
+cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Args &a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int SPL_D, int SPL_F>
+cudaError_t launch_all(const Args &a, const Shape &sh, cudaStream_t s) {
+  static int sms = 0;
+  static bool attr = false;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  if (!attr) {  // dynamic caps leave room for the kernels' static shared memory
+    cudaError_t e = cudaFuncSetAttribute(gateup_kernel<SPL_D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(SMEM_LIMIT - 4096));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(down_kernel<SPL_F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(SMEM_LIMIT - 4096));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaError_t e;
+  const dim3 g1((sh.E + 1) / 2);
+  if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16) route_kernel<uint16_t, uint16_t><<<g1, 256, 0, s>>>(a);
+  else if (sh.x_dtype == DS_F32 && sh.router_dtype == DS_F32) route_kernel<float, float><<<g1, 256, 0, s>>>(a);
+  else return cudaErrorInvalidValue;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(gateup_kernel<SPL_D>, dim3(sms), dim3(NW2 * 32), k2_smem(a.T, a.D), s, a)) != cudaSuccess)
+    return e;
+  return launch_pdl(down_kernel<SPL_F>, dim3(sms), dim3(NW3 * 32), k3_smem(a.T, a.k, a.F, a.Fs), s, a);
+}
+
+}  // namespace
+
+// (n_embd / 256, n_ff / 256) with instantiated kernels
+static bool fast_shape_ok(int nb_d, int nb_f) {
+  return (nb_d == 16 && nb_f == 8) || (nb_d == 4 && nb_f == 4);
+}
+
+bool fused_decode_supported(const Shape &sh, int64_t T) {
+  if (T < 1 || T > 4 || (int64_t)T * sh.k > PMAXD) return false;
+  if (sh.D % QK || sh.F % QK || !fast_shape_ok(sh.D / QK, sh.F / QK)) return false;
+  if (sh.x_dtype != sh.router_dtype || sh.E > 1024) return false;
+  // the shared partial sums [2][4][T][Fs] live in the routed-output region [T*k][D]
+  if ((int64_t)8 * sh.Fs > (int64_t)sh.k * sh.D) return false;
+  return k2_smem((int)T, sh.D) <= SMEM_LIMIT - 4096 && k3_smem((int)T, sh.k, sh.F, sh.Fs) <= SMEM_LIMIT - 4096;
+}
+
+cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const void *x,
+                                const Work &wk, float *out, bool accumulate, cudaStream_t s) {
+  Args a{};
+  a.D = sh.D; a.E = sh.E; a.F = sh.F; a.Fs = sh.Fs; a.k = sh.k; a.T = (int)wk.T;
+  a.routed_scale = sh.routed_scale;
+  a.router_w = W.router_w;
+  a.router_f32 = sh.router_dtype == DS_F32;
+  a.bias = W.router_bias;
+  a.sg = W.shared_gate; a.su = W.shared_up; a.sd = W.shared_down;
+  a.experts = W.experts_q2k;
+  a.expert_bytes = sh.expert_bytes();
+  a.gate_bytes = sh.gate_bytes();
+  a.x = x;
+  a.x_f32 = sh.x_dtype == DS_F32;
+  a.logits = wk.logits; a.ids = wk.ids; a.w = wk.w;
+  a.counts = wk.counts; a.offsets = wk.offsets; a.perm = wk.perm; a.pos = wk.pos; a.used = wk.used;
+  a.h = wk.h;
+  a.pgu = wk.y;
+  a.ctrl = wk.ctrl;
+  a.out = out;
+  a.accumulate = accumulate ? 1 : 0;
+  a.status = status_word();
+  a.n_slots = (int)std::min<int64_t>(sh.E, wk.T * sh.k);
+  const int nb_d = sh.D / QK, nb_f = sh.F / QK;
+  if (nb_d == 16 && nb_f == 8) return launch_all<8, 4>(a, sh, s);
+  if (nb_d == 4 && nb_f == 4) return launch_all<2, 2>(a, sh, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dsm

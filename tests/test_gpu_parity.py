@@ -256,19 +256,22 @@ def test_decode32_zipf_parity():
 
 def test_batch_invariance_decode(decode1):
     """Within one path a token's result does not depend on its batch: tokens of
-    an 8-token batch equal the same tokens in a 3-token batch bit for bit
-    (grouped path), and the single-token path agrees with both at tolerance."""
+    an 8-token batch equal the same tokens in a 5-token batch bit for bit
+    (grouped path, T > 4); tokens of a 4-token batch equal themselves alone
+    (fast path, T <= 4); the two paths agree at tolerance."""
     cfg, lo, att, x64, W = decode1
     from dataclasses import replace
     c8 = replace(cfg, T=8)
     xb = synthetic.build_x(c8)
     out_b, _ = run_layer(c8, W, xb)
-    out_3, _ = run_layer(replace(cfg, T=3), W, xb[2:5].contiguous())
-    assert np.array_equal(out_3, out_b[2:5])
-    for t in (0, 5):
+    out_5, _ = run_layer(replace(cfg, T=5), W, xb[2:7].contiguous())
+    assert np.array_equal(out_5, out_b[2:7])
+    out_4, _ = run_layer(replace(cfg, T=4), W, xb[0:4].contiguous())
+    for t in (0, 3):
         out_1, _ = run_layer(cfg, W, xb[t:t + 1].contiguous())
+        assert np.array_equal(out_1[0], out_4[t])
         check_close(out_1[0].astype(np.float64), out_b[t].astype(np.float64), DECODE_TOL,
-                    "single-token path vs batched path")
+                    "fast path vs grouped path")
 
 
 def test_batch_invariance_single_kernel_path():
