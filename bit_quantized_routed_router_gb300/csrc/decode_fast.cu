@@ -27,6 +27,8 @@
 // converted once: w.x = step * (d * sum sc S - dmin * sum m X).  The only
 // rounding beyond fp32 is that fixed point (|err| <= 2^-16 of the block's
 // largest |v| per element).
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -38,7 +40,10 @@ constexpr int PMAXD = 32;          // token-expert pairs this path serves (one p
 constexpr int NW2 = 12, NW3 = 12;  // warps per CTA of K2 and K3
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 
-enum { C_NUSED = 1 };  // control word: experts with tokens (written with the route)
+enum {
+  C_NUSED = 1,  // control word: experts with tokens (written with the route)
+  C_BAR = 2,    // control word: grid barrier of the one-token streaming kernel
+};
 
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -218,6 +223,7 @@ struct Args {
   float *w;
   int32_t *counts, *offsets, *perm, *pos, *used;
   float *h;    // [P][F] routed activations, perm order
+  float *hs;   // [T][Fs] shared-expert activations (streaming kernel)
   float *pgu;  // [2][4][T][Fs] shared gate / up partial sums (per quarter of n_embd)
   unsigned *ctrl;
   float *out;
@@ -244,6 +250,9 @@ __device__ __forceinline__ void ld8<uint16_t>(const uint16_t *p, float v[8]) {
 template <typename TX, typename TW>
 __global__ void __launch_bounds__(256) route_kernel(const Args a) {
   pdl_trigger();  // the gate/up kernel may start its route-free work now
+  // The dependent kernel touches this word only after its griddepcontrol.wait,
+  // i.e. after this grid has completed.
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.ctrl[C_BAR] = 0u;
   __shared__ float part[8][4];  // [warp][token] partial logits
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // two expert rows per CTA, a quarter of n_embd per warp, loads issued up front
@@ -280,6 +289,7 @@ __global__ void __launch_bounds__(256) route_kernel(const Args a) {
 struct RouteCache {
   int nu, perm, used, base, cnt;
   float w;
+  int pos;  // lane p: position of pair p in the route (select_route_warp only)
 };
 
 // Selection and route by one warp (T * k <= 32): top-k by logit, ties to the
@@ -345,6 +355,7 @@ __device__ RouteCache select_route_warp(const Args &a, bool publish) {
   }
   r.perm = perm_p;
   r.w = my_w;
+  r.pos = rank;
   // lane u learns used[u], its first position and its pair count
   int used_u = 0, base_u = 0, cnt_u = 0;
   for (int q = 0; q < P; ++q) {
@@ -391,6 +402,7 @@ __device__ RouteCache select_route_warp(const Args &a, bool publish) {
 __device__ __forceinline__ RouteCache load_route(const Args &a) {
   const int lane = threadIdx.x & 31, P = a.T * a.k;
   RouteCache r;
+  r.pos = 0;
   r.nu = (int)__ldcg((const int *)(a.ctrl + C_NUSED));
   bool bad = r.nu < 0 || r.nu > P;
   if (bad) r.nu = 0;
@@ -452,7 +464,7 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
   const int gw = warp * gridDim.x + blockIdx.x, nwork = gridDim.x * NW2;
   const int rb = nb * QB;
   bool have_route = false;
-  RouteCache rc{0, 0, 0, 0, 0, 0.f};
+  RouteCache rc{0, 0, 0, 0, 0, 0.f, 0};
   // L2 prefetch (bulk-copy engine, lane 0) of item i's bytes; every lane calls
   // it (the routed address comes from a shuffle)
   auto prefetch = [&](int i) {
@@ -672,6 +684,545 @@ __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
   }
 }
 
+// ============================================================== one token ==
+// The layer for one token in one cooperative kernel that streams every weight
+// byte it needs through a ring of shared-memory stages filled by the
+// bulk-copy engine, so that each SM keeps S_NS * S_STAGE bytes in flight.
+//
+//   phase A  tiles of gate/up rows: the shared expert two rows f, f+1 of
+//            gate and up at a time, then every selected expert S_GU rows of
+//            gate and up at a time -> h (routed, slot order) and hs (shared);
+//   grid barrier (all of h is needed by every output row);
+//   phase B  tiles of rb output rows d: the shared down rows and the rows of
+//            every selected expert's down matrix -> out[d] = y_shared +
+//            sum_j w_j y_j (pair order j).
+//
+// Warps 0..S_CONS-1 consume the stages (the same tile sequence on every
+// warp, so their named barriers always match), warp S_CONS (one lane) issues
+// the bulk copies and runs ahead across the grid barrier, warp S_CONS+1 waits
+// for the router logits and selects the experts.  Every wait is bounded
+// (S_LIMIT_NS); an expired wait sets ST_TIMEOUT and the kernel winds down
+// without writing the output.
+constexpr int S_CONS = 12;                       // consumer warps
+constexpr int S_THREADS = (S_CONS + 2) * 32;     // + producer warp + router warp
+constexpr uint32_t S_STAGE = 32768;              // bytes per ring stage
+constexpr int S_NS = 5;                          // ring stages
+constexpr int S_GU = S_CONS;                     // routed gate/up rows per tile (one per warp)
+constexpr int S_MAXP = 64;                       // slots x rows of a phase-B tile
+constexpr int S_MAXT = 16;                       // shared or phase-B tiles of one block
+constexpr uint64_t S_LIMIT_NS = 2000000000ull;   // bound of every wait
+
+struct StreamShared {
+  uint64_t full[S_NS], empty[S_NS];
+  int rt_used[32];     // slot u -> expert (ascending expert id)
+  int rt_pos[32];      // pair j -> its slot
+  float rt_w[32];      // pair j -> routing weight
+  int rt_nu;           // slots in use
+  int ready;           // the route above is published
+  int abort_;          // a wait expired
+  int go;              // consumers continue past the grid barrier
+  int tile[S_NS];                  // phase-A tile in each stage: shared i >= 0, routed -1 - r
+  float reda[S_MAXT][S_CONS][4];   // per shared tile: partial gate/up sums of each warp
+  float redb[S_MAXT][S_CONS][4];   // per phase-B tile: partial shared-down sums of each warp
+  float yrb[S_MAXT][S_MAXP];       // per phase-B tile: routed down results [slot * rb + row]
+};
+
+__device__ __forceinline__ int vload(const int *p) { return *(volatile const int *)p; }
+
+// Bounded wait for the phase of `bar` with parity `par`; false if it expired
+// (flags ST_TIMEOUT) or another role of the block gave up.
+__device__ bool s_wait(uint64_t *bar, uint32_t par, StreamShared &S, unsigned *status) {
+  if (mbar_try_wait(bar, par)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, par)) {
+    if (vload(&S.abort_)) return false;
+    if (globaltimer_ns() - t0 > S_LIMIT_NS) {
+      flag(status, ST_TIMEOUT);
+      *(volatile int *)&S.abort_ = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bounded wait (one thread) for the route to be published.
+__device__ bool s_wait_ready(StreamShared &S, unsigned *status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!vload(&S.ready)) {
+    if (vload(&S.abort_)) return false;
+    if (globaltimer_ns() - t0 > S_LIMIT_NS) {
+      flag(status, ST_TIMEOUT);
+      *(volatile int *)&S.abort_ = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  __threadfence_block();
+  return true;
+}
+
+// This lane's words of one Q2_K row held in shared memory (layout as load_row).
+template <int SPL>
+__device__ __forceinline__ void load_row_s(const uint8_t *row, RowPart<SPL> &r) {
+  const int lane = threadIdx.x & 31;
+  constexpr int LPB = 16 / SPL;
+  const uint8_t *blk = row + (lane / LPB) * QB;
+  const int s0 = SPL * (lane % LPB);
+  const uint32_t *cw = reinterpret_cast<const uint32_t *>(blk + 16 + 4 * s0);
+#pragma unroll
+  for (int i = 0; i < SPL; ++i) r.codes[i] = cw[i];
+  if (SPL >= 4) {
+    const uint32_t *sw = reinterpret_cast<const uint32_t *>(blk + s0);
+#pragma unroll
+    for (int i = 0; i < (SPL + 3) / 4; ++i) r.scm[i] = sw[i];
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(blk + (s0 & ~3));
+    r.scm[0] = w >> (8 * (s0 & 3));
+  }
+  r.dd = *reinterpret_cast<const uint32_t *>(blk + 80);
+}
+
+// The lane's fixed-point activation words (the sub-blocks LaneMap gives it),
+// held in registers for every row of a phase.
+template <int SPL>
+struct XReg {
+  uint32_t hi[SPL][4], lo[SPL][4], sx[SPL];
+  float step;
+};
+
+template <int SPL>
+__device__ __forceinline__ void load_xreg(const uint32_t *planes, const float *steps, int nsb,
+                                          XReg<SPL> &x) {
+  using M = LaneMap<SPL>;
+  constexpr int Q = M::Q;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int g = 0; g < SPL / Q; ++g) {
+    const int o = g * (32 * Q) + lane * Q;
+    uint32_t w[Q];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      lds_words<Q>(planes + i * nsb + o, w);
+#pragma unroll
+      for (int k = 0; k < Q; ++k) x.hi[g * Q + k][i] = w[k];
+      lds_words<Q>(planes + (4 + i) * nsb + o, w);
+#pragma unroll
+      for (int k = 0; k < Q; ++k) x.lo[g * Q + k][i] = w[k];
+    }
+    lds_words<Q>(planes + 8 * nsb + o, w);
+#pragma unroll
+    for (int k = 0; k < Q; ++k) x.sx[g * Q + k] = w[k];
+  }
+  x.step = steps[lane / M::LPB];
+}
+
+// row_dot with the activation words in registers.
+template <int SPL>
+__device__ __forceinline__ float row_dot_reg(const RowPart<SPL> &r, const XReg<SPL> &x) {
+  int accq = 0, accm = 0;
+#pragma unroll
+  for (int sub = 0; sub < SPL; ++sub) {
+    const uint32_t codes = r.codes[sub];
+    const int scm = (r.scm[sub >> 2] >> (8 * (sub & 3))) & 0xFF;
+    const uint32_t q0 = codes & 0x03030303u, q1 = (codes >> 2) & 0x03030303u;
+    const uint32_t q2 = (codes >> 4) & 0x03030303u, q3 = (codes >> 6) & 0x03030303u;
+    int sh = __dp4a((int)q0, (int)x.hi[sub][0], 0);
+    sh = __dp4a((int)q1, (int)x.hi[sub][1], sh);
+    sh = __dp4a((int)q2, (int)x.hi[sub][2], sh);
+    sh = __dp4a((int)q3, (int)x.hi[sub][3], sh);
+    unsigned sl = __dp4a(q0, x.lo[sub][0], 0u);
+    sl = __dp4a(q1, x.lo[sub][1], sl);
+    sl = __dp4a(q2, x.lo[sub][2], sl);
+    sl = __dp4a(q3, x.lo[sub][3], sl);
+    accq += (scm & 15) * (sh * 256 + (int)sl);  // sc_s * sum_j q_j X_j
+    accm += (scm >> 4) * (int)x.sx[sub];        // m_s * sum_j X_j
+  }
+  const float d = fp16_to_f32((uint16_t)(r.dd & 0xFFFF)), dmin = fp16_to_f32((uint16_t)(r.dd >> 16));
+  return x.step * fmaf(d, (float)accq, -dmin * (float)accm);
+}
+
+__host__ __device__ constexpr size_t s_align(size_t v) { return (v + 127) & ~(size_t)127; }
+
+__device__ __forceinline__ int tiles_of(int n, int bid, int G) { return bid < n ? (n - bid + G - 1) / G : 0; }
+
+// Dynamic shared memory of the streaming kernel: stages, the small state,
+// then one region used as x (phase A) and as h, hs (phase B).
+size_t stream_smem(int D, int F, int Fs, int nslots) {
+  const size_t xa = 4 * (size_t)D + 4 * (9 * (size_t)(D / 16) + D / QK);
+  const size_t hb = 4 * (size_t)nslots * (9 * (F / 16) + F / QK) + 4 * (size_t)Fs;
+  return (size_t)S_NS * S_STAGE + s_align(sizeof(StreamShared)) + std::max(xa, hb);
+}
+
+// Rows per phase-B tile: the largest of 4, 2, 1 whose shared and routed down
+// rows fit one stage.
+int stream_rows_b(int D, int F, int Fs, int nslots) {
+  const int64_t rowb_f = (int64_t)(F / QK) * QB;
+  for (int rb = 4; rb >= 1; rb >>= 1)
+    if (D % rb == 0 && (int64_t)rb * nslots <= S_MAXP &&
+        (int64_t)rb * (2 * (int64_t)Fs + nslots * rowb_f) <= S_STAGE)
+      return rb;
+  return 0;
+}
+
+template <int SPL_D, int SPL_F>
+__global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int rb) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t *stages = smem;
+  StreamShared &S = *reinterpret_cast<StreamShared *>(smem + (size_t)S_NS * S_STAGE);
+  uint8_t *reg = smem + (size_t)S_NS * S_STAGE + s_align(sizeof(StreamShared));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, bid = blockIdx.x;
+  const int D = a.D, F = a.F, Fs = a.Fs;
+  const int nb_d = D / QK, nsb_d = D / 16, nb_f = F / QK, nsb_f = F / 16;
+  const int rowb_d = nb_d * QB, rowb_f = nb_f * QB;
+  const int nsa = Fs / 2;                       // shared gate/up tiles
+  const int ngrp = (F + S_GU - 1) / S_GU;       // routed gate/up tiles per slot
+  const int nslots = a.n_slots;
+  const int nB = D / rb;
+  const int ns_b = tiles_of(nsa, bid, G), nr_b = tiles_of(nslots * ngrp, bid, G);  // this block's phase-A tiles
+  const int nb_b = tiles_of(nB, bid, G);                                          // and phase-B tiles
+  const int hw = 9 * nsb_f + nb_f;
+  constexpr int NT = S_CONS * 32;               // consumer threads
+  float *xraw = reinterpret_cast<float *>(reg);                    // phase A
+  uint32_t *xpl = reinterpret_cast<uint32_t *>(reg + 4 * (size_t)D);
+  uint32_t *hpl = reinterpret_cast<uint32_t *>(reg);               // phase B
+  float *hsm = reinterpret_cast<float *>(reg + 4 * (size_t)nslots * hw);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S_NS; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], S_CONS);
+    }
+    S.ready = 0;
+    S.abort_ = 0;
+    S.go = 0;
+    S.rt_nu = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- router --
+  if (warp == S_CONS + 1) {
+    pdl_wait();  // router logits complete and visible
+    const RouteCache r = select_route_warp(a, bid == 0);
+    S.rt_used[lane] = r.used;
+    S.rt_pos[lane] = r.pos;
+    S.rt_w[lane] = r.w;
+    if (lane == 0) S.rt_nu = r.nu;
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) *(volatile int *)&S.ready = 1;
+    return;
+  }
+
+  // -------------------------------------------------------------- producer --
+  if (warp == S_CONS) {
+    if (lane != 0) return;
+    int kq = 0;
+    bool ok = true;
+    // a free stage for the next tile (its previous tile consumed)
+    auto acquire = [&]() -> uint8_t * {
+      const int st = kq % S_NS;
+      if (kq >= S_NS && !s_wait(&S.empty[st], ((kq / S_NS) & 1) ^ 1, S, a.status)) return nullptr;
+      return stages + (size_t)st * S_STAGE;
+    };
+    // phase A: shared tiles while the route is pending, then shared and
+    // routed tiles interleaved in proportion; the order is published per
+    // stage in S.tile for the consumers
+    bool have_route = false;
+    for (int js = 0, jr = 0; ok && (js < ns_b || jr < nr_b);) {
+      uint8_t *dst = acquire();
+      if (!dst) { ok = false; break; }
+      const int st = kq % S_NS;
+      uint64_t *full = &S.full[st];
+      if (!have_route) have_route = vload(&S.ready) != 0;
+      const bool shared = js < ns_b && (!have_route || jr >= nr_b || (int64_t)js * nr_b <= (int64_t)jr * ns_b);
+      if (shared) {
+        const int i = bid + G * js++;
+        S.tile[st] = i;
+        const uint32_t bytes = 4u * (uint32_t)D;  // rows f, f+1 in bf16
+        mbar_arrive_expect_tx(full, 2 * bytes);
+        bulk_g2s(dst, a.sg + (size_t)(2 * i) * D, bytes, full);
+        bulk_g2s(dst + bytes, a.su + (size_t)(2 * i) * D, bytes, full);
+      } else {
+        if (!have_route && !(have_route = s_wait_ready(S, a.status))) { ok = false; break; }
+        const int r = bid + G * jr++, u = r / ngrp, g = r % ngrp;
+        S.tile[st] = -1 - r;
+        const int rows = min(S_GU, F - g * S_GU);
+        if (u < S.rt_nu) {
+          const uint8_t *gr = a.experts + (int64_t)S.rt_used[u] * a.expert_bytes + (int64_t)g * S_GU * rowb_d;
+          const uint32_t bytes = (uint32_t)(rows * rowb_d);
+          mbar_arrive_expect_tx(full, 2 * bytes);
+          bulk_g2s(dst, gr, bytes, full);
+          bulk_g2s(dst + S_GU * rowb_d, gr + a.gate_bytes, bytes, full);
+        } else {
+          mbar_arrive(full);
+        }
+      }
+      ++kq;
+    }
+    // phase B needs no h: its copies run ahead across the grid barrier
+    for (int m = 0; ok && m < nb_b; ++m) {
+      if (!have_route && !(have_route = s_wait_ready(S, a.status))) break;
+      uint8_t *dst = acquire();
+      if (!dst) break;
+      uint64_t *full = &S.full[kq % S_NS];
+      const int d0 = (bid + G * m) * rb, nu = S.rt_nu;
+      const uint32_t sb = (uint32_t)(rb * 2 * Fs), ub = (uint32_t)(rb * rowb_f);
+      mbar_arrive_expect_tx(full, sb + (uint32_t)nu * ub);
+      if (Fs > 0) bulk_g2s(dst, a.sd + (size_t)d0 * Fs, sb, full);
+      for (int u = 0; u < nu; ++u)
+        bulk_g2s(dst + sb + (size_t)u * ub,
+                 a.experts + (int64_t)S.rt_used[u] * a.expert_bytes + 2 * a.gate_bytes + (int64_t)d0 * rowb_f,
+                 ub, full);
+      ++kq;
+    }
+    // keep the block resident until every copy issued has landed
+    for (int q = kq > S_NS ? kq - S_NS : 0; q < kq; ++q) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&S.full[q % S_NS], (q / S_NS) & 1))
+        if (globaltimer_ns() - t0 > S_LIMIT_NS) { flag(a.status, ST_TIMEOUT); break; }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------- consumers --
+  // x as fp32 (shared-expert rows) and as fixed-point planes (Q2_K rows),
+  // one half-warp per 256-element block, all loads in one round
+  for (int u = warp; u < (nb_d + 1) / 2; u += S_CONS) {
+    const int blk = min(2 * u + (lane >> 4), nb_d - 1);
+    const int64_t e0 = (int64_t)QK * blk + 16 * (lane & 15);
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      v[j] = a.x_f32 ? __ldg((const float *)a.x + e0 + j) : bf16_to_f32(__ldg((const uint16_t *)a.x + e0 + j));
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4 *>(xraw + e0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    digitize_block<SPL_D>(v, blk, xpl, reinterpret_cast<float *>(xpl + 9 * nsb_d), nsb_d);
+  }
+  named_bar(1, NT);
+  int nu = 0;
+  {
+    XReg<SPL_D> xr;
+    load_xreg<SPL_D>(xpl, reinterpret_cast<const float *>(xpl + 9 * nsb_d), nsb_d, xr);
+    bool have_route = false;
+    int js = 0;
+    for (int kq = 0; kq < ns_b + nr_b; ++kq) {
+      const int st = kq % S_NS;
+      const bool got = s_wait(&S.full[st], (kq / S_NS) & 1, S, a.status);
+      const uint8_t *src = stages + (size_t)st * S_STAGE;
+      const int td = got ? S.tile[st] : 0;
+      if (td >= 0) {
+        // rows in the stage: gate f, gate f+1, up f, up f+1; every consumer
+        // thread takes eight-element chunks of all four rows (x read once)
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (got) {
+          for (int c = 8 * threadIdx.x; c < D; c += 8 * NT) {
+            const float4 x0 = *reinterpret_cast<const float4 *>(xraw + c);
+            const float4 x1 = *reinterpret_cast<const float4 *>(xraw + c + 4);
+#pragma unroll
+            for (int row = 0; row < 4; ++row) {
+              float wf[8];
+              bf16x8(*reinterpret_cast<const uint4 *>(src + (size_t)row * 2 * D + 2 * (size_t)c), wf);
+              float t = acc[row];
+              t = fmaf(wf[0], x0.x, t); t = fmaf(wf[1], x0.y, t); t = fmaf(wf[2], x0.z, t); t = fmaf(wf[3], x0.w, t);
+              t = fmaf(wf[4], x1.x, t); t = fmaf(wf[5], x1.y, t); t = fmaf(wf[6], x1.z, t); t = fmaf(wf[7], x1.w, t);
+              acc[row] = t;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[st]);
+        warp_sum_n<4>(acc);
+        if (lane == 0 && js < S_MAXT) {
+#pragma unroll
+          for (int row = 0; row < 4; ++row) S.reda[js][warp][row] = acc[row];
+        }
+        ++js;
+        continue;
+      }
+      if (!have_route) {
+        int rdy = 1;
+        if (lane == 0) rdy = s_wait_ready(S, a.status) ? 1 : 0;
+        rdy = __shfl_sync(0xffffffffu, rdy, 0);
+        __threadfence_block();
+        nu = rdy ? S.rt_nu : 0;
+        have_route = true;
+      }
+      const int r = -1 - td, u = r / ngrp, g = r % ngrp;
+      const int f = g * S_GU + warp;
+      if (got && u < nu && f < F) {
+        RowPart<SPL_D> gp, up;
+        load_row_s<SPL_D>(src + (size_t)warp * rowb_d, gp);
+        load_row_s<SPL_D>(src + (size_t)(S_GU + warp) * rowb_d, up);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[st]);
+        float gu[2] = {row_dot_reg<SPL_D>(gp, xr), row_dot_reg<SPL_D>(up, xr)};
+        warp_sum_n<2>(gu);
+        if (lane == 0) a.h[(int64_t)u * F + f] = silu(gu[0]) * gu[1];
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[st]);
+      }
+    }
+  }
+  // hs of this block's shared tiles: gate and up summed over the warps in
+  // a fixed order
+  named_bar(1, NT);
+  for (int t = threadIdx.x; t < 2 * min(ns_b, S_MAXT); t += NT) {
+    const int m = t >> 1, h = t & 1;
+    float g = 0.f, u = 0.f;
+    for (int w = 0; w < S_CONS; ++w) {
+      g += S.reda[m][w][h];
+      u += S.reda[m][w][2 + h];
+    }
+    a.hs[2 * (bid + G * m) + h] = silu(g) * u;
+  }
+
+  // grid barrier: every block's h and hs are written
+  named_bar(1, NT);
+  if (threadIdx.x == 0) {
+    bool fine = !vload(&S.abort_) && s_wait_ready(S, a.status);
+    if (fine) {
+      pdl_wait();  // the router grid (which reset the barrier word) has completed
+      __threadfence();
+      atom_add_release(a.ctrl + C_BAR, 1u);
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire(a.ctrl + C_BAR) < (unsigned)G) {
+        if (globaltimer_ns() - t0 > S_LIMIT_NS) {
+          flag(a.status, ST_TIMEOUT);
+          fine = false;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    if (!fine) *(volatile int *)&S.abort_ = 1;
+    S.go = fine ? 1 : 0;  // the one decision every consumer warp follows
+  }
+  named_bar(1, NT);
+  if (!vload(&S.go)) return;
+  nu = S.rt_nu;
+
+  // h of every slot in fixed point, and hs: one half-warp per 256-element
+  // block, two blocks per half-warp and pass with all loads issued first
+  {
+    const int nblk = nu * nb_f, nun = (nblk + 1) / 2;
+    for (int un = warp; un < nun; un += 2 * S_CONS) {
+      float v[2][16];
+      int q[2], blk[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int bi = min(2 * min(un + h * S_CONS, nun - 1) + (lane >> 4), nblk - 1);
+        q[h] = bi / nb_f;
+        blk[h] = bi % nb_f;
+        const float4 *hsrc = reinterpret_cast<const float4 *>(a.h + (int64_t)q[h] * F + QK * blk[h] + 16 * (lane & 15));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 f4 = __ldcg(hsrc + j);
+          v[h][4 * j] = f4.x; v[h][4 * j + 1] = f4.y; v[h][4 * j + 2] = f4.z; v[h][4 * j + 3] = f4.w;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        digitize_block<SPL_F>(v[h], blk[h], hpl + q[h] * hw, reinterpret_cast<float *>(hpl + q[h] * hw + 9 * nsb_f), nsb_f);
+    }
+    for (int i = threadIdx.x; i < Fs; i += NT) hsm[i] = __ldcg(a.hs + i);
+  }
+  named_bar(1, NT);
+
+  // phase B: every consumer thread takes eight-element chunks of all rb
+  // shared rows (hs read once); warp w takes the routed (slot, row) pairs
+  // w and w + S_CONS when they are the only two (else it loops over its
+  // pairs one at a time)
+  const int np = nu * rb;
+  const bool two = np <= 2 * S_CONS;
+  int kq = ns_b + nr_b;
+  for (int m = 0; m < nb_b; ++m, ++kq) {
+    const int st = kq % S_NS;
+    const bool got = s_wait(&S.full[st], (kq / S_NS) & 1, S, a.status);
+    const uint8_t *src = stages + (size_t)st * S_STAGE;
+    float ys[4] = {0.f, 0.f, 0.f, 0.f};
+    if (got) {
+      for (int c = 8 * threadIdx.x; c < Fs; c += 8 * NT) {
+        const float4 h0 = *reinterpret_cast<const float4 *>(hsm + c);
+        const float4 h1 = *reinterpret_cast<const float4 *>(hsm + c + 4);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if (r >= rb) break;
+          float wf[8];
+          bf16x8(*reinterpret_cast<const uint4 *>(src + (size_t)r * 2 * Fs + 2 * (size_t)c), wf);
+          float t = ys[r];
+          t = fmaf(wf[0], h0.x, t); t = fmaf(wf[1], h0.y, t); t = fmaf(wf[2], h0.z, t); t = fmaf(wf[3], h0.w, t);
+          t = fmaf(wf[4], h1.x, t); t = fmaf(wf[5], h1.y, t); t = fmaf(wf[6], h1.z, t); t = fmaf(wf[7], h1.w, t);
+          ys[r] = t;
+        }
+      }
+    }
+    const uint8_t *routed = src + (size_t)rb * 2 * Fs;
+    float y[2] = {0.f, 0.f};
+    if (two) {
+      RowPart<SPL_F> rp[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int p = warp + h * S_CONS;
+        if (got && p < np) load_row_s<SPL_F>(routed + (size_t)p * rowb_f, rp[h]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[st]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int p = warp + h * S_CONS;
+        if (got && p < np) {
+          const uint32_t *pl = hpl + (p / rb) * hw;
+          y[h] = row_dot<SPL_F>(rp[h], pl, reinterpret_cast<const float *>(pl + 9 * nsb_f), nsb_f);
+        }
+      }
+      float v6[6] = {ys[0], ys[1], ys[2], ys[3], y[0], y[1]};
+      warp_sum_n<6>(v6);
+      if (lane == 0 && m < S_MAXT) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) S.redb[m][warp][r] = v6[r];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (warp + h * S_CONS < np) S.yrb[m][warp + h * S_CONS] = v6[4 + h];
+      }
+    } else {
+      // one pair at a time, the stage released after the last
+      warp_sum_n<4>(ys);
+      if (lane == 0 && m < S_MAXT) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) S.redb[m][warp][r] = ys[r];
+      }
+      for (int p = warp; p < np; p += S_CONS) {
+        float yy = 0.f;
+        if (got) {
+          RowPart<SPL_F> rp;
+          load_row_s<SPL_F>(routed + (size_t)p * rowb_f, rp);
+          const uint32_t *pl = hpl + (p / rb) * hw;
+          yy = row_dot<SPL_F>(rp, pl, reinterpret_cast<const float *>(pl + 9 * nsb_f), nsb_f);
+        }
+        yy = warp_sum(yy);
+        if (lane == 0 && m < S_MAXT) S.yrb[m][p] = yy;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[st]);
+    }
+  }
+  // the combine of this block's output rows: y_shared (summed over the warps
+  // in a fixed order) + sum_j w_j y_j in pair order j
+  named_bar(1, NT);
+  if (vload(&S.abort_)) return;
+  for (int t = threadIdx.x; t < min(nb_b, S_MAXT) * rb; t += NT) {
+    const int m = t / rb, r = t % rb;
+    float acc = 0.f;
+    for (int w = 0; w < S_CONS; ++w) acc += S.redb[m][w][r];
+    for (int j = 0; j < a.k; ++j) acc = fmaf(S.rt_w[j], S.yrb[m][S.rt_pos[j] * rb + r], acc);
+    float *o = a.out + (int64_t)(bid + G * m) * rb + r;
+    *o = a.accumulate ? *o + acc : acc;
+  }
+}
+
 size_t k2_smem(int T, int D) { return 4 * (size_t)T * (9 * (D / 16) + D / QK); }
 size_t k3_smem(int T, int k, int F, int Fs) {
   return 4 * ((size_t)T * k * (9 * (F / 16) + F / QK) + (size_t)T * Fs);
@@ -721,6 +1272,55 @@ cudaError_t launch_all(const Args &a, const Shape &sh, cudaStream_t s) {
   return launch_pdl(down_kernel<SPL_F>, dim3(sms), dim3(NW3 * 32), k3_smem(a.T, a.k, a.F, a.Fs), s, a);
 }
 
+// One token: router logits, then the streaming kernel (cooperative, so the
+// grid barrier is safe; PDL lets its prologue overlap the router grid).
+template <int SPL_D, int SPL_F>
+cudaError_t launch_stream(const Args &a, const Shape &sh, int rb, cudaStream_t s) {
+  static int sms = 0;
+  static bool attr = false;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  const size_t smem = stream_smem(a.D, a.F, a.Fs, a.n_slots);
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(stream_kernel<SPL_D, SPL_F>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<SPL_D, SPL_F>, S_THREADS, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    attr = true;
+  }
+  const dim3 g1((sh.E + 1) / 2);
+  if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16) route_kernel<uint16_t, uint16_t><<<g1, 256, 0, s>>>(a);
+  else if (sh.x_dtype == DS_F32 && sh.router_dtype == DS_F32) route_kernel<float, float><<<g1, 256, 0, s>>>(a);
+  else return cudaErrorInvalidValue;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(S_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeCooperative;
+  attrs[0].val.cooperative = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, stream_kernel<SPL_D, SPL_F>, a, rb);
+  if (e != cudaSuccess) {  // without the overlap: plain stream order
+    (void)cudaGetLastError();
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, stream_kernel<SPL_D, SPL_F>, a, rb);
+  }
+  return e;
+}
+
 }  // namespace
 
 // (n_embd / 256, n_ff / 256) with instantiated kernels
@@ -754,6 +1354,7 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
   a.logits = wk.logits; a.ids = wk.ids; a.w = wk.w;
   a.counts = wk.counts; a.offsets = wk.offsets; a.perm = wk.perm; a.pos = wk.pos; a.used = wk.used;
   a.h = wk.h;
+  a.hs = wk.hs;
   a.pgu = wk.y;
   a.ctrl = wk.ctrl;
   a.out = out;
@@ -761,6 +1362,18 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
   a.status = status_word();
   a.n_slots = (int)std::min<int64_t>(sh.E, wk.T * sh.k);
   const int nb_d = sh.D / QK, nb_f = sh.F / QK;
+  if (a.T == 1) {
+    const int rb = stream_rows_b(a.D, a.F, a.Fs, a.n_slots);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool fits = rb > 0 && sms > 0 && stream_smem(a.D, a.F, a.Fs, a.n_slots) <= SMEM_LIMIT &&
+                      a.n_slots <= 32 && 8 * (int64_t)a.D <= S_STAGE &&
+                      2 * S_GU * (int64_t)nb_d * QB <= S_STAGE && nb_f % 4 == 0 &&
+                      (a.Fs / 2 + sms - 1) / sms <= S_MAXT && (a.D / rb + sms - 1) / sms <= S_MAXT;
+    if (fits && nb_d == 16 && nb_f == 8) return launch_stream<8, 4>(a, sh, rb, s);
+    if (fits && nb_d == 4 && nb_f == 4) return launch_stream<2, 2>(a, sh, rb, s);
+  }
   if (nb_d == 16 && nb_f == 8) return launch_all<8, 4>(a, sh, s);
   if (nb_d == 4 && nb_f == 4) return launch_all<2, 2>(a, sh, s);
   return cudaErrorInvalidValue;
