@@ -204,6 +204,35 @@ __device__ __forceinline__ void warp_sum_n(float v[N]) {
     for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
 }
 
+// Warp totals of N values (N = 2, 4, 8) in 5 + N - 2 shuffles instead of
+// 5 N: at each of the first levels a lane hands half of its running sums to
+// its partner and keeps the other half.  Lane l ends with the total of
+// v[l / (32 / N)].
+template <int N>
+__device__ __forceinline__ float warp_sum_spread(const float v[N]) {
+  const int lane = threadIdx.x & 31;
+  float cur[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) cur[i] = v[i];
+  int n = N;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (n > 1) {
+      const bool hi = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const float send = hi ? cur[i] : cur[n / 2 + i];
+        const float keep = hi ? cur[n / 2 + i] : cur[i];
+        cur[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+      n /= 2;
+    } else {
+      cur[0] += __shfl_xor_sync(0xffffffffu, cur[0], o);
+    }
+  }
+  return cur[0];
+}
+
 __device__ __forceinline__ int shfl(int v, int l) { return __shfl_sync(0xffffffffu, v, l); }
 __device__ __forceinline__ float shflf(float v, int l) { return __shfl_sync(0xffffffffu, v, l); }
 
@@ -706,7 +735,7 @@ __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
 constexpr int S_CONS = 12;                       // consumer warps
 constexpr int S_THREADS = (S_CONS + 2) * 32;     // + producer warp + router warp
 constexpr uint32_t S_STAGE = 32768;              // bytes per ring stage
-constexpr int S_NS = 5;                          // ring stages
+constexpr int S_NS = 3;                          // ring stages
 constexpr int S_GU = S_CONS;                     // routed gate/up rows per tile (one per warp)
 constexpr int S_MAXP = 64;                       // slots x rows of a phase-B tile
 constexpr int S_MAXT = 16;                       // shared or phase-B tiles of one block
@@ -879,7 +908,10 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
   const int ngrp = (F + S_GU - 1) / S_GU;       // routed gate/up tiles per slot
   const int nslots = a.n_slots;
   const int nB = D / rb;
-  const int ns_b = tiles_of(nsa, bid, G), nr_b = tiles_of(nslots * ngrp, bid, G);  // this block's phase-A tiles
+  // this block's phase-A tiles; routed tiles are dealt from the last block
+  // down, so the blocks with one shared tile fewer get one routed tile more
+  const int rbid = G - 1 - bid;
+  const int ns_b = tiles_of(nsa, bid, G), nr_b = tiles_of(nslots * ngrp, rbid, G);
   const int nb_b = tiles_of(nB, bid, G);                                          // and phase-B tiles
   const int hw = 9 * nsb_f + nb_f;
   constexpr int NT = S_CONS * 32;               // consumer threads
@@ -946,7 +978,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
         bulk_g2s(dst + bytes, a.su + (size_t)(2 * i) * D, bytes, full);
       } else {
         if (!have_route && !(have_route = s_wait_ready(S, a.status))) { ok = false; break; }
-        const int r = bid + G * jr++, u = r / ngrp, g = r % ngrp;
+        const int r = rbid + G * jr++, u = r / ngrp, g = r % ngrp;
         S.tile[st] = -1 - r;
         const int rows = min(S_GU, F - g * S_GU);
         if (u < S.rt_nu) {
@@ -1033,11 +1065,8 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[st]);
-        warp_sum_n<4>(acc);
-        if (lane == 0 && js < S_MAXT) {
-#pragma unroll
-          for (int row = 0; row < 4; ++row) S.reda[js][warp][row] = acc[row];
-        }
+        const float tot = warp_sum_spread<4>(acc);  // lane 8 row: total of row
+        if ((lane & 7) == 0 && js < S_MAXT) S.reda[js][warp][lane >> 3] = tot;
         ++js;
         continue;
       }
@@ -1057,9 +1086,10 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
         load_row_s<SPL_D>(src + (size_t)(S_GU + warp) * rowb_d, up);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[st]);
-        float gu[2] = {row_dot_reg<SPL_D>(gp, xr), row_dot_reg<SPL_D>(up, xr)};
-        warp_sum_n<2>(gu);
-        if (lane == 0) a.h[(int64_t)u * F + f] = silu(gu[0]) * gu[1];
+        const float gu[2] = {row_dot_reg<SPL_D>(gp, xr), row_dot_reg<SPL_D>(up, xr)};
+        const float tot = warp_sum_spread<2>(gu);  // lane 0: gate, lane 16: up
+        const float upv = __shfl_sync(0xffffffffu, tot, 16);
+        if (lane == 0) a.h[(int64_t)u * F + f] = silu(tot) * upv;
       } else {
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[st]);
@@ -1178,14 +1208,12 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
           y[h] = row_dot<SPL_F>(rp[h], pl, reinterpret_cast<const float *>(pl + 9 * nsb_f), nsb_f);
         }
       }
-      float v6[6] = {ys[0], ys[1], ys[2], ys[3], y[0], y[1]};
-      warp_sum_n<6>(v6);
-      if (lane == 0 && m < S_MAXT) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) S.redb[m][warp][r] = v6[r];
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (warp + h * S_CONS < np) S.yrb[m][warp + h * S_CONS] = v6[4 + h];
+      const float v8[8] = {ys[0], ys[1], ys[2], ys[3], y[0], y[1], 0.f, 0.f};
+      const float tot = warp_sum_spread<8>(v8);  // lane 4 i: total of v8[i]
+      const int vi = lane >> 2;
+      if ((lane & 3) == 0 && m < S_MAXT) {
+        if (vi < 4) S.redb[m][warp][vi] = tot;
+        else if (vi < 6 && warp + (vi - 4) * S_CONS < np) S.yrb[m][warp + (vi - 4) * S_CONS] = tot;
       }
     } else {
       // one pair at a time, the stage released after the last
