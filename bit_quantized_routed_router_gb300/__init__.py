@@ -25,7 +25,10 @@ DS_F32, DS_BF16 = 0, 1
 SYMBOLS = ["ds_moe_q2k_bytes", "ds_moe_expert_bytes", "ds_moe_quantize_q2k",
            "ds_moe_dequantize_q2k", "ds_moe_workspace_bytes", "ds_moe_layer",
            "ds_moe_layer_hostio", "ds_moe_stack", "ds_moe_sync_status", "ds_moe_version",
-           "ds_moe_layer_noalloc"]
+           "ds_moe_layer_noalloc", "ds_moe_layer_path"]
+
+# ds_moe_layer_path results
+PATH_NONE, PATH_STREAM, PATH_DECODE3, PATH_GROUPED_GEMV, PATH_TENSOR_CORE = 0, 1, 2, 3, 4
 
 
 class DsMoeError(RuntimeError):
@@ -163,6 +166,18 @@ def quantize_q2k(w, out, stream=None):
 
 def dequantize_q2k(q, rows, in_dim, out, stream=None):
     _call(lib().ds_moe_dequantize_q2k, q.data_ptr(), rows, in_dim, out.data_ptr(), _stream(stream))
+
+
+def layer_path(shape: MoEShape, T: int, x=None) -> int:
+    """Which kernels ds_moe_layer runs for T tokens (a PATH_* value)."""
+    L = lib()
+    L.ds_moe_layer_path.restype = ctypes.c_int
+    L.ds_moe_layer_path.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    sh = shape.c()
+    rc = L.ds_moe_layer_path(ctypes.byref(sh), T, _ptr(x) if x is not None else 256)
+    if rc < 0:
+        raise DsMoeError(rc, "shape rejected")
+    return rc
 
 
 def workspace_bytes(shape: MoEShape, T: int) -> int:

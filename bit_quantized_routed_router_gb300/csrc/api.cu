@@ -105,6 +105,8 @@ size_t layout(const Shape &sh, int64_t T, char *base, Work *wk) {
   w.xn = (uint16_t *)take(sizeof(uint16_t) * T * sh.D);
   w.x_dev = take(xbytes);
   w.out_dev = (float *)take(sizeof(float) * T * sh.D);
+  w.tc = prefill_tc_supported(sh, T) ? (void *)take(prefill_tc_workspace(sh, T)) : nullptr;
+  if (!base) w.tc = nullptr;
   w.T = T;
   w.n_chunks = n_chunks;
   if (wk) *wk = w;
@@ -139,8 +141,12 @@ int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *ou
     if ((e = cudaMemsetAsync(wk.ctrl, 0, 256, s)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "workspace control reset");
     if ((e = launch_route(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
-    if ((e = launch_decode_ffn(sh, W, x, wk, s)) != cudaSuccess)
+    if (wk.tc && aligned(x, 16) && prefill_tc_supported(sh, wk.T)) {
+      if ((e = launch_prefill_tc(sh, W, x, wk, wk.tc, s)) != cudaSuccess)
+        return cuda_fail(err, errlen, e, "expert FFN (tensor cores)");
+    } else if ((e = launch_decode_ffn(sh, W, x, wk, s)) != cudaSuccess) {
       return cuda_fail(err, errlen, e, "expert FFN");
+    }
     if ((e = launch_combine(sh, wk, out, accumulate, s)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "combine");
   }
@@ -317,8 +323,20 @@ int ds_moe_sync_status(void *stream, char *err, size_t errlen) {
   if (v & ST_QUANT_INPUT)
     return fail(err, errlen, DS_ERR_DEVICE_CHECK, "quantiser input not finite or |w| > 65504 (status 0x%x)", v);
   if (v & ST_BAD_ID) return fail(err, errlen, DS_ERR_DEVICE_CHECK, "expert id out of range (status 0x%x)", v);
+  if (v & ST_RANGE)
+    return fail(err, errlen, DS_ERR_DEVICE_CHECK,
+                "a value beyond the fp16 range reached the tensor-core path and was saturated (status 0x%x)", v);
   if (v) return fail(err, errlen, DS_ERR_DEVICE_CHECK, "device check failed (status 0x%x)", v);
   return DS_OK;
+}
+
+int ds_moe_layer_path(const ds_moe_shape *shape, int64_t T, const void *x) {
+  Shape sh;
+  if (check_shape(shape, nullptr, 0, &sh) != DS_OK || T < 0) return DS_ERR_INVALID_ARG;
+  if (T == 0) return DS_PATH_NONE;
+  if (fused_decode_supported(sh, T)) return stream_decode_supported(sh, T) ? DS_PATH_STREAM : DS_PATH_DECODE3;
+  if (aligned(x, 16) && prefill_tc_supported(sh, T)) return DS_PATH_TENSOR_CORE;
+  return DS_PATH_GROUPED_GEMV;
 }
 
 const char *ds_moe_version(void) { return "ds_moe 0.1 (sm_103a)"; }

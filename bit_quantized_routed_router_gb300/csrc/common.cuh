@@ -19,6 +19,7 @@ enum : unsigned {
   ST_BAD_ID = 1u << 1,        // expert id outside [0, E)
   ST_TIMEOUT = 1u << 2,       // a bounded device wait expired
   ST_BAD_COUNT = 1u << 3,     // route counts inconsistent
+  ST_RANGE = 1u << 4,         // a value beyond the fp16 range met the tensor-core path (saturated)
 };
 
 // Status word address for the current device (set up once per device).

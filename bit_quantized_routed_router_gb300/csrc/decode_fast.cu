@@ -1365,6 +1365,21 @@ bool fused_decode_supported(const Shape &sh, int64_t T) {
   return k2_smem((int)T, sh.D) <= SMEM_LIMIT - 4096 && k3_smem((int)T, sh.k, sh.F, sh.Fs) <= SMEM_LIMIT - 4096;
 }
 
+bool stream_decode_supported(const Shape &sh, int64_t T) {
+  if (T != 1 || !fused_decode_supported(sh, T)) return false;
+  const int nb_d = sh.D / QK, nb_f = sh.F / QK, nslots = std::min(sh.E, sh.k);
+  const int rb = stream_rows_b(sh.D, sh.F, sh.Fs, nslots);
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  return rb > 0 && sms > 0 && stream_smem(sh.D, sh.F, sh.Fs, nslots) <= SMEM_LIMIT && nslots <= 32 &&
+         8 * (int64_t)sh.D <= S_STAGE && 2 * S_GU * (int64_t)nb_d * QB <= S_STAGE && nb_f % 4 == 0 &&
+         (sh.Fs / 2 + sms - 1) / sms <= S_MAXT && (sh.D / rb + sms - 1) / sms <= S_MAXT;
+}
+
 cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const void *x,
                                 const Work &wk, float *out, bool accumulate, cudaStream_t s) {
   Args a{};
@@ -1390,17 +1405,10 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
   a.status = status_word();
   a.n_slots = (int)std::min<int64_t>(sh.E, wk.T * sh.k);
   const int nb_d = sh.D / QK, nb_f = sh.F / QK;
-  if (a.T == 1) {
+  if (stream_decode_supported(sh, wk.T)) {
     const int rb = stream_rows_b(a.D, a.F, a.Fs, a.n_slots);
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool fits = rb > 0 && sms > 0 && stream_smem(a.D, a.F, a.Fs, a.n_slots) <= SMEM_LIMIT &&
-                      a.n_slots <= 32 && 8 * (int64_t)a.D <= S_STAGE &&
-                      2 * S_GU * (int64_t)nb_d * QB <= S_STAGE && nb_f % 4 == 0 &&
-                      (a.Fs / 2 + sms - 1) / sms <= S_MAXT && (a.D / rb + sms - 1) / sms <= S_MAXT;
-    if (fits && nb_d == 16 && nb_f == 8) return launch_stream<8, 4>(a, sh, rb, s);
-    if (fits && nb_d == 4 && nb_f == 4) return launch_stream<2, 2>(a, sh, rb, s);
+    if (nb_d == 16 && nb_f == 8) return launch_stream<8, 4>(a, sh, rb, s);
+    if (nb_d == 4 && nb_f == 4) return launch_stream<2, 2>(a, sh, rb, s);
   }
   if (nb_d == 16 && nb_f == 8) return launch_all<8, 4>(a, sh, s);
   if (nb_d == 4 && nb_f == 4) return launch_all<2, 2>(a, sh, s);

@@ -26,6 +26,7 @@ struct Work {
   uint16_t *xn;      // [T][D] bf16 normalised input (stack)
   void *x_dev;       // [T][D] device copy of host x (hostio)
   float *out_dev;    // [T][D] device out (hostio)
+  void *tc;          // tensor-core path scratch (prefill_tc_workspace bytes), or null
   int64_t T;
   int64_t n_chunks;
 };
@@ -46,8 +47,17 @@ cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const vo
 // Decode path for T <= 8: the whole layer in one persistent kernel (writes or
 // accumulates into out, and fills the route arrays of the workspace).
 bool fused_decode_supported(const Shape &sh, int64_t T);
+// ... and within it, the one-token streaming kernel.
+bool stream_decode_supported(const Shape &sh, int64_t T);
 cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const void *x,
                                 const Work &wk, float *out, bool accumulate, cudaStream_t s);
+// Large batches: the expert FFNs as grouped tcgen05 GEMMs (after
+// launch_route; the combine follows).  tc_ws holds prefill_tc_workspace bytes.
+constexpr int64_t TC_MIN_T = 64;
+bool prefill_tc_supported(const Shape &sh, int64_t T);
+size_t prefill_tc_workspace(const Shape &sh, int64_t T);
+cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
+                              void *tc_ws, cudaStream_t s);
 cudaError_t launch_combine(const Shape &sh, const Work &wk, float *out, bool accumulate,
                            cudaStream_t s);
 

@@ -1,0 +1,757 @@
+// Large-batch (prefill) expert FFNs on the 5th-generation tensor cores.
+//
+// What it computes is the expert part of the layer of "Understanding Dwarf
+// Star" 5.3.2 / 5.3.4 / 5.3.7: for every routed expert e and its tokens,
+// h = SiLU(X_e Wg_e^T) * (X_e Wu_e^T) and y = h Wd_e^T with the Q2_K weights
+// of 3.3.3 dequantised on the fly (2.8.1-2.8.2), plus the always-active bf16
+// shared expert over all tokens.  The router, selection, route and the
+// combine out = y_shared + sum_j w_j y_j run in their own kernels.
+//
+// Both contractions run "weights as M": a tile is 128 weight rows (the f
+// rows of gate and up, or the d rows of down) times up to N tokens of one
+// expert (N rounded up to a multiple of 16), so an expert with 96 tokens
+// wastes no more than 15 columns.  Per tile and 64-wide K step:
+//
+//   dequant warps  Q2_K rows -> fp16 in the 128-byte swizzled K-major layout
+//                  of the MMA, from raw 96-byte block copies that the copy
+//                  warp stages in shared memory two blocks ahead;
+//   copy warp      bulk-tensor (TMA) loads of the token rows (fp16) and, for
+//                  the dense shared expert, of its weight rows;
+//   MMA thread     tcgen05.mma kind::f16, fp32 accumulators in tensor memory
+//                  (two accumulator buffers, so the epilogue of one tile
+//                  overlaps the main loop of the next);
+//   epilogue warps tcgen05.ld of the accumulators: SiLU(g) * u -> h (fp16),
+//                  or y (fp32).
+//
+// Dequantised weights are exact fp32 values d*sc*q - dmin*m rounded once to
+// fp16.  Within every group of 16 consecutive K indices the operands are
+// stored in a fixed order (position p holds index 4 (p mod 4) + p / 4) that
+// makes the dequantisation a byte permutation; the activations are written
+// in the same order, and a K-sum does not depend on the order of its terms.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dsm {
+namespace {
+
+constexpr int TC_BM = 128;                 // weight rows per tile (MMA M)
+constexpr int TC_BK = 64;                  // K per stage: one 128-byte swizzle row
+constexpr int TC_NGU = 128;                // tokens per gate/up tile at most
+constexpr int TC_NDN = 256;                // tokens per down tile at most
+constexpr int TC_STAGES = 3;
+constexpr uint32_t TC_TILE_BYTES = TC_BM * 128;       // one 128 x 64 operand tile (16 KB)
+constexpr uint32_t TC_STAGE_BYTES = 3 * TC_TILE_BYTES; // gate/up: A_g, A_u, B; down: A, B (256 rows)
+constexpr int TC_RAW_SLOTS = 3;
+constexpr uint32_t TC_RAW_ROW = 96;        // bytes copied per weight row and 256-weight block
+constexpr uint32_t TC_RAW_BYTES = 2 * TC_BM * TC_RAW_ROW;
+constexpr int TC_EPI = 4, TC_DQ = 8;       // epilogue and dequant warps
+constexpr int TC_MMA_WARP = TC_EPI, TC_TMA_WARP = TC_EPI + 1, TC_DQ0 = TC_EPI + 2;
+constexpr int TC_THREADS = (TC_EPI + 2 + TC_DQ) * 32;
+constexpr uint64_t TC_LIMIT_NS = 2000000000ull;
+constexpr uint32_t TC_TMEM_COLS = 512;
+
+// Tile of a contraction: kind 0 = routed expert e, 1 = shared expert; brow =
+// first row of the token operand (a route position for routed tiles, a token
+// for shared ones); n tokens; blk = 128-row block of weights.
+struct TcTile {
+  int kind, e, brow, n, blk;
+};
+
+struct TcArgs {
+  int D, F, Fs, P, T;
+  const uint8_t *experts;
+  int64_t expert_bytes, gate_bytes;
+  const int4 *tiles;
+  const int *n_tiles;
+  uint16_t *h16;  // fp16: routed rows [P][F] (K order permuted), then shared rows [T][Fs]
+  float *y;       // [P][D] routed outputs, perm order
+  float *ys;      // [T][D] shared output
+  unsigned *status;
+};
+
+__device__ __forceinline__ TcTile tile_at(const int4 *list, int i) {
+  const int4 v = list[i];
+  return TcTile{v.x, v.y, v.z, v.w & 0xFFFF, v.w >> 16};
+}
+
+// ------------------------------------------------------------ PTX wrappers --
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
+// layout (8-row groups 1024 bytes apart), start address `addr`.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset: 8 rows x 128 bytes
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulation, both operands
+// K-major, M = 128, N = n (a multiple of 16 up to 256); bf16 when ab_bf16.
+__device__ __forceinline__ uint32_t f16_idesc(int n, bool ab_bf16) {
+  uint32_t d = 1u << 4;                   // D format fp32
+  if (ab_bf16) d |= (1u << 7) | (1u << 10);
+  d |= (uint32_t)(n >> 3) << 17;
+  d |= (uint32_t)(TC_BM >> 4) << 24;
+  return d;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct TcShared {
+  uint64_t full[TC_STAGES], empty[TC_STAGES];
+  uint64_t raw_full[TC_RAW_SLOTS], raw_empty[TC_RAW_SLOTS];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem;
+  int abort_;
+};
+
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t par, TcShared &S, unsigned *status) {
+  if (mbar_try_wait(bar, par)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, par)) {
+    if (*(volatile int *)&S.abort_) return false;
+    if (globaltimer_ns() - t0 > TC_LIMIT_NS) {
+      flag(status, ST_TIMEOUT);
+      *(volatile int *)&S.abort_ = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// K of a tile and its 256-weight blocks.
+template <bool GU>
+__device__ __forceinline__ int tile_k(const TcArgs &a, const TcTile &t) {
+  return GU ? a.D : (t.kind == 0 ? a.F : a.Fs);
+}
+
+// The fp16 pair (v[qa], v[qb]) for the selector nibbles built below: lut_lo
+// holds v0 | v1 << 16, lut_hi v2 | v3 << 16.
+__device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(sel));
+  return r;
+}
+
+// Dequantise sub-block s (16 weights) of one Q2_K block held at `blk` into
+// the two 16-byte chunks of its K positions (the order described at the top
+// of the file): chunk 0 = positions 0-7, chunk 1 = positions 8-15.
+__device__ __forceinline__ void dequant_sub(const uint8_t *blk, int s, uint4 &c0, uint4 &c1) {
+  const uint32_t codes = *reinterpret_cast<const uint32_t *>(blk + 16 + 4 * s);
+  const uint32_t scw = *reinterpret_cast<const uint32_t *>(blk + 4 * (s >> 2));
+  const uint32_t dd = *reinterpret_cast<const uint32_t *>(blk + 80);
+  const uint32_t scm = (scw >> (8 * (s & 3))) & 0xFFu;
+  const float d = fp16_to_f32((uint16_t)(dd & 0xFFFFu)), dmin = fp16_to_f32((uint16_t)(dd >> 16));
+  const float av = d * (float)(scm & 15u), bv = dmin * (float)(scm >> 4);  // both exact
+  const __half2 v01 = __floats2half2_rn(-bv, fmaf(av, 1.f, -bv));
+  const __half2 v23 = __floats2half2_rn(fmaf(av, 2.f, -bv), fmaf(av, 3.f, -bv));
+  const uint32_t lo = *reinterpret_cast<const uint32_t *>(&v01);
+  const uint32_t hi = *reinterpret_cast<const uint32_t *>(&v23);
+  uint32_t w[8];
+#pragma unroll
+  for (int sh = 0; sh < 4; ++sh) {
+    // bytes c of y: code of weight 4c + sh; nibbles 2q, 2q + 1 select v_q
+    const uint32_t y = (codes >> (2 * sh)) & 0x03030303u;
+    const uint32_t sel = y * 0x22u + 0x10101010u;
+    w[2 * sh] = prmt(lo, hi, sel);            // weights sh, 4 + sh
+    w[2 * sh + 1] = prmt(lo, hi, sel >> 16);  // weights 8 + sh, 12 + sh
+  }
+  c0 = make_uint4(w[0], w[1], w[2], w[3]);
+  c1 = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Byte offset of 16-byte chunk c (K elements 8c..8c+7) of row r in a
+// 128-byte-swizzled K-major tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Iteration over this block's tiles and their 256-wide K blocks.
+struct TileWalk {
+  int ti, kb, nkb;
+  TcTile t;
+};
+
+template <bool GU>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_gemm_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tm_b_routed,
+                   const __grid_constant__ CUtensorMap tm_b_shared, const __grid_constant__ CUtensorMap tm_a0,
+                   const __grid_constant__ CUtensorMap tm_a1) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *stages = smem;
+  uint8_t *raw = smem + TC_STAGES * TC_STAGE_BYTES;
+  TcShared &S = *reinterpret_cast<TcShared *>(raw + TC_RAW_SLOTS * TC_RAW_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, bid = blockIdx.x;
+  const int n_tiles = *a.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < TC_STAGES; ++i) {
+      mbar_init(&S.full[i], 1 + TC_DQ);
+      mbar_init(&S.empty[i], 1);
+    }
+    for (int i = 0; i < TC_RAW_SLOTS; ++i) {
+      mbar_init(&S.raw_full[i], 1);
+      mbar_init(&S.raw_empty[i], TC_DQ);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.acc_full[i], 1);
+      mbar_init(&S.acc_empty[i], TC_EPI);
+    }
+    mbar_init(&S.drain, 1);
+    S.abort_ = 0;
+    fence_mbar_init();
+  }
+  if (warp == TC_MMA_WARP) {  // the whole warp allocates the accumulators
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&S.tmem)),
+                 "r"(TC_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem;
+
+  if (warp == TC_TMA_WARP) {
+    // -------------------------------------------------- copies (one warp) --
+    // Raw Q2_K blocks (one 96-byte copy per weight row and 256-wide K block)
+    // of the routed tiles run ahead of the stages: when the stages of the
+    // routed block c begin, blocks up to c + 2 are issued.  (ri, rkb) walks
+    // the routed blocks in the order the dequant warps consume them.
+    int st_it = 0, rawq = 0, rawpos = 0, ri = 0, rkb = 0;
+    bool ok = true;
+    auto issue_raw = [&]() -> int {  // 1 issued, 0 none left, -1 failed wait
+      for (;;) {
+        if (bid + G * ri >= n_tiles) return 0;
+        const TcTile t = tile_at(a.tiles, bid + G * ri);
+        if (t.kind == 0 && rkb < tile_k<GU>(a, t) / QK) break;
+        ++ri;
+        rkb = 0;
+      }
+      const TcTile t = tile_at(a.tiles, bid + G * ri);
+      const int slot = rawq % TC_RAW_SLOTS;
+      if (rawq >= TC_RAW_SLOTS) {
+        int w = 1;
+        if (lane == 0) w = tc_wait(&S.raw_empty[slot], ((rawq / TC_RAW_SLOTS) & 1) ^ 1, S, a.status);
+        if (!__shfl_sync(0xffffffffu, w, 0)) return -1;
+      }
+      const int rows = GU ? 2 * TC_BM : TC_BM;
+      if (lane == 0) mbar_arrive_expect_tx(&S.raw_full[slot], rows * TC_RAW_ROW);
+      __syncwarp();
+      const int64_t rowb = GU ? (int64_t)(a.D / QK) * QB : (int64_t)(a.F / QK) * QB;
+      const uint8_t *base = a.experts + (int64_t)t.e * a.expert_bytes + (GU ? 0 : 2 * a.gate_bytes);
+      const uint32_t src_off = (uint32_t)(QB * rkb) & ~15u;  // 16-byte aligned start of the block's copy
+      for (int r = lane; r < rows; r += 32) {
+        const int m = r / TC_BM, rr = r % TC_BM;
+        const uint8_t *src = base + (int64_t)m * a.gate_bytes + ((int64_t)t.blk * TC_BM + rr) * rowb + src_off;
+        bulk_g2s(raw + (size_t)slot * TC_RAW_BYTES + (size_t)r * TC_RAW_ROW, src, TC_RAW_ROW, &S.raw_full[slot]);
+      }
+      ++rawq;
+      ++rkb;
+      return 1;
+    };
+    for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
+      const TcTile t = tile_at(a.tiles, bid + G * i);
+      const int nk = tile_k<GU>(a, t) / TC_BK;
+      const int nb = (t.n + 15) & ~15;
+      const bool routed = t.kind == 0;
+      for (int kc = 0; ok && kc < nk; ++kc) {
+        if (routed && (kc & 3) == 0) {
+          ++rawpos;
+          while (rawq < rawpos + 2) {
+            const int r = issue_raw();
+            if (r < 0) ok = false;
+            if (r <= 0) break;
+          }
+          if (!ok) break;
+        }
+        const int s = st_it % TC_STAGES;
+        if (st_it >= TC_STAGES) {
+          int w = 1;
+          if (lane == 0) w = tc_wait(&S.empty[s], ((st_it / TC_STAGES) & 1) ^ 1, S, a.status);
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        }
+        uint8_t *stage = stages + (size_t)s * TC_STAGE_BYTES;
+        if (lane == 0) {
+          const int nbox = (nb + 31) / 32;
+          uint32_t bytes = (uint32_t)nbox * 32 * 128;
+          if (!routed) bytes += (GU ? 2 : 1) * TC_TILE_BYTES;
+          mbar_arrive_expect_tx(&S.full[s], bytes);
+          uint8_t *bdst = stage + (GU ? 2 : 1) * TC_TILE_BYTES;
+          const CUtensorMap *bm = routed ? &tm_b_routed : &tm_b_shared;
+          for (int bx = 0; bx < nbox; ++bx) tma_load_2d(bdst + bx * 32 * 128, bm, kc * TC_BK, t.brow + 32 * bx, &S.full[s]);
+          if (!routed) {
+            tma_load_2d(stage, &tm_a0, kc * TC_BK, t.blk * TC_BM, &S.full[s]);
+            if (GU) tma_load_2d(stage + TC_TILE_BYTES, &tm_a1, kc * TC_BK, t.blk * TC_BM, &S.full[s]);
+          }
+        }
+        __syncwarp();
+        ++st_it;
+      }
+    }
+    // every copy issued has landed before the block may end
+    if (lane == 0) {
+      for (int q = st_it > TC_STAGES ? st_it - TC_STAGES : 0; q < st_it; ++q) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&S.full[q % TC_STAGES], (q / TC_STAGES) & 1))
+          if (globaltimer_ns() - t0 > TC_LIMIT_NS) { flag(a.status, ST_TIMEOUT); break; }
+      }
+      for (int q = rawq > TC_RAW_SLOTS ? rawq - TC_RAW_SLOTS : 0; q < rawq; ++q) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&S.raw_full[q % TC_RAW_SLOTS], (q / TC_RAW_SLOTS) & 1))
+          if (globaltimer_ns() - t0 > TC_LIMIT_NS) { flag(a.status, ST_TIMEOUT); break; }
+      }
+    }
+  } else if (warp >= TC_DQ0) {
+    // ------------------------------------------------------ dequant warps --
+    const int dt = threadIdx.x - TC_DQ0 * 32;  // 0 .. 32 TC_DQ - 1
+    int st_it = 0, raw_it = 0;
+    bool ok = true;
+    for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
+      const TcTile t = tile_at(a.tiles, bid + G * i);
+      const int K = tile_k<GU>(a, t), nk = K / TC_BK;
+      const bool routed = t.kind == 0;
+      const int rows = GU ? 2 * TC_BM : TC_BM;
+      for (int kc = 0; ok && kc < nk; ++kc) {
+        const int slot = raw_it % TC_RAW_SLOTS;
+        if (routed && (kc & 3) == 0 && !tc_wait(&S.raw_full[slot], (raw_it / TC_RAW_SLOTS) & 1, S, a.status)) {
+          ok = false;
+          break;
+        }
+        const int s = st_it % TC_STAGES;
+        if (st_it >= TC_STAGES && !tc_wait(&S.empty[s], ((st_it / TC_STAGES) & 1) ^ 1, S, a.status)) {
+          ok = false;
+          break;
+        }
+        if (routed) {
+          uint8_t *stage = stages + (size_t)s * TC_STAGE_BYTES;
+          const uint8_t *rs = raw + (size_t)slot * TC_RAW_BYTES;
+          const uint32_t boff = (uint32_t)(QB * (kc >> 2)) & 15u;  // block start inside its 96-byte copy
+          const int q4 = kc & 3;                                  // quarter of the block in this stage
+          // unit: (row, sub-block j of the four in this stage)
+          for (int u = dt; u < rows * 4; u += TC_DQ * 32) {
+            const int r = u >> 2, j = u & 3;
+            uint4 c0, c1;
+            dequant_sub(rs + (size_t)r * TC_RAW_ROW + boff, 4 * q4 + j, c0, c1);
+            uint8_t *tile = stage + (size_t)(r / TC_BM) * TC_TILE_BYTES;
+            const int rr = r % TC_BM;
+            *reinterpret_cast<uint4 *>(tile + sw128_off(rr, 2 * j)) = c0;
+            *reinterpret_cast<uint4 *>(tile + sw128_off(rr, 2 * j + 1)) = c1;
+          }
+          fence_proxy_async();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.full[s]);
+        if (routed && (kc & 3) == 3) {
+          if (lane == 0) mbar_arrive(&S.raw_empty[slot]);
+          ++raw_it;
+        }
+        ++st_it;
+      }
+    }
+  } else if (warp == TC_MMA_WARP) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int st_it = 0;
+      bool ok = true;
+      for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
+        const TcTile t = tile_at(a.tiles, bid + G * i);
+        const int K = tile_k<GU>(a, t), nk = K / TC_BK;
+        const int nb = (t.n + 15) & ~15;
+        const int buf = i & 1;
+        if (i >= 2 && !tc_wait(&S.acc_empty[buf], ((i >> 1) & 1) ^ 1, S, a.status)) break;
+        tc_fence_after();
+        const uint32_t idesc = f16_idesc(nb, GU && t.kind == 1);
+        const uint32_t d0 = tmem + (uint32_t)(buf * 256);
+        for (int kc = 0; kc < nk; ++kc) {
+          const int s = st_it % TC_STAGES;
+          if (!tc_wait(&S.full[s], (st_it / TC_STAGES) & 1, S, a.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sbase = smem_u32(stages + (size_t)s * TC_STAGE_BYTES);
+          const uint32_t bbase = sbase + (GU ? 2 : 1) * TC_TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; ++kk) {
+            const bool acc = kc > 0 || kk > 0;
+            const uint64_t bd = sw128_desc(bbase + 32 * kk);
+            mma_f16(d0, sw128_desc(sbase + 32 * kk), bd, idesc, acc);
+            if (GU) mma_f16(d0 + 128, sw128_desc(sbase + TC_TILE_BYTES + 32 * kk), bd, idesc, acc);
+          }
+          mma_commit(&S.empty[s]);  // the stage is free once these MMAs have read it
+          ++st_it;
+        }
+        if (!ok) break;
+        mma_commit(&S.acc_full[buf]);
+      }
+      // nothing of this thread may still run when the accumulators are freed
+      mma_commit(&S.drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&S.drain, 0))
+        if (globaltimer_ns() - t0 > TC_LIMIT_NS) { flag(a.status, ST_TIMEOUT); break; }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ epilogue warps --
+    const int q = warp;  // TMEM lanes 32 q .. 32 q + 31
+    const int r = 32 * q + lane;
+    for (int i = 0; bid + G * i < n_tiles; ++i) {
+      const TcTile t = tile_at(a.tiles, bid + G * i);
+      const int buf = i & 1;
+      if (!tc_wait(&S.acc_full[buf], (i >> 1) & 1, S, a.status)) break;
+      tc_fence_after();
+      const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256);
+      if (GU) {
+        const int f = t.blk * TC_BM + r;
+        const int ld = t.kind == 0 ? a.F : a.Fs;
+        // routed h is stored in the permuted K order of the down weights
+        uint16_t *hrow = t.kind == 0 ? a.h16 + (int64_t)t.brow * a.F + (f & ~15) + 4 * (f & 3) + ((f & 15) >> 2)
+                                     : a.h16 + (int64_t)a.P * a.F + (int64_t)t.brow * a.Fs + f;
+        for (int j0 = 0; j0 < t.n; j0 += 16) {
+          float g[16], u[16];
+          tmem_ld16(tl + j0, g);
+          tmem_ld16(tl + 128 + j0, u);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j0 + j < t.n) {
+              const float hv = silu(g[j]) * u[j];
+              hrow[(int64_t)(j0 + j) * ld] = __half_as_ushort(__float2half_rn(hv));
+            }
+        }
+      } else {
+        const int d = t.blk * TC_BM + r;
+        float *orow = (t.kind == 0 ? a.y : a.ys) + (int64_t)t.brow * a.D + d;
+        for (int j0 = 0; j0 < t.n; j0 += 16) {
+          float v[16];
+          tmem_ld16(tl + j0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j0 + j < t.n) orow[(int64_t)(j0 + j) * a.D] = v[j];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acc_empty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == TC_MMA_WARP) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS) : "memory");
+  }
+}
+
+// ------------------------------------------------------------ small kernels --
+
+// Token rows gathered into route order, bf16 -> fp16, each group of 16 in
+// the permuted K order: xp[p][16 g + i] = x[perm[p] / k][16 g + 4 (i % 4) + i / 4].
+__global__ void __launch_bounds__(256) gather_x16_kernel(const uint16_t *__restrict__ x,
+                                                         const int32_t *__restrict__ perm, int64_t P,
+                                                         int D, int k, uint16_t *__restrict__ xp,
+                                                         unsigned *status) {
+  const int ng = D / 16;
+  const int64_t n = P * ng;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t p = i / ng;
+    const int g = (int)(i % ng);
+    const int32_t q = perm[p];
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)(q / k) * D + 16 * g);
+    const uint4 s0 = src[0], s1 = src[1];
+    const uint32_t w[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[2 * j] = __uint_as_float(w[j] << 16);
+      v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    bool over = false;
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float a0 = v[4 * ((2 * j) & 3) + (2 * j) / 4], a1 = v[4 * ((2 * j + 1) & 3) + (2 * j + 1) / 4];
+      over |= fabsf(a0) > 65504.f || fabsf(a1) > 65504.f;
+      a0 = fminf(fmaxf(a0, -65504.f), 65504.f);
+      a1 = fminf(fmaxf(a1, -65504.f), 65504.f);
+      const __half2 h = __floats2half2_rn(a0, a1);
+      o[j] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    if (over) flag(status, ST_RANGE);
+    uint4 *dst = reinterpret_cast<uint4 *>(xp + p * D + 16 * g);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+// bf16 -> fp16 copy of a matrix (the shared down weights).
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint16_t *__restrict__ src, int64_t n8,
+                                                          uint16_t *__restrict__ dst, unsigned *status) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 s = reinterpret_cast<const uint4 *>(src)[i];
+    const uint32_t w[4] = {s.x, s.y, s.z, s.w};
+    uint32_t o[4];
+    bool over = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float a0 = __uint_as_float(w[j] << 16), a1 = __uint_as_float(w[j] & 0xFFFF0000u);
+      over |= fabsf(a0) > 65504.f || fabsf(a1) > 65504.f;
+      a0 = fminf(fmaxf(a0, -65504.f), 65504.f);
+      a1 = fminf(fmaxf(a1, -65504.f), 65504.f);
+      const __half2 h = __floats2half2_rn(a0, a1);
+      o[j] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    if (over) flag(status, ST_RANGE);
+    reinterpret_cast<uint4 *>(dst)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Tile lists of both contractions from the route: shared-expert tiles
+// first (full token chunks), then per expert its token chunks times the
+// weight-row blocks (chunk-major, so neighbouring tiles share token rows).
+// One block of 1024 threads, one thread per expert.
+__global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict__ counts,
+                                                       const int32_t *__restrict__ offsets, int E, int64_t T,
+                                                       int64_t P, int D, int F, int Fs, int4 *__restrict__ gu,
+                                                       int4 *__restrict__ dn, int *__restrict__ n_gu,
+                                                       int *__restrict__ n_dn) {
+  __shared__ int scan_gu[1024], scan_dn[1024];
+  const int e = threadIdx.x;
+  const int ne = e < E ? counts[e] : 0;
+  const int cg = (ne + TC_NGU - 1) / TC_NGU, cd = (ne + TC_NDN - 1) / TC_NDN;
+  const int tg = cg * (F / TC_BM), td = cd * (D / TC_BM);
+  scan_gu[e] = tg;
+  scan_dn[e] = td;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {  // inclusive scans
+    const int a = e >= o ? scan_gu[e - o] : 0, b = e >= o ? scan_dn[e - o] : 0;
+    __syncthreads();
+    scan_gu[e] += a;
+    scan_dn[e] += b;
+    __syncthreads();
+  }
+  const int sg_chunks = Fs > 0 ? (int)((T + TC_NGU - 1) / TC_NGU) : 0;
+  const int sd_chunks = Fs > 0 ? (int)((T + TC_NDN - 1) / TC_NDN) : 0;
+  const int n_sg = sg_chunks * (Fs / TC_BM), n_sd = sd_chunks * (D / TC_BM);
+  // shared tiles
+  for (int i = e; i < n_sg; i += 1024) {
+    const int c = i / (Fs / TC_BM), b = i % (Fs / TC_BM);
+    const int t0 = c * TC_NGU, n = (int)min((int64_t)TC_NGU, T - t0);
+    gu[i] = make_int4(1, 0, t0, n | (b << 16));
+  }
+  for (int i = e; i < n_sd; i += 1024) {
+    const int c = i / (D / TC_BM), b = i % (D / TC_BM);
+    const int t0 = c * TC_NDN, n = (int)min((int64_t)TC_NDN, T - t0);
+    dn[i] = make_int4(1, 0, t0, n | (b << 16));
+  }
+  if (e < E && ne > 0) {
+    const int base = offsets[e];
+    int o = n_sg + scan_gu[e] - tg;
+    for (int c = 0; c < cg; ++c)
+      for (int b = 0; b < F / TC_BM; ++b) {
+        const int n = min(TC_NGU, ne - c * TC_NGU);
+        gu[o++] = make_int4(0, e, base + c * TC_NGU, n | (b << 16));
+      }
+    o = n_sd + scan_dn[e] - td;
+    for (int c = 0; c < cd; ++c)
+      for (int b = 0; b < D / TC_BM; ++b) {
+        const int n = min(TC_NDN, ne - c * TC_NDN);
+        dn[o++] = make_int4(0, e, base + c * TC_NDN, n | (b << 16));
+      }
+  }
+  if (e == 1023) {
+    *n_gu = n_sg + scan_gu[1023];
+    *n_dn = n_sd + scan_dn[1023];
+  }
+}
+
+// ---------------------------------------------------------------- host side --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Row-major 16-bit matrix [rows][cols] as a 2-D map with 64 x box_rows boxes
+// in the 128-byte swizzle (zero fill beyond the edges).
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t TC_SMEM = 1024 + TC_STAGES * TC_STAGE_BYTES + TC_RAW_SLOTS * TC_RAW_BYTES + sizeof(TcShared);
+
+}  // namespace
+
+bool prefill_tc_supported(const Shape &sh, int64_t T) {
+  if (T < TC_MIN_T || T > (int64_t)1 << 24) return false;
+  if (sh.x_dtype != DS_BF16 || sh.router_dtype != DS_BF16) return false;
+  if (sh.D % 1024 || sh.F % 1024 || sh.Fs % TC_BM) return false;  // whole 4-block groups: raw copies stay inside rows
+  if (sh.E > 1024 || T * sh.k > ((int64_t)1 << 31) - 1) return false;
+  if ((int64_t)sh.Fs > (int64_t)sh.k * sh.F) return false;  // fp16 h of both kinds fits the fp32 [P][F] region
+  return encode_fn() != nullptr;
+}
+
+size_t prefill_tc_workspace(const Shape &sh, int64_t T) {
+  const int64_t P = T * sh.k;
+  const int64_t n_gu = ((T + TC_NGU - 1) / TC_NGU) * (sh.Fs / TC_BM) + (P / TC_NGU + sh.E) * (sh.F / TC_BM);
+  const int64_t n_dn = ((T + TC_NDN - 1) / TC_NDN) * (sh.D / TC_BM) + (P / TC_NDN + sh.E) * (sh.D / TC_BM);
+  const size_t a = 256;
+  auto up = [&](size_t v) { return (v + a - 1) / a * a; };
+  return up(2 * (size_t)P * sh.D) + up(2 * (size_t)sh.D * std::max(sh.Fs, 1)) + up(16 * (size_t)n_gu) +
+         up(16 * (size_t)n_dn) + up(16);
+}
+
+cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
+                              void *tc_ws, cudaStream_t s) {
+  const int64_t T = wk.T, P = T * sh.k;
+  unsigned *st = status_word();
+  static int sms = 0;
+  static bool attr = false;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  // workspace carve-up (see prefill_tc_workspace)
+  const int64_t n_gu = ((T + TC_NGU - 1) / TC_NGU) * (sh.Fs / TC_BM) + (P / TC_NGU + sh.E) * (sh.F / TC_BM);
+  const int64_t n_dn = ((T + TC_NDN - 1) / TC_NDN) * (sh.D / TC_BM) + (P / TC_NDN + sh.E) * (sh.D / TC_BM);
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  char *p = static_cast<char *>(tc_ws);
+  uint16_t *xp = reinterpret_cast<uint16_t *>(p);
+  p += up(2 * (size_t)P * sh.D);
+  uint16_t *sd16 = reinterpret_cast<uint16_t *>(p);
+  p += up(2 * (size_t)sh.D * std::max(sh.Fs, 1));
+  int4 *tiles_gu = reinterpret_cast<int4 *>(p);
+  p += up(16 * (size_t)n_gu);
+  int4 *tiles_dn = reinterpret_cast<int4 *>(p);
+  p += up(16 * (size_t)n_dn);
+  int *cnt = reinterpret_cast<int *>(p);
+  uint16_t *h16 = reinterpret_cast<uint16_t *>(wk.h);  // [P + T][F] fp16 fits in the fp32 [P][F] region
+
+  cudaError_t e;
+  gather_x16_kernel<<<(unsigned)std::min<int64_t>((P * (sh.D / 16) + 255) / 256, 8 * sms), 256, 0, s>>>(
+      (const uint16_t *)x, wk.perm, P, sh.D, sh.k, xp, st);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (sh.Fs > 0) {
+    const int64_t n8 = (int64_t)sh.D * sh.Fs / 8;
+    bf16_to_f16_kernel<<<(unsigned)std::min<int64_t>((n8 + 255) / 256, 8 * sms), 256, 0, s>>>(
+        (const uint16_t *)W.shared_down, n8, sd16, st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  tc_plan_kernel<<<1, 1024, 0, s>>>(wk.counts, wk.offsets, sh.E, T, P, sh.D, sh.F, sh.Fs, tiles_gu, tiles_dn, cnt,
+                                    cnt + 1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  TcArgs a{};
+  a.D = sh.D; a.F = sh.F; a.Fs = sh.Fs; a.P = (int)P; a.T = (int)T;
+  a.experts = W.experts_q2k;
+  a.expert_bytes = sh.expert_bytes();
+  a.gate_bytes = sh.gate_bytes();
+  a.h16 = h16;
+  a.y = wk.y;
+  a.ys = wk.ys;
+  a.status = st;
+
+  CUtensorMap m_xp, m_x, m_sg, m_su, m_h, m_sd;
+  const int fs1 = std::max(sh.Fs, TC_BM);
+  if (!make_map(&m_xp, xp, P, sh.D, 32, false) || !make_map(&m_x, x, T, sh.D, 32, true) ||
+      !make_map(&m_sg, sh.Fs > 0 ? (const void *)W.shared_gate : (const void *)W.experts_q2k, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
+      !make_map(&m_su, sh.Fs > 0 ? (const void *)W.shared_up : (const void *)W.experts_q2k, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
+      !make_map(&m_h, h16, P, sh.F, 32, false) ||
+      !make_map(&m_sd, sd16, sh.D, fs1, TC_BM, false))
+    return cudaErrorInvalidValue;
+  a.tiles = tiles_gu;
+  a.n_tiles = cnt;
+  tc_gemm_kernel<true><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_xp, m_x, m_sg, m_su);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // the shared rows of h have n_ff_shared columns: their own map
+  CUtensorMap m_hs;
+  if (!make_map(&m_hs, h16 + (size_t)P * sh.F, T, std::max(sh.Fs, 64), 32, false)) return cudaErrorInvalidValue;
+  a.tiles = tiles_dn;
+  a.n_tiles = cnt + 1;
+  tc_gemm_kernel<false><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_h, m_hs, m_sd, m_sd);
+  return cudaGetLastError();
+}
+
+}  // namespace dsm

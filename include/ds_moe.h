@@ -135,8 +135,15 @@ int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, 
  *        its contents need no initialisation and are scratch after return
  *   dbg  optional debug outputs (NULL to skip)
  * Tokens are independent: row t of out depends only on row t of x.
- * T == 0 is a no-op.  Decode-sized batches (T <= 64) use the fused
- * dequantising GEMV path; larger batches use the grouped tensor-core path. */
+ * T == 0 is a no-op.  The kernels that run depend on T and the shape (see
+ * ds_moe_layer_path): one token at the instantiated widths streams the whole
+ * layer through one cooperative kernel; up to four tokens use a three-kernel
+ * decode chain; T >= 64 with bf16 x and router and n_embd, n_ff multiples of
+ * 1024 runs the expert FFNs as grouped tcgen05 GEMMs with fp16 operands
+ * (dequantised weights and activations rounded once to fp16; an |x| or
+ * intermediate above 65504 is saturated and reported by ds_moe_sync_status
+ * as DS_ERR_DEVICE_CHECK); every other case uses the grouped dequantising
+ * GEMV path with fp32 arithmetic. */
 int ds_moe_layer(const ds_moe_shape *shape, const ds_moe_weights *weights, const void *x, int64_t T,
                  float *out, void *workspace, size_t workspace_bytes, const ds_moe_debug *dbg,
                  void *stream, char *err, size_t errlen);
@@ -177,6 +184,18 @@ int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_
  *   (other streams or threads) race on the array: serialise them. */
 int ds_moe_layer_noalloc(const ds_moe_shape *shape, const ds_moe_weights *weights, const void *x,
                          int64_t T, float *out, void *stream, char *err, size_t errlen);
+
+/* Which kernels ds_moe_layer runs for T tokens of this shape with this x
+ * pointer (host call; nothing is launched).  Returns one of the DS_PATH_*
+ * values, or DS_ERR_INVALID_ARG for a shape ds_moe_layer would reject. */
+enum {
+  DS_PATH_NONE = 0,          /* T == 0 */
+  DS_PATH_STREAM = 1,        /* one token: router kernel + one cooperative streaming kernel */
+  DS_PATH_DECODE3 = 2,       /* T <= 4: router, gate/up and down kernels chained */
+  DS_PATH_GROUPED_GEMV = 3,  /* route kernels + grouped dequantising GEMVs + combine */
+  DS_PATH_TENSOR_CORE = 4    /* route kernels + grouped tcgen05 GEMMs + combine */
+};
+int ds_moe_layer_path(const ds_moe_shape *shape, int64_t T, const void *x);
 
 /* Synchronise `stream`, then read and clear this device's sticky status
  * word.  Returns DS_OK, DS_ERR_TIMEOUT or DS_ERR_DEVICE_CHECK (with a message

@@ -103,3 +103,13 @@ def test_quantize_rejects_bad_arguments_on_host(L):
     assert L.ds_moe_quantize_q2k(16, -1, 256, 16, None, err, 256) == ds.DS_ERR_INVALID_ARG
     assert L.ds_moe_quantize_q2k(18, 4, 256, 16, None, err, 256) == ds.DS_ERR_INVALID_ARG
     assert L.ds_moe_quantize_q2k(16, 0, 256, 16, None, err, 256) == ds.DS_OK
+
+
+def test_layer_path_host_checks(L):
+    sh = ds.MoEShape(4096, 256, 2048, 2048, 6)
+    assert ds.layer_path(sh, 0) == ds.PATH_NONE
+    assert ds.layer_path(sh, 8) in (ds.PATH_DECODE3, ds.PATH_GROUPED_GEMV)
+    with pytest.raises(ds.DsMoeError):
+        ds.layer_path(ds.MoEShape(4000, 256, 2048, 2048, 6), 4)
+    with pytest.raises(ds.DsMoeError):
+        ds.layer_path(sh, -1)

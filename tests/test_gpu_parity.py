@@ -220,6 +220,40 @@ def test_tiny_prefill_sized_batch():
     layer_parity(c, PREFILL_TOL)
 
 
+def _tc(T, Fs, k, E, zipf=0.0, seed=7):
+    from dataclasses import replace
+    return replace(dsgen.TINY, name=f"tc D=1024 F=1024 T={T} Fs={Fs} k={k} E={E} zipf={zipf}", T=T,
+                   D=1024, F=1024, E=E, k=k, Fs=Fs, shared_sigma=0.02, x_dtype="bf16",
+                   router_dtype="bf16", router_sigma=0.02, zipf_s=zipf, seed=seed)
+
+
+@pytest.mark.parametrize("T,Fs,k,E,zipf", [(300, 1024, 4, 16, 0.0), (64, 1024, 2, 8, 0.0),
+                                            (200, 0, 6, 40, 0.0), (520, 1024, 6, 32, 1.1)])
+def test_prefill_tensor_core_path(T, Fs, k, E, zipf):
+    """Batches of 64 tokens or more with bf16 inputs and widths that are
+    multiples of 1024 run the expert FFNs as grouped tcgen05 GEMMs: the whole
+    output against the oracle at the prefill tolerance.  The cases cover the
+    smallest batch of the path, several 128-token chunks per expert (ragged
+    last chunks), no shared expert, an odd expert count, and a Zipf-skewed
+    route whose hottest experts exceed one 256-token down chunk."""
+    cfg = _tc(T, Fs, k, E, zipf)
+    assert ds.layer_path(synthetic.shape_of(cfg), T) == ds.PATH_TENSOR_CORE
+    layer_parity(cfg, PREFILL_TOL)
+
+
+def test_layer_path_selection():
+    """The kernels each decode and prefill workload runs on."""
+    from dataclasses import replace
+    sh = synthetic.shape_of(dsgen.DECODE1)
+    assert ds.layer_path(sh, 0) == ds.PATH_NONE
+    assert ds.layer_path(sh, 1) == ds.PATH_STREAM
+    assert ds.layer_path(sh, 4) == ds.PATH_DECODE3
+    assert ds.layer_path(sh, 32) == ds.PATH_GROUPED_GEMV
+    assert ds.layer_path(synthetic.shape_of(dsgen.PREFILL), 4096) == ds.PATH_TENSOR_CORE
+    assert ds.layer_path(synthetic.shape_of(dsgen.TINY), 700) == ds.PATH_GROUPED_GEMV  # fp32 x
+    assert ds.layer_path(synthetic.shape_of(replace(dsgen.DECODE1, T=1)), 64) == ds.PATH_TENSOR_CORE
+
+
 @pytest.fixture(scope="module")
 def decode1():
     cfg = dsgen.DECODE1
