@@ -13,7 +13,8 @@
 // wastes no more than 15 columns.  Per tile and 64-wide K step:
 //
 //   dequant warps  Q2_K rows -> fp16 in the 128-byte swizzled K-major layout
-//                  of the MMA, from raw 96-byte block copies that the copy
+//                  of the MMA, from raw copies (96 bytes per row holding one
+//                  84-byte block, 128 rows per tensor copy) that the copy
 //                  warp stages in shared memory two blocks ahead;
 //   copy warp      bulk-tensor (TMA) loads of the token rows (fp16) and, for
 //                  the dense shared expert, of its weight rows;
@@ -87,6 +88,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -229,11 +239,14 @@ struct TileWalk {
 
 template <bool GU>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    tc_gemm_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tm_b_routed,
+    tc_gemm_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tm_raw,
+                   const __grid_constant__ CUtensorMap tm_b_routed,
                    const __grid_constant__ CUtensorMap tm_b_shared, const __grid_constant__ CUtensorMap tm_a0,
                    const __grid_constant__ CUtensorMap tm_a1) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  // 1024-byte aligned base (the swizzle pattern repeats every 1024 bytes);
+  // derived from the array itself so that accesses stay shared-memory ones
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *stages = smem;
   uint8_t *raw = smem + TC_STAGES * TC_STAGE_BYTES;
   TcShared &S = *reinterpret_cast<TcShared *>(raw + TC_RAW_SLOTS * TC_RAW_BYTES);
@@ -293,16 +306,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!__shfl_sync(0xffffffffu, w, 0)) return -1;
       }
       const int rows = GU ? 2 * TC_BM : TC_BM;
-      if (lane == 0) mbar_arrive_expect_tx(&S.raw_full[slot], rows * TC_RAW_ROW);
-      __syncwarp();
-      const int64_t rowb = GU ? (int64_t)(a.D / QK) * QB : (int64_t)(a.F / QK) * QB;
-      const uint8_t *base = a.experts + (int64_t)t.e * a.expert_bytes + (GU ? 0 : 2 * a.gate_bytes);
-      const uint32_t src_off = (uint32_t)(QB * rkb) & ~15u;  // 16-byte aligned start of the block's copy
-      for (int r = lane; r < rows; r += 32) {
-        const int m = r / TC_BM, rr = r % TC_BM;
-        const uint8_t *src = base + (int64_t)m * a.gate_bytes + ((int64_t)t.blk * TC_BM + rr) * rowb + src_off;
-        bulk_g2s(raw + (size_t)slot * TC_RAW_BYTES + (size_t)r * TC_RAW_ROW, src, TC_RAW_ROW, &S.raw_full[slot]);
+      if (lane == 0) {
+        // words [x, x + 24) of 128 weight rows: the 96-byte window, 16-byte
+        // aligned, that holds block rkb of each row
+        mbar_arrive_expect_tx(&S.raw_full[slot], rows * TC_RAW_ROW);
+        const int xw = (int)(((uint32_t)(QB * rkb) & ~15u) >> 2);
+        uint8_t *dst = raw + (size_t)slot * TC_RAW_BYTES;
+        tma_load_3d(dst, &tm_raw, xw, t.blk * TC_BM, t.e, &S.raw_full[slot]);
+        if (GU) tma_load_3d(dst + TC_BM * TC_RAW_ROW, &tm_raw, xw, a.F + t.blk * TC_BM, t.e, &S.raw_full[slot]);
       }
+      __syncwarp();
       ++rawq;
       ++rkb;
       return 1;
@@ -652,6 +665,22 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The Q2_K rows of every expert as a 3-D map of 32-bit words: x = word in
+// a row, y = row (gate rows then up rows, or down rows), z = expert; boxes
+// of 24 words x 128 rows.
+bool make_raw_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int64_t E,
+                  int64_t expert_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)rows, (cuuint64_t)E};
+  const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_bytes};
+  const cuuint32_t box[3] = {TC_RAW_ROW / 4, (cuuint32_t)TC_BM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr size_t TC_SMEM = 1024 + TC_STAGES * TC_STAGE_BYTES + TC_RAW_SLOTS * TC_RAW_BYTES + sizeof(TcShared);
 
 }  // namespace
@@ -741,16 +770,21 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
       !make_map(&m_h, h16, P, sh.F, 32, false) ||
       !make_map(&m_sd, sd16, sh.D, fs1, TC_BM, false))
     return cudaErrorInvalidValue;
+  CUtensorMap m_rgu, m_rdn;
+  if (!make_raw_map(&m_rgu, W.experts_q2k, (int64_t)(sh.D / QK) * QB, 2 * (int64_t)sh.F, sh.E, sh.expert_bytes()) ||
+      !make_raw_map(&m_rdn, W.experts_q2k + 2 * sh.gate_bytes(), (int64_t)(sh.F / QK) * QB, sh.D, sh.E,
+                    sh.expert_bytes()))
+    return cudaErrorInvalidValue;
   a.tiles = tiles_gu;
   a.n_tiles = cnt;
-  tc_gemm_kernel<true><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_xp, m_x, m_sg, m_su);
+  tc_gemm_kernel<true><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_rgu, m_xp, m_x, m_sg, m_su);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the shared rows of h have n_ff_shared columns: their own map
   CUtensorMap m_hs;
   if (!make_map(&m_hs, h16 + (size_t)P * sh.F, T, std::max(sh.Fs, 64), 32, false)) return cudaErrorInvalidValue;
   a.tiles = tiles_dn;
   a.n_tiles = cnt + 1;
-  tc_gemm_kernel<false><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_h, m_hs, m_sd, m_sd);
+  tc_gemm_kernel<false><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_rdn, m_h, m_hs, m_sd, m_sd);
   return cudaGetLastError();
 }
 
