@@ -140,12 +140,15 @@ int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *ou
   } else {
     if ((e = cudaMemsetAsync(wk.ctrl, 0, 256, s)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "workspace control reset");
-    if ((e = launch_route(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
     if (wk.tc && aligned(x, 16) && prefill_tc_supported(sh, wk.T)) {
+      if ((e = launch_router_tc(sh, W, x, wk, s)) != cudaSuccess)
+        return cuda_fail(err, errlen, e, "router (tensor cores)");
+      if ((e = launch_select_route(sh, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
       if ((e = launch_prefill_tc(sh, W, x, wk, wk.tc, s)) != cudaSuccess)
         return cuda_fail(err, errlen, e, "expert FFN (tensor cores)");
-    } else if ((e = launch_decode_ffn(sh, W, x, wk, s)) != cudaSuccess) {
-      return cuda_fail(err, errlen, e, "expert FFN");
+    } else {
+      if ((e = launch_route(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
+      if ((e = launch_decode_ffn(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "expert FFN");
     }
     if ((e = launch_combine(sh, wk, out, accumulate, s)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "combine");

@@ -40,6 +40,8 @@ cudaError_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t in_dim, fl
 // stable permutation, used-expert list).
 cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
                          cudaStream_t s);
+// The part of launch_route after the logits: selection and route.
+cudaError_t launch_select_route(const Shape &sh, const Work &wk, cudaStream_t s);
 
 // Decode path: grouped dequantising GEMVs and the combine.
 cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const void *x,
@@ -58,6 +60,9 @@ bool prefill_tc_supported(const Shape &sh, int64_t T);
 size_t prefill_tc_workspace(const Shape &sh, int64_t T);
 cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
                               void *tc_ws, cudaStream_t s);
+// Router logits of the tensor-core path (bf16 x and router, tcgen05).
+cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
+                             cudaStream_t s);
 cudaError_t launch_combine(const Shape &sh, const Work &wk, float *out, bool accumulate,
                            cudaStream_t s);
 

@@ -63,8 +63,14 @@ struct TcTile {
   int kind, e, brow, n, blk;
 };
 
+// The three contractions of the path.
+enum { MODE_GU = 0, MODE_DN = 1, MODE_ROUTER = 2 };
+
 struct TcArgs {
-  int D, F, Fs, P, T;
+  int D, F, Fs, P, T, E;
+  int router_tiles;        // MODE_ROUTER: tiles (E / 128 rounded up) x (T / 256 rounded up)
+  float *logits;           // MODE_ROUTER: [T][E]
+  const float *bias;       // MODE_ROUTER: [E] or null
   const uint8_t *experts;
   int64_t expert_bytes, gate_bytes;
   const int4 *tiles;
@@ -184,10 +190,21 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t par, TcShared &S
   return true;
 }
 
-// K of a tile and its 256-weight blocks.
-template <bool GU>
+// K of a tile.
+template <int MODE>
 __device__ __forceinline__ int tile_k(const TcArgs &a, const TcTile &t) {
-  return GU ? a.D : (t.kind == 0 ? a.F : a.Fs);
+  return MODE == MODE_DN ? (t.kind == 0 ? a.F : a.Fs) : a.D;
+}
+
+// Tile i of this launch: from the list, or (router) by position.
+template <int MODE>
+__device__ __forceinline__ TcTile get_tile(const TcArgs &a, int i) {
+  if (MODE == MODE_ROUTER) {
+    const int neb = (a.E + TC_BM - 1) / TC_BM;
+    const int t0 = (i / neb) * TC_NDN;
+    return TcTile{1, 0, t0, min(TC_NDN, a.T - t0), i % neb};
+  }
+  return tile_at(a.tiles, i);
 }
 
 // The fp16 pair (v[qa], v[qb]) for the selector nibbles built below: lut_lo
@@ -237,7 +254,7 @@ struct TileWalk {
   TcTile t;
 };
 
-template <bool GU>
+template <int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tm_raw,
                    const __grid_constant__ CUtensorMap tm_b_routed,
@@ -250,9 +267,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint8_t *stages = smem;
   uint8_t *raw = smem + TC_STAGES * TC_STAGE_BYTES;
   TcShared &S = *reinterpret_cast<TcShared *>(raw + TC_RAW_SLOTS * TC_RAW_BYTES);
+  constexpr bool GU = MODE == MODE_GU;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, bid = blockIdx.x;
-  const int n_tiles = *a.n_tiles;
+  const int n_tiles = MODE == MODE_ROUTER ? a.router_tiles : *a.n_tiles;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < TC_STAGES; ++i) {
@@ -293,12 +311,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     auto issue_raw = [&]() -> int {  // 1 issued, 0 none left, -1 failed wait
       for (;;) {
         if (bid + G * ri >= n_tiles) return 0;
-        const TcTile t = tile_at(a.tiles, bid + G * ri);
-        if (t.kind == 0 && rkb < tile_k<GU>(a, t) / QK) break;
+        const TcTile t = get_tile<MODE>(a, bid + G * ri);
+        if (t.kind == 0 && rkb < tile_k<MODE>(a, t) / QK) break;
         ++ri;
         rkb = 0;
       }
-      const TcTile t = tile_at(a.tiles, bid + G * ri);
+      const TcTile t = get_tile<MODE>(a, bid + G * ri);
       const int slot = rawq % TC_RAW_SLOTS;
       if (rawq >= TC_RAW_SLOTS) {
         int w = 1;
@@ -321,8 +339,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       return 1;
     };
     for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
-      const TcTile t = tile_at(a.tiles, bid + G * i);
-      const int nk = tile_k<GU>(a, t) / TC_BK;
+      const TcTile t = get_tile<MODE>(a, bid + G * i);
+      const int nk = tile_k<MODE>(a, t) / TC_BK;
       const int nb = (t.n + 15) & ~15;
       const bool routed = t.kind == 0;
       for (int kc = 0; ok && kc < nk; ++kc) {
@@ -378,8 +396,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int st_it = 0, raw_it = 0;
     bool ok = true;
     for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
-      const TcTile t = tile_at(a.tiles, bid + G * i);
-      const int K = tile_k<GU>(a, t), nk = K / TC_BK;
+      const TcTile t = get_tile<MODE>(a, bid + G * i);
+      const int K = tile_k<MODE>(a, t), nk = K / TC_BK;
       const bool routed = t.kind == 0;
       const int rows = GU ? 2 * TC_BM : TC_BM;
       for (int kc = 0; ok && kc < nk; ++kc) {
@@ -425,13 +443,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int st_it = 0;
       bool ok = true;
       for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
-        const TcTile t = tile_at(a.tiles, bid + G * i);
-        const int K = tile_k<GU>(a, t), nk = K / TC_BK;
+        const TcTile t = get_tile<MODE>(a, bid + G * i);
+        const int K = tile_k<MODE>(a, t), nk = K / TC_BK;
         const int nb = (t.n + 15) & ~15;
         const int buf = i & 1;
         if (i >= 2 && !tc_wait(&S.acc_empty[buf], ((i >> 1) & 1) ^ 1, S, a.status)) break;
         tc_fence_after();
-        const uint32_t idesc = f16_idesc(nb, GU && t.kind == 1);
+        const uint32_t idesc = f16_idesc(nb, (GU && t.kind == 1) || MODE == MODE_ROUTER);
         const uint32_t d0 = tmem + (uint32_t)(buf * 256);
         for (int kc = 0; kc < nk; ++kc) {
           const int s = st_it % TC_STAGES;
@@ -464,7 +482,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int q = warp;  // TMEM lanes 32 q .. 32 q + 31
     const int r = 32 * q + lane;
     for (int i = 0; bid + G * i < n_tiles; ++i) {
-      const TcTile t = tile_at(a.tiles, bid + G * i);
+      const TcTile t = get_tile<MODE>(a, bid + G * i);
       const int buf = i & 1;
       if (!tc_wait(&S.acc_full[buf], (i >> 1) & 1, S, a.status)) break;
       tc_fence_after();
@@ -485,6 +503,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               const float hv = silu(g[j]) * u[j];
               hrow[(int64_t)(j0 + j) * ld] = __half_as_ushort(__float2half_rn(hv));
             }
+        }
+      } else if (MODE == MODE_ROUTER) {
+        const int e = t.blk * TC_BM + r;
+        const float b = (a.bias && e < a.E) ? a.bias[e] : 0.f;
+        float *orow = a.logits + (int64_t)t.brow * a.E + e;
+        for (int j0 = 0; j0 < t.n; j0 += 16) {
+          float v[16];
+          tmem_ld16(tl + j0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j0 + j < t.n && e < a.E) orow[(int64_t)(j0 + j) * a.E] = v[j] + b;
         }
       } else {
         const int d = t.blk * TC_BM + r;
@@ -685,6 +714,36 @@ constexpr size_t TC_SMEM = 1024 + TC_STAGES * TC_STAGE_BYTES + TC_RAW_SLOTS * TC
 
 }  // namespace
 
+cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
+                             cudaStream_t s) {
+  static int sms = 0;
+  static bool attr = false;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  if (!attr) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t T = wk.T;
+  TcArgs a{};
+  a.D = sh.D; a.F = sh.F; a.Fs = sh.Fs; a.T = (int)T; a.E = sh.E;
+  a.router_tiles = (int)(((sh.E + TC_BM - 1) / TC_BM) * ((T + TC_NDN - 1) / TC_NDN));
+  a.logits = wk.logits;
+  a.bias = W.router_bias;
+  a.status = status_word();
+  CUtensorMap m_wr, m_x;
+  if (!make_map(&m_wr, W.router_w, sh.E, sh.D, TC_BM, true) || !make_map(&m_x, x, T, sh.D, 32, true))
+    return cudaErrorInvalidValue;
+  tc_gemm_kernel<MODE_ROUTER><<<std::min<int>(sms, a.router_tiles), TC_THREADS, TC_SMEM, s>>>(a, m_wr, m_x, m_x,
+                                                                                              m_wr, m_wr);
+  return cudaGetLastError();
+}
+
 bool prefill_tc_supported(const Shape &sh, int64_t T) {
   if (T < TC_MIN_T || T > (int64_t)1 << 24) return false;
   if (sh.x_dtype != DS_BF16 || sh.router_dtype != DS_BF16) return false;
@@ -716,9 +775,11 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   }
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_DN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -777,14 +838,14 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
     return cudaErrorInvalidValue;
   a.tiles = tiles_gu;
   a.n_tiles = cnt;
-  tc_gemm_kernel<true><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_rgu, m_xp, m_x, m_sg, m_su);
+  tc_gemm_kernel<MODE_GU><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_rgu, m_xp, m_x, m_sg, m_su);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the shared rows of h have n_ff_shared columns: their own map
   CUtensorMap m_hs;
   if (!make_map(&m_hs, h16 + (size_t)P * sh.F, T, std::max(sh.Fs, 64), 32, false)) return cudaErrorInvalidValue;
   a.tiles = tiles_dn;
   a.n_tiles = cnt + 1;
-  tc_gemm_kernel<false><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_rdn, m_h, m_hs, m_sd, m_sd);
+  tc_gemm_kernel<MODE_DN><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_rdn, m_h, m_hs, m_sd, m_sd);
   return cudaGetLastError();
 }
 

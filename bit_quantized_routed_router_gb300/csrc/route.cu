@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(ROUTE_CHUNK) route_scatter_kernel(
 cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
                          cudaStream_t s) {
   const int64_t T = wk.T;
-  const int E = sh.E, D = sh.D, k = sh.k;
+  const int E = sh.E, D = sh.D;
   unsigned *st = status_word();
   const int tb = T <= 64 ? (int)T : 16;
   dim3 g((E + 7) / 8, (unsigned)((T + tb - 1) / tb));
@@ -312,7 +312,15 @@ cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  return launch_select_route(sh, wk, s);
+}
+
+cudaError_t launch_select_route(const Shape &sh, const Work &wk, cudaStream_t s) {
+  const int64_t T = wk.T;
+  const int E = sh.E, k = sh.k;
+  unsigned *st = status_word();
   const int64_t P = T * k;
+  cudaError_t err;
   static bool attrs = false;
   if (!attrs) {  // up to 33E+1 ints (E <= 1024: 132 KB) of dynamic shared memory
     err = cudaFuncSetAttribute(select_route_small_kernel,
