@@ -763,7 +763,7 @@ __device__ __forceinline__ int vload(const int *p) { return *(volatile const int
 __device__ bool s_wait(uint64_t *bar, uint32_t par, StreamShared &S, unsigned *status) {
   if (mbar_try_wait(bar, par)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, par)) {
+  while (!mbar_try_wait_sleep(bar, par, 20000u)) {  // sleeps until the phase completes (20 us at most)
     if (vload(&S.abort_)) return false;
     if (globaltimer_ns() - t0 > S_LIMIT_NS) {
       flag(status, ST_TIMEOUT);

@@ -43,13 +43,12 @@ namespace {
 constexpr int TC_BM = 128;                 // weight rows per tile (MMA M)
 constexpr int TC_BK = 64;                  // K per stage: one 128-byte swizzle row
 constexpr int TC_NGU = 128;                // tokens per gate/up tile at most
-constexpr int TC_NDN = 256;                // tokens per down tile at most
-constexpr int TC_STAGES = 3;
+constexpr int TC_NDN = 128;                // tokens per down tile at most
+constexpr int TC_NRT = 256;                // tokens per router tile at most
 constexpr uint32_t TC_TILE_BYTES = TC_BM * 128;       // one 128 x 64 operand tile (16 KB)
-constexpr uint32_t TC_STAGE_BYTES = 3 * TC_TILE_BYTES; // gate/up: A_g, A_u, B; down: A, B (256 rows)
-constexpr int TC_RAW_SLOTS = 3;
 constexpr uint32_t TC_RAW_ROW = 96;        // bytes copied per weight row and 256-weight block
-constexpr uint32_t TC_RAW_BYTES = 2 * TC_BM * TC_RAW_ROW;
+constexpr int TC_MAX_STAGES = 5, TC_MAX_RAW = 3;
+constexpr int TC_TILE_CACHE = 128;         // a block's first tiles, copied to shared memory
 constexpr int TC_EPI = 4, TC_DQ = 8;       // epilogue and dequant warps
 constexpr int TC_MMA_WARP = TC_EPI, TC_TMA_WARP = TC_EPI + 1, TC_DQ0 = TC_EPI + 2;
 constexpr int TC_THREADS = (TC_EPI + 2 + TC_DQ) * 32;
@@ -65,6 +64,19 @@ struct TcTile {
 
 // The three contractions of the path.
 enum { MODE_GU = 0, MODE_DN = 1, MODE_ROUTER = 2 };
+
+// Pipeline shape per contraction: a stage holds A_TILES weight tiles (gate
+// and up, or one) and a token tile of NMAX rows; RAW slots of raw Q2_K
+// blocks (one per 256-wide K block) feed the dequant warps.
+template <int MODE>
+struct TcCfg {
+  static constexpr int A_TILES = MODE == MODE_GU ? 2 : 1;
+  static constexpr int NMAX = MODE == MODE_GU ? TC_NGU : MODE == MODE_DN ? TC_NDN : TC_NRT;
+  static constexpr int STAGES = MODE == MODE_GU ? 3 : MODE == MODE_DN ? 5 : 4;
+  static constexpr int RAW = MODE == MODE_ROUTER ? 1 : 3;
+  static constexpr uint32_t STAGE_BYTES = (A_TILES + NMAX / 128) * TC_TILE_BYTES;
+  static constexpr uint32_t RAW_BYTES = A_TILES * TC_BM * TC_RAW_ROW;
+};
 
 struct TcArgs {
   int D, F, Fs, P, T, E;
@@ -168,18 +180,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
 }
 
 struct TcShared {
-  uint64_t full[TC_STAGES], empty[TC_STAGES];
-  uint64_t raw_full[TC_RAW_SLOTS], raw_empty[TC_RAW_SLOTS];
+  uint64_t full[TC_MAX_STAGES], empty[TC_MAX_STAGES];
+  uint64_t raw_full[TC_MAX_RAW], raw_empty[TC_MAX_RAW];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t drain;
   uint32_t tmem;
   int abort_;
+  int4 tiles[TC_TILE_CACHE];
 };
 
+// Bounded wait for the phase of `bar` with parity `par`.  Each try lets the
+// thread sleep until the phase completes (or 20 us pass), so waiting warps
+// do not take issue slots from the dequantising ones.
 __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t par, TcShared &S, unsigned *status) {
   if (mbar_try_wait(bar, par)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, par)) {
+  while (!mbar_try_wait_sleep(bar, par, 20000u)) {
     if (*(volatile int *)&S.abort_) return false;
     if (globaltimer_ns() - t0 > TC_LIMIT_NS) {
       flag(status, ST_TIMEOUT);
@@ -201,8 +217,8 @@ template <int MODE>
 __device__ __forceinline__ TcTile get_tile(const TcArgs &a, int i) {
   if (MODE == MODE_ROUTER) {
     const int neb = (a.E + TC_BM - 1) / TC_BM;
-    const int t0 = (i / neb) * TC_NDN;
-    return TcTile{1, 0, t0, min(TC_NDN, a.T - t0), i % neb};
+    const int t0 = (i / neb) * TC_NRT;
+    return TcTile{1, 0, t0, min(TC_NRT, a.T - t0), i % neb};
   }
   return tile_at(a.tiles, i);
 }
@@ -215,15 +231,14 @@ __device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel)
   return r;
 }
 
-// Dequantise sub-block s (16 weights) of one Q2_K block held at `blk` into
-// the two 16-byte chunks of its K positions (the order described at the top
-// of the file): chunk 0 = positions 0-7, chunk 1 = positions 8-15.
-__device__ __forceinline__ void dequant_sub(const uint8_t *blk, int s, uint4 &c0, uint4 &c1) {
-  const uint32_t codes = *reinterpret_cast<const uint32_t *>(blk + 16 + 4 * s);
-  const uint32_t scw = *reinterpret_cast<const uint32_t *>(blk + 4 * (s >> 2));
-  const uint32_t dd = *reinterpret_cast<const uint32_t *>(blk + 80);
-  const uint32_t scm = (scw >> (8 * (s & 3))) & 0xFFu;
-  const float d = fp16_to_f32((uint16_t)(dd & 0xFFFFu)), dmin = fp16_to_f32((uint16_t)(dd >> 16));
+// Dequantise one sub-block (16 weights) of a Q2_K block from its code word
+// and scale byte (sc low nibble, m high nibble), d and dmin, into the two
+// 16-byte chunks of its K positions (the order described at the top of the
+// file): chunk 0 = positions 0-7, chunk 1 = positions 8-15.  The four values
+// v_q = fp16(d sc q - dmin m) are computed exactly in fp32 and rounded once;
+// each weight is then a byte permutation of them, selected by its code.
+__device__ __forceinline__ void dequant_codes(uint32_t codes, uint32_t scm, float d, float dmin, uint4 &c0,
+                                              uint4 &c1) {
   const float av = d * (float)(scm & 15u), bv = dmin * (float)(scm >> 4);  // both exact
   const __half2 v01 = __floats2half2_rn(-bv, fmaf(av, 1.f, -bv));
   const __half2 v23 = __floats2half2_rn(fmaf(av, 2.f, -bv), fmaf(av, 3.f, -bv));
@@ -232,27 +247,18 @@ __device__ __forceinline__ void dequant_sub(const uint8_t *blk, int s, uint4 &c0
   uint32_t w[8];
 #pragma unroll
   for (int sh = 0; sh < 4; ++sh) {
-    // bytes c of y: code of weight 4c + sh; nibbles 2q, 2q + 1 select v_q
     const uint32_t y = (codes >> (2 * sh)) & 0x03030303u;
     const uint32_t sel = y * 0x22u + 0x10101010u;
-    w[2 * sh] = prmt(lo, hi, sel);            // weights sh, 4 + sh
-    w[2 * sh + 1] = prmt(lo, hi, sel >> 16);  // weights 8 + sh, 12 + sh
+    w[2 * sh] = prmt(lo, hi, sel);
+    w[2 * sh + 1] = prmt(lo, hi, sel >> 16);
   }
   c0 = make_uint4(w[0], w[1], w[2], w[3]);
   c1 = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-// Byte offset of 16-byte chunk c (K elements 8c..8c+7) of row r in a
-// 128-byte-swizzled K-major tile.
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
-}
-
-// Iteration over this block's tiles and their 256-wide K blocks.
-struct TileWalk {
-  int ti, kb, nkb;
-  TcTile t;
-};
+// Operand tiles are 128 rows x 64 K-elements in the 128-byte swizzle of the
+// MMA descriptors: 16-byte chunk c (K elements 8c..8c+7) of row r sits at
+// byte r * 128 + ((c ^ (r mod 8)) * 16) of the 1024-byte aligned tile.
 
 template <int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -265,6 +271,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // derived from the array itself so that accesses stay shared-memory ones
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *stages = smem;
+  using C = TcCfg<MODE>;
+  constexpr int TC_STAGES = C::STAGES, TC_RAW_SLOTS = C::RAW;
+  constexpr uint32_t TC_STAGE_BYTES = C::STAGE_BYTES, TC_RAW_BYTES = C::RAW_BYTES;
   uint8_t *raw = smem + TC_STAGES * TC_STAGE_BYTES;
   TcShared &S = *reinterpret_cast<TcShared *>(raw + TC_RAW_SLOTS * TC_RAW_BYTES);
   constexpr bool GU = MODE == MODE_GU;
@@ -272,6 +281,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int G = gridDim.x, bid = blockIdx.x;
   const int n_tiles = MODE == MODE_ROUTER ? a.router_tiles : *a.n_tiles;
 
+  if (MODE != MODE_ROUTER)
+    for (int j = threadIdx.x; j < TC_TILE_CACHE && bid + G * j < n_tiles; j += TC_THREADS) S.tiles[j] = a.tiles[bid + G * j];
+  // tile i of this block
+  auto tile_of = [&](int i) -> TcTile {
+    if (MODE == MODE_ROUTER) return get_tile<MODE>(a, bid + G * i);
+    const int4 v = i < TC_TILE_CACHE ? S.tiles[i] : a.tiles[bid + G * i];
+    return TcTile{v.x, v.y, v.z, v.w & 0xFFFF, v.w >> 16};
+  };
   if (threadIdx.x == 0) {
     for (int i = 0; i < TC_STAGES; ++i) {
       mbar_init(&S.full[i], 1 + TC_DQ);
@@ -306,17 +323,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // of the routed tiles run ahead of the stages: when the stages of the
     // routed block c begin, blocks up to c + 2 are issued.  (ri, rkb) walks
     // the routed blocks in the order the dequant warps consume them.
+    if (lane == 0) {  // descriptors into the TMA unit's cache before the first copies
+      const CUtensorMap *maps[5] = {&tm_raw, &tm_b_routed, &tm_b_shared, &tm_a0, &tm_a1};
+      for (int m = 0; m < 5; ++m)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(maps[m])) : "memory");
+    }
     int st_it = 0, rawq = 0, rawpos = 0, ri = 0, rkb = 0;
     bool ok = true;
     auto issue_raw = [&]() -> int {  // 1 issued, 0 none left, -1 failed wait
       for (;;) {
         if (bid + G * ri >= n_tiles) return 0;
-        const TcTile t = get_tile<MODE>(a, bid + G * ri);
+        const TcTile t = tile_of(ri);
         if (t.kind == 0 && rkb < tile_k<MODE>(a, t) / QK) break;
         ++ri;
         rkb = 0;
       }
-      const TcTile t = get_tile<MODE>(a, bid + G * ri);
+      const TcTile t = tile_of(ri);
       const int slot = rawq % TC_RAW_SLOTS;
       if (rawq >= TC_RAW_SLOTS) {
         int w = 1;
@@ -339,9 +361,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       return 1;
     };
     for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
-      const TcTile t = get_tile<MODE>(a, bid + G * i);
+      const TcTile t = tile_of(i);
       const int nk = tile_k<MODE>(a, t) / TC_BK;
-      const int nb = (t.n + 15) & ~15;
       const bool routed = t.kind == 0;
       for (int kc = 0; ok && kc < nk; ++kc) {
         if (routed && (kc & 3) == 0) {
@@ -361,13 +382,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         uint8_t *stage = stages + (size_t)s * TC_STAGE_BYTES;
         if (lane == 0) {
-          const int nbox = (nb + 31) / 32;
-          uint32_t bytes = (uint32_t)nbox * 32 * 128;
-          if (!routed) bytes += (GU ? 2 : 1) * TC_TILE_BYTES;
+          // one box of NMAX token rows (rows past the tile's tokens only feed
+          // accumulator columns that are never read)
+          uint32_t bytes = (uint32_t)C::NMAX * 128;
+          if (!routed) bytes += C::A_TILES * TC_TILE_BYTES;
           mbar_arrive_expect_tx(&S.full[s], bytes);
-          uint8_t *bdst = stage + (GU ? 2 : 1) * TC_TILE_BYTES;
-          const CUtensorMap *bm = routed ? &tm_b_routed : &tm_b_shared;
-          for (int bx = 0; bx < nbox; ++bx) tma_load_2d(bdst + bx * 32 * 128, bm, kc * TC_BK, t.brow + 32 * bx, &S.full[s]);
+          uint8_t *bdst = stage + C::A_TILES * TC_TILE_BYTES;
+          tma_load_2d(bdst, routed ? &tm_b_routed : &tm_b_shared, kc * TC_BK, t.brow, &S.full[s]);
           if (!routed) {
             tma_load_2d(stage, &tm_a0, kc * TC_BK, t.blk * TC_BM, &S.full[s]);
             if (GU) tma_load_2d(stage + TC_TILE_BYTES, &tm_a1, kc * TC_BK, t.blk * TC_BM, &S.full[s]);
@@ -392,14 +413,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else if (warp >= TC_DQ0) {
     // ------------------------------------------------------ dequant warps --
-    const int dt = threadIdx.x - TC_DQ0 * 32;  // 0 .. 32 TC_DQ - 1
+    // Thread dt owns one weight row of every stage: gate/up: row dt (gate
+    // rows, then up rows), all four sub-blocks; down: row dt % 128, sub-blocks
+    // 2 (dt / 128) and the next.  Its raw and destination offsets are fixed.
+    constexpr int NSUB = GU ? 4 : 2;
+    const int dt = threadIdx.x - TC_DQ0 * 32;  // 0 .. 255
+    const int r = GU ? dt : dt % TC_BM;
+    const int jb = GU ? 0 : 2 * (dt / TC_BM);
+    const uint32_t raw_row = (uint32_t)r * TC_RAW_ROW;
+    const uint32_t dst_row = (uint32_t)((r / TC_BM) * TC_TILE_BYTES + (r % TC_BM) * 128);
+    const int x7 = r & 7;
     int st_it = 0, raw_it = 0;
     bool ok = true;
     for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
-      const TcTile t = get_tile<MODE>(a, bid + G * i);
+      const TcTile t = tile_of(i);
       const int K = tile_k<MODE>(a, t), nk = K / TC_BK;
       const bool routed = t.kind == 0;
-      const int rows = GU ? 2 * TC_BM : TC_BM;
       for (int kc = 0; ok && kc < nk; ++kc) {
         const int slot = raw_it % TC_RAW_SLOTS;
         if (routed && (kc & 3) == 0 && !tc_wait(&S.raw_full[slot], (raw_it / TC_RAW_SLOTS) & 1, S, a.status)) {
@@ -411,20 +440,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           ok = false;
           break;
         }
-        if (routed) {
-          uint8_t *stage = stages + (size_t)s * TC_STAGE_BYTES;
-          const uint8_t *rs = raw + (size_t)slot * TC_RAW_BYTES;
-          const uint32_t boff = (uint32_t)(QB * (kc >> 2)) & 15u;  // block start inside its 96-byte copy
-          const int q4 = kc & 3;                                  // quarter of the block in this stage
-          // unit: (row, sub-block j of the four in this stage)
-          for (int u = dt; u < rows * 4; u += TC_DQ * 32) {
-            const int r = u >> 2, j = u & 3;
+        if (routed && dt < (GU ? 2 : 1) * TC_BM * (4 / NSUB)) {
+          uint8_t *dst = stages + (size_t)s * TC_STAGE_BYTES + dst_row;
+          // the block's bytes start (84 kb) mod 16 into its 96-byte copy
+          const uint8_t *blk = raw + (size_t)slot * TC_RAW_BYTES + raw_row + ((uint32_t)(QB * (kc >> 2)) & 15u);
+          const int q4 = kc & 3;  // quarter of the block in this stage: sub-blocks 4 q4 ..
+          const uint32_t scw = *reinterpret_cast<const uint32_t *>(blk + 4 * q4);
+          const uint32_t dd = *reinterpret_cast<const uint32_t *>(blk + 80);
+          const float d = fp16_to_f32((uint16_t)(dd & 0xFFFFu)), dmin = fp16_to_f32((uint16_t)(dd >> 16));
+#pragma unroll
+          for (int jj = 0; jj < NSUB; ++jj) {
+            const int j = jb + jj;
+            const uint32_t codes = *reinterpret_cast<const uint32_t *>(blk + 16 + 4 * (4 * q4 + j));
             uint4 c0, c1;
-            dequant_sub(rs + (size_t)r * TC_RAW_ROW + boff, 4 * q4 + j, c0, c1);
-            uint8_t *tile = stage + (size_t)(r / TC_BM) * TC_TILE_BYTES;
-            const int rr = r % TC_BM;
-            *reinterpret_cast<uint4 *>(tile + sw128_off(rr, 2 * j)) = c0;
-            *reinterpret_cast<uint4 *>(tile + sw128_off(rr, 2 * j + 1)) = c1;
+            dequant_codes(codes, (scw >> (8 * j)) & 0xFFu, d, dmin, c0, c1);
+            *reinterpret_cast<uint4 *>(dst + (((2 * j) ^ x7) << 4)) = c0;
+            *reinterpret_cast<uint4 *>(dst + (((2 * j + 1) ^ x7) << 4)) = c1;
           }
           fence_proxy_async();
         }
@@ -443,7 +474,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int st_it = 0;
       bool ok = true;
       for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
-        const TcTile t = get_tile<MODE>(a, bid + G * i);
+        const TcTile t = tile_of(i);
         const int K = tile_k<MODE>(a, t), nk = K / TC_BK;
         const int nb = (t.n + 15) & ~15;
         const int buf = i & 1;
@@ -456,13 +487,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (!tc_wait(&S.full[s], (st_it / TC_STAGES) & 1, S, a.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sbase = smem_u32(stages + (size_t)s * TC_STAGE_BYTES);
-          const uint32_t bbase = sbase + (GU ? 2 : 1) * TC_TILE_BYTES;
+          const uint32_t bbase = sbase + C::A_TILES * TC_TILE_BYTES;
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk) {
-            const bool acc = kc > 0 || kk > 0;
             const uint64_t bd = sw128_desc(bbase + 32 * kk);
-            mma_f16(d0, sw128_desc(sbase + 32 * kk), bd, idesc, acc);
-            if (GU) mma_f16(d0 + 128, sw128_desc(sbase + TC_TILE_BYTES + 32 * kk), bd, idesc, acc);
+            if (GU) {  // gate and up: two accumulators, interleaved
+              const bool acc = kc > 0 || kk > 0;
+              mma_f16(d0, sw128_desc(sbase + 32 * kk), bd, idesc, acc);
+              mma_f16(d0 + 128, sw128_desc(sbase + TC_TILE_BYTES + 32 * kk), bd, idesc, acc);
+            } else if (MODE == MODE_DN) {
+              // two partial accumulators (even and odd K steps) so that
+              // consecutive MMAs do not chain on one accumulator; the
+              // epilogue adds them
+              mma_f16(d0 + 128 * (kk & 1), sw128_desc(sbase + 32 * kk), bd, idesc, kc > 0 || kk > 1);
+            } else {
+              mma_f16(d0, sw128_desc(sbase + 32 * kk), bd, idesc, kc > 0 || kk > 0);
+            }
           }
           mma_commit(&S.empty[s]);  // the stage is free once these MMAs have read it
           ++st_it;
@@ -482,7 +522,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int q = warp;  // TMEM lanes 32 q .. 32 q + 31
     const int r = 32 * q + lane;
     for (int i = 0; bid + G * i < n_tiles; ++i) {
-      const TcTile t = get_tile<MODE>(a, bid + G * i);
+      const TcTile t = tile_of(i);
       const int buf = i & 1;
       if (!tc_wait(&S.acc_full[buf], (i >> 1) & 1, S, a.status)) break;
       tc_fence_after();
@@ -519,11 +559,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int d = t.blk * TC_BM + r;
         float *orow = (t.kind == 0 ? a.y : a.ys) + (int64_t)t.brow * a.D + d;
         for (int j0 = 0; j0 < t.n; j0 += 16) {
-          float v[16];
+          float v[16], w[16];
           tmem_ld16(tl + j0, v);
+          tmem_ld16(tl + 128 + j0, w);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (j0 + j < t.n) orow[(int64_t)(j0 + j) * a.D] = v[j];
+            if (j0 + j < t.n) orow[(int64_t)(j0 + j) * a.D] = v[j] + w[j];
         }
       }
       tc_fence_before();
@@ -710,7 +751,15 @@ bool make_raw_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t r
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t TC_SMEM = 1024 + TC_STAGES * TC_STAGE_BYTES + TC_RAW_SLOTS * TC_RAW_BYTES + sizeof(TcShared);
+template <int MODE>
+constexpr size_t tc_smem() {
+  return 1024 + TcCfg<MODE>::STAGES * TcCfg<MODE>::STAGE_BYTES + TcCfg<MODE>::RAW * TcCfg<MODE>::RAW_BYTES +
+         sizeof(TcShared);
+}
+static_assert(tc_smem<MODE_GU>() <= 227 * 1024 && tc_smem<MODE_DN>() <= 227 * 1024 &&
+                  tc_smem<MODE_ROUTER>() <= 227 * 1024,
+              "pipeline exceeds the shared memory of a block");
+static_assert(TcCfg<MODE_DN>::STAGES <= TC_MAX_STAGES && TcCfg<MODE_GU>::RAW <= TC_MAX_RAW, "barrier arrays");
 
 }  // namespace
 
@@ -725,21 +774,21 @@ cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const voi
   }
   if (!attr) {
     const cudaError_t e =
-        cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+        cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_ROUTER>());
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int64_t T = wk.T;
   TcArgs a{};
   a.D = sh.D; a.F = sh.F; a.Fs = sh.Fs; a.T = (int)T; a.E = sh.E;
-  a.router_tiles = (int)(((sh.E + TC_BM - 1) / TC_BM) * ((T + TC_NDN - 1) / TC_NDN));
+  a.router_tiles = (int)(((sh.E + TC_BM - 1) / TC_BM) * ((T + TC_NRT - 1) / TC_NRT));
   a.logits = wk.logits;
   a.bias = W.router_bias;
   a.status = status_word();
   CUtensorMap m_wr, m_x;
-  if (!make_map(&m_wr, W.router_w, sh.E, sh.D, TC_BM, true) || !make_map(&m_x, x, T, sh.D, 32, true))
+  if (!make_map(&m_wr, W.router_w, sh.E, sh.D, TC_BM, true) || !make_map(&m_x, x, T, sh.D, TC_NRT, true))
     return cudaErrorInvalidValue;
-  tc_gemm_kernel<MODE_ROUTER><<<std::min<int>(sms, a.router_tiles), TC_THREADS, TC_SMEM, s>>>(a, m_wr, m_x, m_x,
+  tc_gemm_kernel<MODE_ROUTER><<<std::min<int>(sms, a.router_tiles), TC_THREADS, tc_smem<MODE_ROUTER>(), s>>>(a, m_wr, m_x, m_x,
                                                                                               m_wr, m_wr);
   return cudaGetLastError();
 }
@@ -775,11 +824,11 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   }
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_GU>());
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_DN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_DN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_DN>());
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_ROUTER>());
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -825,10 +874,10 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
 
   CUtensorMap m_xp, m_x, m_sg, m_su, m_h, m_sd;
   const int fs1 = std::max(sh.Fs, TC_BM);
-  if (!make_map(&m_xp, xp, P, sh.D, 32, false) || !make_map(&m_x, x, T, sh.D, 32, true) ||
+  if (!make_map(&m_xp, xp, P, sh.D, TC_NGU, false) || !make_map(&m_x, x, T, sh.D, TC_NGU, true) ||
       !make_map(&m_sg, sh.Fs > 0 ? (const void *)W.shared_gate : (const void *)W.experts_q2k, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
       !make_map(&m_su, sh.Fs > 0 ? (const void *)W.shared_up : (const void *)W.experts_q2k, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
-      !make_map(&m_h, h16, P, sh.F, 32, false) ||
+      !make_map(&m_h, h16, P, sh.F, TC_NDN, false) ||
       !make_map(&m_sd, sd16, sh.D, fs1, TC_BM, false))
     return cudaErrorInvalidValue;
   CUtensorMap m_rgu, m_rdn;
@@ -838,14 +887,14 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
     return cudaErrorInvalidValue;
   a.tiles = tiles_gu;
   a.n_tiles = cnt;
-  tc_gemm_kernel<MODE_GU><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_rgu, m_xp, m_x, m_sg, m_su);
+  tc_gemm_kernel<MODE_GU><<<sms, TC_THREADS, tc_smem<MODE_GU>(), s>>>(a, m_rgu, m_xp, m_x, m_sg, m_su);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the shared rows of h have n_ff_shared columns: their own map
   CUtensorMap m_hs;
-  if (!make_map(&m_hs, h16 + (size_t)P * sh.F, T, std::max(sh.Fs, 64), 32, false)) return cudaErrorInvalidValue;
+  if (!make_map(&m_hs, h16 + (size_t)P * sh.F, T, std::max(sh.Fs, 64), TC_NDN, false)) return cudaErrorInvalidValue;
   a.tiles = tiles_dn;
   a.n_tiles = cnt + 1;
-  tc_gemm_kernel<MODE_DN><<<sms, TC_THREADS, TC_SMEM, s>>>(a, m_rdn, m_h, m_hs, m_sd, m_sd);
+  tc_gemm_kernel<MODE_DN><<<sms, TC_THREADS, tc_smem<MODE_DN>(), s>>>(a, m_rdn, m_h, m_hs, m_sd, m_sd);
   return cudaGetLastError();
 }
 
