@@ -70,9 +70,9 @@ enum { MODE_GU = 0, MODE_DN = 1, MODE_ROUTER = 2 };
 // blocks (one per 256-wide K block) feed the dequant warps.
 template <int MODE>
 struct TcCfg {
-  static constexpr int A_TILES = MODE == MODE_GU ? 2 : 1;
+  static constexpr int A_TILES = MODE == MODE_ROUTER ? 1 : 2;  // gate + up, or two 128-row down blocks
   static constexpr int NMAX = MODE == MODE_GU ? TC_NGU : MODE == MODE_DN ? TC_NDN : TC_NRT;
-  static constexpr int STAGES = MODE == MODE_GU ? 3 : MODE == MODE_DN ? 5 : 4;
+  static constexpr int STAGES = MODE == MODE_ROUTER ? 4 : 3;
   static constexpr int RAW = MODE == MODE_ROUTER ? 1 : 3;
   static constexpr uint32_t STAGE_BYTES = (A_TILES + NMAX / 128) * TC_TILE_BYTES;
   static constexpr uint32_t RAW_BYTES = A_TILES * TC_BM * TC_RAW_ROW;
@@ -263,7 +263,8 @@ __device__ __forceinline__ void dequant_codes(uint32_t codes, uint32_t scm, floa
 template <int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tm_raw,
-                   const __grid_constant__ CUtensorMap tm_b_routed,
+                   const __grid_constant__ CUtensorMap tm_b_r32, const __grid_constant__ CUtensorMap tm_b_r64,
+                   const __grid_constant__ CUtensorMap tm_b_r96, const __grid_constant__ CUtensorMap tm_b_routed,
                    const __grid_constant__ CUtensorMap tm_b_shared, const __grid_constant__ CUtensorMap tm_a0,
                    const __grid_constant__ CUtensorMap tm_a1) {
   extern __shared__ uint8_t smem_raw[];
@@ -324,8 +325,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // routed block c begin, blocks up to c + 2 are issued.  (ri, rkb) walks
     // the routed blocks in the order the dequant warps consume them.
     if (lane == 0) {  // descriptors into the TMA unit's cache before the first copies
-      const CUtensorMap *maps[5] = {&tm_raw, &tm_b_routed, &tm_b_shared, &tm_a0, &tm_a1};
-      for (int m = 0; m < 5; ++m)
+      const CUtensorMap *maps[8] = {&tm_raw, &tm_b_r32, &tm_b_r64, &tm_b_r96, &tm_b_routed, &tm_b_shared, &tm_a0, &tm_a1};
+      for (int m = 0; m < 8; ++m)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(maps[m])) : "memory");
     }
     int st_it = 0, rawq = 0, rawpos = 0, ri = 0, rkb = 0;
@@ -345,15 +346,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) w = tc_wait(&S.raw_empty[slot], ((rawq / TC_RAW_SLOTS) & 1) ^ 1, S, a.status);
         if (!__shfl_sync(0xffffffffu, w, 0)) return -1;
       }
-      const int rows = GU ? 2 * TC_BM : TC_BM;
+      const int rows = 2 * TC_BM;
       if (lane == 0) {
         // words [x, x + 24) of 128 weight rows: the 96-byte window, 16-byte
         // aligned, that holds block rkb of each row
         mbar_arrive_expect_tx(&S.raw_full[slot], rows * TC_RAW_ROW);
         const int xw = (int)(((uint32_t)(QB * rkb) & ~15u) >> 2);
         uint8_t *dst = raw + (size_t)slot * TC_RAW_BYTES;
-        tma_load_3d(dst, &tm_raw, xw, t.blk * TC_BM, t.e, &S.raw_full[slot]);
-        if (GU) tma_load_3d(dst + TC_BM * TC_RAW_ROW, &tm_raw, xw, a.F + t.blk * TC_BM, t.e, &S.raw_full[slot]);
+        // gate/up: rows blk*128 of gate and of up; down: rows blk*256 and blk*256 + 128
+        const int y0 = GU ? t.blk * TC_BM : 2 * t.blk * TC_BM;
+        tma_load_3d(dst, &tm_raw, xw, y0, t.e, &S.raw_full[slot]);
+        tma_load_3d(dst + TC_BM * TC_RAW_ROW, &tm_raw, xw, GU ? a.F + y0 : y0 + TC_BM, t.e, &S.raw_full[slot]);
       }
       __syncwarp();
       ++rawq;
@@ -382,16 +385,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         uint8_t *stage = stages + (size_t)s * TC_STAGE_BYTES;
         if (lane == 0) {
-          // one box of NMAX token rows (rows past the tile's tokens only feed
-          // accumulator columns that are never read)
-          uint32_t bytes = (uint32_t)C::NMAX * 128;
+          // one box of token rows: the tile's width rounded up to 32 (routed
+          // tiles) or NMAX (shared ones); rows past the tile's tokens only
+          // feed accumulator columns that are never read
+          const int bsel = routed && MODE != MODE_ROUTER ? min((t.n - 1) >> 5, 3) : 3;
+          const CUtensorMap *bm = !routed ? &tm_b_shared
+                                  : bsel == 0 ? &tm_b_r32 : bsel == 1 ? &tm_b_r64 : bsel == 2 ? &tm_b_r96 : &tm_b_routed;
+          uint32_t bytes = routed ? (uint32_t)(bsel + 1) * 32 * 128 : (uint32_t)C::NMAX * 128;
           if (!routed) bytes += C::A_TILES * TC_TILE_BYTES;
           mbar_arrive_expect_tx(&S.full[s], bytes);
           uint8_t *bdst = stage + C::A_TILES * TC_TILE_BYTES;
-          tma_load_2d(bdst, routed ? &tm_b_routed : &tm_b_shared, kc * TC_BK, t.brow, &S.full[s]);
+          tma_load_2d(bdst, bm, kc * TC_BK, t.brow, &S.full[s]);
           if (!routed) {
-            tma_load_2d(stage, &tm_a0, kc * TC_BK, t.blk * TC_BM, &S.full[s]);
-            if (GU) tma_load_2d(stage + TC_TILE_BYTES, &tm_a1, kc * TC_BK, t.blk * TC_BM, &S.full[s]);
+            if (GU) {
+              tma_load_2d(stage, &tm_a0, kc * TC_BK, t.blk * TC_BM, &S.full[s]);
+              tma_load_2d(stage + TC_TILE_BYTES, &tm_a1, kc * TC_BK, t.blk * TC_BM, &S.full[s]);
+            } else if (MODE == MODE_DN) {
+              tma_load_2d(stage, &tm_a0, kc * TC_BK, 2 * t.blk * TC_BM, &S.full[s]);
+              tma_load_2d(stage + TC_TILE_BYTES, &tm_a0, kc * TC_BK, 2 * t.blk * TC_BM + TC_BM, &S.full[s]);
+            } else {
+              tma_load_2d(stage, &tm_a0, kc * TC_BK, t.blk * TC_BM, &S.full[s]);
+            }
           }
         }
         __syncwarp();
@@ -416,10 +430,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // Thread dt owns one weight row of every stage: gate/up: row dt (gate
     // rows, then up rows), all four sub-blocks; down: row dt % 128, sub-blocks
     // 2 (dt / 128) and the next.  Its raw and destination offsets are fixed.
-    constexpr int NSUB = GU ? 4 : 2;
+    constexpr int NSUB = 4;
     const int dt = threadIdx.x - TC_DQ0 * 32;  // 0 .. 255
-    const int r = GU ? dt : dt % TC_BM;
-    const int jb = GU ? 0 : 2 * (dt / TC_BM);
+    const int r = dt;
+    const int jb = 0;
     const uint32_t raw_row = (uint32_t)r * TC_RAW_ROW;
     const uint32_t dst_row = (uint32_t)((r / TC_BM) * TC_TILE_BYTES + (r % TC_BM) * 128);
     const int x7 = r & 7;
@@ -440,7 +454,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           ok = false;
           break;
         }
-        if (routed && dt < (GU ? 2 : 1) * TC_BM * (4 / NSUB)) {
+        if (routed) {
           uint8_t *dst = stages + (size_t)s * TC_STAGE_BYTES + dst_row;
           // the block's bytes start (84 kb) mod 16 into its 96-byte copy
           const uint8_t *blk = raw + (size_t)slot * TC_RAW_BYTES + raw_row + ((uint32_t)(QB * (kc >> 2)) & 15u);
@@ -491,15 +505,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk) {
             const uint64_t bd = sw128_desc(bbase + 32 * kk);
-            if (GU) {  // gate and up: two accumulators, interleaved
+            if (C::A_TILES == 2) {  // gate and up, or two down blocks: two accumulators
               const bool acc = kc > 0 || kk > 0;
               mma_f16(d0, sw128_desc(sbase + 32 * kk), bd, idesc, acc);
               mma_f16(d0 + 128, sw128_desc(sbase + TC_TILE_BYTES + 32 * kk), bd, idesc, acc);
-            } else if (MODE == MODE_DN) {
-              // two partial accumulators (even and odd K steps) so that
-              // consecutive MMAs do not chain on one accumulator; the
-              // epilogue adds them
-              mma_f16(d0 + 128 * (kk & 1), sw128_desc(sbase + 32 * kk), bd, idesc, kc > 0 || kk > 1);
             } else {
               mma_f16(d0, sw128_desc(sbase + 32 * kk), bd, idesc, kc > 0 || kk > 0);
             }
@@ -556,7 +565,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (j0 + j < t.n && e < a.E) orow[(int64_t)(j0 + j) * a.E] = v[j] + b;
         }
       } else {
-        const int d = t.blk * TC_BM + r;
+        const int d = 2 * t.blk * TC_BM + r;  // and d + 128 from the second accumulator
         float *orow = (t.kind == 0 ? a.y : a.ys) + (int64_t)t.brow * a.D + d;
         for (int j0 = 0; j0 < t.n; j0 += 16) {
           float v[16], w[16];
@@ -564,7 +573,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tmem_ld16(tl + 128 + j0, w);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (j0 + j < t.n) orow[(int64_t)(j0 + j) * a.D] = v[j] + w[j];
+            if (j0 + j < t.n) {
+              orow[(int64_t)(j0 + j) * a.D] = v[j];
+              orow[(int64_t)(j0 + j) * a.D + TC_BM] = w[j];
+            }
         }
       }
       tc_fence_before();
@@ -657,7 +669,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict
   const int e = threadIdx.x;
   const int ne = e < E ? counts[e] : 0;
   const int cg = (ne + TC_NGU - 1) / TC_NGU, cd = (ne + TC_NDN - 1) / TC_NDN;
-  const int tg = cg * (F / TC_BM), td = cd * (D / TC_BM);
+  const int tg = cg * (F / TC_BM), td = cd * (D / (2 * TC_BM));
   scan_gu[e] = tg;
   scan_dn[e] = td;
   __syncthreads();
@@ -670,7 +682,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict
   }
   const int sg_chunks = Fs > 0 ? (int)((T + TC_NGU - 1) / TC_NGU) : 0;
   const int sd_chunks = Fs > 0 ? (int)((T + TC_NDN - 1) / TC_NDN) : 0;
-  const int n_sg = sg_chunks * (Fs / TC_BM), n_sd = sd_chunks * (D / TC_BM);
+  const int n_sg = sg_chunks * (Fs / TC_BM), n_sd = sd_chunks * (D / (2 * TC_BM));
   // shared tiles
   for (int i = e; i < n_sg; i += 1024) {
     const int c = i / (Fs / TC_BM), b = i % (Fs / TC_BM);
@@ -678,7 +690,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict
     gu[i] = make_int4(1, 0, t0, n | (b << 16));
   }
   for (int i = e; i < n_sd; i += 1024) {
-    const int c = i / (D / TC_BM), b = i % (D / TC_BM);
+    const int c = i / (D / (2 * TC_BM)), b = i % (D / (2 * TC_BM));
     const int t0 = c * TC_NDN, n = (int)min((int64_t)TC_NDN, T - t0);
     dn[i] = make_int4(1, 0, t0, n | (b << 16));
   }
@@ -692,7 +704,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict
       }
     o = n_sd + scan_dn[e] - td;
     for (int c = 0; c < cd; ++c)
-      for (int b = 0; b < D / TC_BM; ++b) {
+      for (int b = 0; b < D / (2 * TC_BM); ++b) {
         const int n = min(TC_NDN, ne - c * TC_NDN);
         dn[o++] = make_int4(0, e, base + c * TC_NDN, n | (b << 16));
       }
@@ -788,8 +800,8 @@ cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const voi
   CUtensorMap m_wr, m_x;
   if (!make_map(&m_wr, W.router_w, sh.E, sh.D, TC_BM, true) || !make_map(&m_x, x, T, sh.D, TC_NRT, true))
     return cudaErrorInvalidValue;
-  tc_gemm_kernel<MODE_ROUTER><<<std::min<int>(sms, a.router_tiles), TC_THREADS, tc_smem<MODE_ROUTER>(), s>>>(a, m_wr, m_x, m_x,
-                                                                                              m_wr, m_wr);
+  tc_gemm_kernel<MODE_ROUTER><<<std::min<int>(sms, a.router_tiles), TC_THREADS, tc_smem<MODE_ROUTER>(), s>>>(a, m_wr, m_x, m_x, m_x, m_x,
+                                                                                              m_x, m_wr, m_wr);
   return cudaGetLastError();
 }
 
@@ -887,14 +899,25 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
     return cudaErrorInvalidValue;
   a.tiles = tiles_gu;
   a.n_tiles = cnt;
-  tc_gemm_kernel<MODE_GU><<<sms, TC_THREADS, tc_smem<MODE_GU>(), s>>>(a, m_rgu, m_xp, m_x, m_sg, m_su);
+  // routed token rows with boxes of 32, 64, 96 and 128 rows
+  CUtensorMap m_xp32, m_xp64, m_xp96;
+  if (!make_map(&m_xp32, xp, P, sh.D, 32, false) || !make_map(&m_xp64, xp, P, sh.D, 64, false) ||
+      !make_map(&m_xp96, xp, P, sh.D, 96, false))
+    return cudaErrorInvalidValue;
+  tc_gemm_kernel<MODE_GU><<<sms, TC_THREADS, tc_smem<MODE_GU>(), s>>>(a, m_rgu, m_xp32, m_xp64, m_xp96, m_xp, m_x, m_sg,
+                                                                      m_su);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the shared rows of h have n_ff_shared columns: their own map
   CUtensorMap m_hs;
   if (!make_map(&m_hs, h16 + (size_t)P * sh.F, T, std::max(sh.Fs, 64), TC_NDN, false)) return cudaErrorInvalidValue;
   a.tiles = tiles_dn;
   a.n_tiles = cnt + 1;
-  tc_gemm_kernel<MODE_DN><<<sms, TC_THREADS, tc_smem<MODE_DN>(), s>>>(a, m_rdn, m_h, m_hs, m_sd, m_sd);
+  CUtensorMap m_h32, m_h64, m_h96;
+  if (!make_map(&m_h32, h16, P, sh.F, 32, false) || !make_map(&m_h64, h16, P, sh.F, 64, false) ||
+      !make_map(&m_h96, h16, P, sh.F, 96, false))
+    return cudaErrorInvalidValue;
+  tc_gemm_kernel<MODE_DN><<<sms, TC_THREADS, tc_smem<MODE_DN>(), s>>>(a, m_rdn, m_h32, m_h64, m_h96, m_h, m_hs, m_sd,
+                                                                      m_sd);
   return cudaGetLastError();
 }
 
