@@ -8,10 +8,12 @@ than L2: the timed steps rotate over independently generated layers, as a
 decode pass does, so no step finds the previous step's weights in L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--extra] [--layers R]
+                    [--layers R] [--no-extra] [--no-cpu-baseline]
 
-Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
-on a bounded sample of the same workload instead.
+Prints one JSON line (rank 0).  Its "extra" object times the metric's other
+workloads (prefill T=4096 uniform and Zipf against the bf16 tensor roofline,
+decode T=32 Zipf against HBM).  --impl reference times the fp64 CPU oracle on
+a bounded sample of the decode workload instead.
 """
 from __future__ import annotations
 
@@ -190,7 +192,7 @@ def gpu_arm(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2: steps rotate over {R} independently generated "
                          f"layers ({R * (cfg.E * cfg.expert_bytes) / 1e9:.1f} GB of experts)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "decode step: route_kernel -> gateup_kernel -> down_kernel (whole PDL chain timed as one launch)",
+        "roofline": {"bound": "hbm", "kernel": "decode step: route_kernel + stream_kernel (both timed as one launch)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": pk_kind,
                      "traffic": None, "algorithmic_bytes": bytes_per_step},
@@ -202,7 +204,82 @@ def gpu_arm(args, rank, world, local_rank):
     return line
 
 
-LAUNCHES_PER_DECODE_STEP = 3  # router logits; select+route+gate/up; down+combine (PDL chain)
+LAUNCHES_PER_DECODE_STEP = 2  # router logits; the one-token streaming kernel
+
+PREFILL_FLOPS = 1.4517e12  # 4096 x (6*3*2*D*F + 3*2*D*F + 2*D*E) at the Flash shape
+
+
+def time_layer(cfg, iters, dev, warmup=3):
+    """(ms per layer call, used experts, path) for one synthetic layer of cfg
+    with its inputs resident; CUDA events over `iters` calls after warm-up."""
+    import torch
+    import bit_quantized_routed_router_gb300 as ds
+    from bit_quantized_routed_router_gb300 import synthetic
+
+    sh = synthetic.shape_of(cfg)
+    W = synthetic.build_layer(cfg, device=dev)
+    x = synthetic.build_x(cfg, device=dev)
+    out = torch.empty((cfg.T, cfg.D), dtype=torch.float32, device=dev)
+    ws = torch.empty(ds.workspace_bytes(sh, cfg.T), dtype=torch.uint8, device=dev)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    ds.layer(sh, W, x, out, ws, debug={"counts": counts})
+    used = int((counts > 0).sum().item())
+    for _ in range(warmup):
+        ds.layer(sh, W, x, out, ws)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        ds.layer(sh, W, x, out, ws)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ds.sync_status()
+    path = ds.layer_path(sh, cfg.T, x)
+    del W, ws, out
+    torch.cuda.empty_cache()
+    return e0.elapsed_time(e1) / iters, used, path
+
+
+def extra_workloads(args, dev):
+    """The other timed workloads of the metric (not the headline line):
+    prefill T=4096 (uniform and Zipf router) against the bf16 tensor roofline,
+    decode T=32 Zipf against the HBM roofline.  Each on its own layer, inputs
+    resident, CUDA events over `iters` layer calls after warm-up."""
+    import torch
+    import bit_quantized_routed_router_gb300 as ds
+    from bit_quantized_routed_router_gb300 import synthetic
+
+    pk, pk_kind = peaks()
+    res = {}
+    for cfg, iters in ((dsgen.PREFILL, 10), (dsgen.PREFILL_ZIPF, 10), (dsgen.DECODE32_ZIPF, 200)):
+        ms, used, path = time_layer(cfg, iters, dev)
+        entry = {"tokens_per_s": cfg.T / (ms / 1e3), "ms_per_layer": ms, "T": cfg.T,
+                 "used_experts": used, "path": path}
+        if cfg.T >= 64:
+            tfs = PREFILL_FLOPS / (ms / 1e3) / 1e12
+            peak = float(pk.get("bf16_tflops", BF16_FALLBACK_TFS))
+            entry["roofline"] = {"bound": "tensor", "achieved": tfs, "peak": peak, "unit": "TFLOP/s",
+                                 "frac": tfs / peak, "peak_source": pk_kind,
+                                 "algorithmic_flops": PREFILL_FLOPS}
+        else:
+            b = algorithmic_bytes(cfg, used, cfg.T)
+            gbs = b / (ms / 1e3) / 1e9
+            hbm = float(pk.get("hbm_gbs", HBM_FALLBACK_GBS))
+            entry["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                 "frac": gbs / hbm, "peak_source": pk_kind, "algorithmic_bytes": b}
+        res[cfg.name] = entry
+    return res
+
+
+# single workloads for profiling runs (not the benchmark line)
+WORKLOADS = {
+    "prefill": dsgen.PREFILL,
+    "prefill_zipf": dsgen.PREFILL_ZIPF,
+    "decode32": dsgen.DECODE32_ZIPF,
+    # same shapes at 1/4 of the experts and tokens (about 96 tokens per
+    # expert as at full size): a case small enough for full profiler captures
+    "prefill_small": None,
+}
 
 
 # ------------------------------------------------------------ oracle (CPU) --
@@ -264,11 +341,26 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=4, help="rotating layers (L2 defeat)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the prefill / decode-32 extras")
+    ap.add_argument("--workload", default="decode", choices=["decode"] + list(WORKLOADS),
+                    help="time one other workload only (profiling runs); prints its own JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.workload != "decode":
+        import torch
+        from dataclasses import replace
+        from bit_quantized_routed_router_gb300 import build as libbuild
+        libbuild.build()
+        cfg = WORKLOADS[args.workload] or replace(dsgen.PREFILL, name="prefill T=1024 E=64 (profiling case)",
+                                                   T=1024, E=64)
+        ms, used, path = time_layer(cfg, args.steps, torch.device("cuda", 0), warmup=args.warmup)
+        print(json.dumps({"workload": cfg.name, "ms_per_layer": ms, "tokens_per_s": cfg.T / (ms / 1e3),
+                          "used_experts": used, "path": path, "steps": args.steps}), flush=True)
+        return
 
     if args.impl == "reference":
         line = reference_arm(args, rank)
@@ -280,6 +372,9 @@ def main():
         import torch
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line = gpu_arm(args, rank, world, local_rank)
+    if rank == 0 and not args.no_extra and world == 1:
+        import torch
+        line["extra"] = extra_workloads(args, torch.device("cuda", local_rank))
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = oracle_sample()

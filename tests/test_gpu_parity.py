@@ -248,7 +248,8 @@ def test_layer_path_selection():
     assert ds.layer_path(sh, 0) == ds.PATH_NONE
     assert ds.layer_path(sh, 1) == ds.PATH_STREAM
     assert ds.layer_path(sh, 4) == ds.PATH_DECODE3
-    assert ds.layer_path(sh, 32) == ds.PATH_GROUPED_GEMV
+    assert ds.layer_path(sh, 8) == ds.PATH_GROUPED_GEMV
+    assert ds.layer_path(sh, 32) == ds.PATH_TENSOR_CORE
     assert ds.layer_path(synthetic.shape_of(dsgen.PREFILL), 4096) == ds.PATH_TENSOR_CORE
     assert ds.layer_path(synthetic.shape_of(dsgen.TINY), 700) == ds.PATH_GROUPED_GEMV  # fp32 x
     assert ds.layer_path(synthetic.shape_of(replace(dsgen.DECODE1, T=1)), 64) == ds.PATH_TENSOR_CORE
