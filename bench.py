@@ -240,10 +240,57 @@ def time_layer(cfg, iters, dev, warmup=3):
     return e0.elapsed_time(e1) / iters, used, path
 
 
+def time_stack(cfg, iters, dev, warmup=3):
+    """The 43-layer stack (x += layer(bf16(RMSNorm(x))) per layer, T tokens):
+    (ms per step, bytes read per step, distinct experts per layer, path).  One
+    step = the residual reset to the same input (a 128 KB device copy) + one
+    ds_moe_stack call over every layer, all experts resident.  The experts a
+    step reads are counted on an untimed pass that advances the same residual
+    one layer at a time (bit-identical to the multi-layer call) and reads each
+    layer's expert counts from a ds_moe_layer call on the normalised input."""
+    import torch
+    import bit_quantized_routed_router_gb300 as ds
+    from bit_quantized_routed_router_gb300 import synthetic
+    from dataclasses import replace
+
+    sh = synthetic.shape_of(cfg)
+    Ws = [synthetic.build_layer(cfg, l, device=dev) for l in range(cfg.layers)]
+    x0 = torch.from_numpy(dsgen.host_x(replace(cfg, x_dtype="f32"))).to(dev)
+    x = x0.clone()
+    ws = torch.empty(ds.workspace_bytes(sh, cfg.T), dtype=torch.uint8, device=dev)
+    out = torch.empty((cfg.T, cfg.D), dtype=torch.float32, device=dev)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    used = []
+    for W in Ws:
+        xn = (x * torch.rsqrt(x.square().mean(dim=1, keepdim=True) + 1e-6)).to(torch.bfloat16)
+        ds.layer(sh, W, xn, out, ws, debug={"counts": counts})
+        used.append(int((counts > 0).sum().item()))
+        ds.stack(sh, [W], x, ws)
+    ds.sync_status()
+    for _ in range(warmup):
+        x.copy_(x0)
+        ds.stack(sh, Ws, x, ws)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        x.copy_(x0)
+        ds.stack(sh, Ws, x, ws)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ds.sync_status()
+    path = ds.layer_path(sh, cfg.T, xn)
+    per_layer_fixed = cfg.Fs * cfg.D * 2 * 3 + cfg.E * cfg.D * 2
+    b = sum(u * cfg.expert_bytes + per_layer_fixed for u in used)
+    del Ws, ws, out, x, x0
+    torch.cuda.empty_cache()
+    return e0.elapsed_time(e1) / iters, b, used, path
+
+
 def extra_workloads(args, dev):
     """The other timed workloads of the metric (not the headline line):
     prefill T=4096 (uniform and Zipf router) against the bf16 tensor roofline,
-    decode T=32 Zipf against the HBM roofline.  Each on its own layer, inputs
+    decode T=32 Zipf and the 43-layer stack at T=8 against the HBM roofline.  Each on its own layer, inputs
     resident, CUDA events over `iters` layer calls after warm-up."""
     import torch
     import bit_quantized_routed_router_gb300 as ds
@@ -268,6 +315,17 @@ def extra_workloads(args, dev):
             entry["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                                  "frac": gbs / hbm, "peak_source": pk_kind, "algorithmic_bytes": b}
         res[cfg.name] = entry
+    cfg = dsgen.STACK
+    ms, b, used, path = time_stack(cfg, 20, dev)
+    gbs = b / (ms / 1e3) / 1e9
+    hbm = float(pk.get("hbm_gbs", HBM_FALLBACK_GBS))
+    res[cfg.name] = {"tokens_per_s": cfg.T / (ms / 1e3), "ms_per_step": ms, "T": cfg.T,
+                     "layers": cfg.layers, "bytes_read_per_s": b / (ms / 1e3),
+                     "used_experts_per_layer": {"min": min(used), "max": max(used),
+                                                "mean": sum(used) / len(used)},
+                     "path": path,
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                  "frac": gbs / hbm, "peak_source": pk_kind, "algorithmic_bytes": b}}
     return res
 
 
@@ -276,6 +334,7 @@ WORKLOADS = {
     "prefill": dsgen.PREFILL,
     "prefill_zipf": dsgen.PREFILL_ZIPF,
     "decode32": dsgen.DECODE32_ZIPF,
+    "stack": dsgen.STACK,
     # same shapes at 1/4 of the experts and tokens (about 96 tokens per
     # expert as at full size): a case small enough for full profiler captures
     "prefill_small": None,
@@ -357,6 +416,12 @@ def main():
         libbuild.build()
         cfg = WORKLOADS[args.workload] or replace(dsgen.PREFILL, name="prefill T=1024 E=64 (profiling case)",
                                                    T=1024, E=64)
+        if args.workload == "stack":
+            ms, b, used, path = time_stack(cfg, args.steps, torch.device("cuda", 0), warmup=args.warmup)
+            print(json.dumps({"workload": cfg.name, "ms_per_step": ms, "tokens_per_s": cfg.T / (ms / 1e3),
+                              "bytes_read_per_s": b / (ms / 1e3), "used_experts": used, "path": path,
+                              "steps": args.steps}), flush=True)
+            return
         ms, used, path = time_layer(cfg, args.steps, torch.device("cuda", 0), warmup=args.warmup)
         print(json.dumps({"workload": cfg.name, "ms_per_layer": ms, "tokens_per_s": cfg.T / (ms / 1e3),
                           "used_experts": used, "path": path, "steps": args.steps}), flush=True)

@@ -208,7 +208,7 @@ def layer_hostio(shape: MoEShape, weights: MoEWeights, x_host, out_host, workspa
 
 def layer_noalloc(shape: MoEShape, weights: MoEWeights, x, out, stream=None, T: int | None = None):
     """layer() without a workspace: the library's static device scratch is used
-    (for callers that cannot allocate; at most 8 MiB of scratch, serialise calls)."""
+    (for callers that cannot allocate; at most 64 MiB of scratch, serialise calls)."""
     T = x.shape[0] if T is None else T
     _call(lib().ds_moe_layer_noalloc, ctypes.byref(shape.c()), ctypes.byref(weights.c()),
           x.data_ptr(), T, out.data_ptr(), _stream(stream))

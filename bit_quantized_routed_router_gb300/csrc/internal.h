@@ -55,7 +55,7 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
                                 const Work &wk, float *out, bool accumulate, cudaStream_t s);
 // Large batches: the expert FFNs as grouped tcgen05 GEMMs (after
 // launch_route; the combine follows).  tc_ws holds prefill_tc_workspace bytes.
-constexpr int64_t TC_MIN_T = 16;
+constexpr int64_t TC_MIN_T = 5;
 bool prefill_tc_supported(const Shape &sh, int64_t T);
 size_t prefill_tc_workspace(const Shape &sh, int64_t T);
 cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,

@@ -23,7 +23,7 @@
 
 namespace {
 
-constexpr size_t NOALLOC_SCRATCH_BYTES = 8u << 20;  // 8 MiB per GPU
+constexpr size_t NOALLOC_SCRATCH_BYTES = 64u << 20;  // 64 MiB per GPU
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 

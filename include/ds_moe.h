@@ -138,7 +138,7 @@ int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, 
  * T == 0 is a no-op.  The kernels that run depend on T and the shape (see
  * ds_moe_layer_path): one token at the instantiated widths streams the whole
  * layer through one cooperative kernel; up to four tokens use a three-kernel
- * decode chain; T >= 16 with bf16 x and router and n_embd, n_ff multiples of
+ * decode chain; T >= 5 with bf16 x and router and n_embd, n_ff multiples of
  * 1024 runs the expert FFNs as grouped tcgen05 GEMMs with fp16 operands
  * (dequantised weights and activations rounded once to fp16; an |x| or
  * intermediate above 65504 is saturated and reported by ds_moe_sync_status
@@ -170,13 +170,16 @@ int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_
  * call the layer -- for example code being captured into a CUDA graph, where
  * allocation calls are not allowed, or a plugin whose host program owns all
  * device memory through its own allocator.  It takes no workspace: its
- * scratch is a static 8 MiB device array inside this library, allocated on
+ * scratch is a static 64 MiB device array inside this library, allocated on
  * each GPU when the library is loaded there and held until the process
  * exits.  The pages have no counterpart to this entry point.
  *   x, T, out, stream, err: as for ds_moe_layer (no debug outputs).
  *   Rejects, with DS_ERR_INVALID_ARG and a message, any T whose
- *   ds_moe_workspace_bytes exceeds 8 MiB (about 40 tokens at the 4096/256/6/
- *   2048 shape).  Allocates nothing: no cudaMalloc, no cudaFree.
+ *   ds_moe_workspace_bytes exceeds 64 MiB (at the 4096/256/6/2048 shape a
+ *   batch of about 5 or more tokens takes the tensor-core path, whose scratch
+ *   includes a 16.8 MB fp16 copy of the shared down matrix; the limit is then
+ *   reached at about 200 tokens).  Allocates nothing: no cudaMalloc, no
+ *   cudaFree.
  *   The first call on a device looks up the array's device address with
  *   that device current; make that first call before any stream capture.
  *   Every call reuses the same array and leaves its contents behind; the

@@ -248,7 +248,7 @@ def test_layer_path_selection():
     assert ds.layer_path(sh, 0) == ds.PATH_NONE
     assert ds.layer_path(sh, 1) == ds.PATH_STREAM
     assert ds.layer_path(sh, 4) == ds.PATH_DECODE3
-    assert ds.layer_path(sh, 8) == ds.PATH_GROUPED_GEMV
+    assert ds.layer_path(sh, 8) == ds.PATH_TENSOR_CORE
     assert ds.layer_path(sh, 32) == ds.PATH_TENSOR_CORE
     assert ds.layer_path(synthetic.shape_of(dsgen.PREFILL), 4096) == ds.PATH_TENSOR_CORE
     assert ds.layer_path(synthetic.shape_of(dsgen.TINY), 700) == ds.PATH_GROUPED_GEMV  # fp32 x
@@ -292,7 +292,7 @@ def test_decode32_zipf_parity():
 def test_batch_invariance_decode(decode1):
     """Within one path a token's result does not depend on its batch: tokens of
     an 8-token batch equal the same tokens in a 5-token batch bit for bit
-    (grouped path, T > 4), and tokens of a 2-token batch equal the same tokens
+    (tensor-core path, T > 4), and tokens of a 2-token batch equal the same tokens
     in a 4-token batch (three-kernel path, 2 <= T <= 4).  A token alone takes
     the one-token streaming kernel; every path agrees with the others at
     tolerance."""
@@ -311,7 +311,7 @@ def test_batch_invariance_decode(decode1):
         check_close(out_1[0].astype(np.float64), out_4[t].astype(np.float64), DECODE_TOL,
                     "one-token kernel vs three-kernel path")
         check_close(out_1[0].astype(np.float64), out_b[t].astype(np.float64), DECODE_TOL,
-                    "one-token kernel vs grouped path")
+                    "one-token kernel vs tensor-core path")
 
 
 def test_batch_invariance_small_width():
@@ -361,43 +361,43 @@ def test_zero_tokens_is_noop(decode1):
     assert torch.all(out == 3.0)
 
 
-def _stack_oracle(cfg, n_layers):
-    """Oracle residual after each of n_layers stack steps (own residual; fp32
-    between layers).  Returns the input and the residual after each layer."""
+def test_stack_parity_by_layer():
+    """The stack  x <- x + layer(bf16(RMSNorm(x)))  at full width, T=8, four
+    layers.  Every layer is checked on the residual the GPU itself produced
+    before it: the oracle normalises that residual, runs the layer in fp64 and
+    adds it, and the GPU's next residual must match within the tolerance of
+    the path the layer takes (a batch of 8 runs on the tensor cores: 5e-3 *
+    rms of the update).  Comparing whole trajectories instead would not test
+    the kernels: routing is discontinuous, and residual differences at the
+    level of the float tolerance move logits by far more than the 1e-4 gap the
+    generator guarantees, so after a few layers a token may rightly take
+    another expert on one side.  A token whose logits on the GPU's residual
+    have a near-tie (gap < 1e-4) is left out of that layer's comparison.
+    ds_moe_stack over several layers is bit-identical to these one-layer calls
+    (next test)."""
     from dataclasses import replace
-    x0 = dsgen.host_x(replace(cfg, x_dtype="f32"))
-    xr, outs = x0.copy(), []
-    for l in range(n_layers):
-        lo = oracle.LayerOracle(cfg, l)
-        r64 = oracle.as_f64(oracle.rmsnorm_bf16(xr), "bf16")
-        if np.any(oracle.min_top_gap(lo.logits(r64), cfg.k) < oracle.GAP):
-            pytest.skip("near-tie in a stack layer's input for this seed")
-        (res, _, _, _) = lo.forward(r64)
-        xr = (xr.astype(np.float64) + res).astype(np.float32)
-        outs.append(xr.copy())
-    return x0, outs
-
-
-def test_stack_parity_by_depth():
-    """The stack  x <- x + layer(bf16(RMSNorm(x)))  at full width, T=8.
-    Depth 1 must meet the decode tolerance on the update.  Each later layer
-    re-rounds its normalised input to bf16, so residual differences at the
-    1e-5 level flip a few bf16 roundings and the difference grows with depth;
-    the bound used is 2e-3 * depth * rms(update)."""
     cfg = dsgen.STACK
-    n_layers = 3
-    x0, outs = _stack_oracle(cfg, n_layers)
+    n_layers = 4
     Ws = [synthetic.build_layer(cfg, l) for l in range(n_layers)]
     sh = synthetic.shape_of(cfg)
+    tol = PREFILL_TOL if ds.layer_path(sh, cfg.T) == ds.PATH_TENSOR_CORE else DECODE_TOL
     ws = torch.empty(ds.workspace_bytes(sh, cfg.T), dtype=torch.uint8, device="cuda")
-    for depth in range(1, n_layers + 1):
-        x = torch.from_numpy(x0).cuda()
-        ds.stack(sh, Ws[:depth], x, ws)
+    x = torch.from_numpy(dsgen.host_x(replace(cfg, x_dtype="f32"))).cuda()
+    checked = 0
+    for l in range(n_layers):
+        x_in = x.cpu().numpy()
+        ds.stack(sh, [Ws[l]], x, ws)
         ds.sync_status()
-        upd = x.cpu().numpy().astype(np.float64) - x0
-        r = check_close(upd, outs[depth - 1].astype(np.float64) - x0, DECODE_TOL * depth,
-                        f"stack update at depth {depth}")
-        print(f"stack depth {depth}: max|err|/rms = {r:.2e}")
+        got = x.cpu().numpy().astype(np.float64) - x_in
+        lo = oracle.LayerOracle(cfg, l)
+        r64 = oracle.as_f64(oracle.rmsnorm_bf16(x_in), "bf16")
+        res, _, _, L = lo.forward(r64)
+        keep = oracle.min_top_gap(L, cfg.k) >= oracle.GAP
+        ref = (x_in.astype(np.float64) + res).astype(np.float32).astype(np.float64) - x_in
+        r = check_close(got[keep], ref[keep], tol, f"stack layer {l} ({keep.sum()} tokens)")
+        print(f"stack layer {l}: max|err|/rms = {r:.2e}")
+        checked += int(keep.sum())
+    assert checked >= n_layers * cfg.T - 2
 
 
 def test_stack_equals_layer_by_layer():
