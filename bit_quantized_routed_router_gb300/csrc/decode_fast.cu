@@ -326,33 +326,58 @@ struct RouteCache {
 // stable route puts pair p at #(pairs with a smaller expert, or the same
 // expert and a smaller p).  Returns the calling lane's RouteCache entries; with
 // publish, also writes ids, w, counts, offsets, perm, pos and used.
-__device__ RouteCache select_route_warp(const Args &a, bool publish) {
+__device__ RouteCache select_route_warp(const Args &a, bool publish, volatile int *loaded = nullptr) {
   const int lane = threadIdx.x & 31, P = a.T * a.k;
   int my_id = 0;     // lane p: expert of pair p
   float my_lg = 0.f; // lane p: its logit
+  const int nv = (a.E + 31) / 32;  // logits per lane (E <= 1024)
   for (int t = 0; t < a.T; ++t) {
     const float *L = a.logits + (int64_t)t * a.E;
     float lv[32];
 #pragma unroll
-    for (int ii = 0; ii < 32; ++ii) lv[ii] = lane + 32 * ii < a.E ? __ldcg(L + lane + 32 * ii) : -INFINITY;
+    for (int ii = 0; ii < 32; ++ii) lv[ii] = ii < nv && lane + 32 * ii < a.E ? __ldcg(L + lane + 32 * ii) : -INFINITY;
+    if (loaded && t == a.T - 1) {
+      // every lane's logits have arrived (the flag's value depends on them)
+      float mx = lv[0];
+#pragma unroll
+      for (int ii = 1; ii < 32; ++ii) mx = fmaxf(mx, lv[ii]);
+      int one;  // 1, computed from mx so that it waits for the loads
+      asm volatile("{\n\t.reg .pred p;\n\tsetp.num.f32 p, %1, %1;\n\tselp.s32 %0, 1, 1, p;\n\t}" : "=r"(one) : "f"(mx));
+      const int got = __all_sync(0xffffffffu, one);
+      if (lane == 0) *loaded = got;
+    }
+    // each lane's best remaining candidate (largest logit, then lowest
+    // index); per pick the warp takes the best of those, and only the lane
+    // that supplied it looks for its next one
     uint32_t taken = 0;
-    for (int j = 0; j < a.k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    auto rescan = [&]() {
+      bv = -INFINITY;
+      bi = 0x7fffffff;
 #pragma unroll
       for (int ii = 0; ii < 32; ++ii) {
+        if (ii >= nv) break;
         const int ee = lane + 32 * ii;
         if (ee < a.E && !(taken & (1u << ii)) && (lv[ii] > bv || (lv[ii] == bv && ee < bi))) { bv = lv[ii]; bi = ee; }
       }
+    };
+    rescan();
+    for (int j = 0; j < a.k; ++j) {
+      float wv = bv;
+      int wi = bi;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+        if (ov > wv || (ov == wv && oi < wi)) { wv = ov; wi = oi; }
       }
-      if (bi < 0 || bi >= a.E) { if (lane == 0 && publish) flag(a.status, ST_BAD_ID); bi = 0; }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == t * a.k + j) { my_id = bi; my_lg = bv; }
+      if (wi < 0 || wi >= a.E) { if (lane == 0 && publish) flag(a.status, ST_BAD_ID); wi = 0; }
+      if ((wi & 31) == lane && wi == bi) {
+        taken |= 1u << (wi >> 5);
+        rescan();
+      }
+      if (lane == t * a.k + j) { my_id = wi; my_lg = wv; }
     }
   }
   // weights: softmax over each token's selected logits
@@ -748,6 +773,7 @@ struct StreamShared {
   float rt_w[32];      // pair j -> routing weight
   int rt_nu;           // slots in use
   int ready;           // the route above is published
+  int lg_loaded;       // the router warp holds the logits
   int abort_;          // a wait expired
   int go;              // consumers continue past the grid barrier
   int tile[S_NS];                  // phase-A tile in each stage: shared i >= 0, routed -1 - r
@@ -926,6 +952,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       mbar_init(&S.empty[i], S_CONS);
     }
     S.ready = 0;
+    S.lg_loaded = 0;
     S.abort_ = 0;
     S.go = 0;
     S.rt_nu = 0;
@@ -936,7 +963,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
   // ---------------------------------------------------------------- router --
   if (warp == S_CONS + 1) {
     pdl_wait();  // router logits complete and visible
-    const RouteCache r = select_route_warp(a, bid == 0);
+    const RouteCache r = select_route_warp(a, bid == 0, &S.lg_loaded);
     S.rt_used[lane] = r.used;
     S.rt_pos[lane] = r.pos;
     S.rt_w[lane] = r.w;
@@ -952,6 +979,20 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
     if (lane != 0) return;
     int kq = 0;
     bool ok = true;
+    // the router warp's logit loads go first: behind a full copy ring they
+    // would wait several microseconds, and the routed tiles with them
+    {
+      const uint64_t t0 = globaltimer_ns();
+      while (!vload(&S.lg_loaded) && !vload(&S.abort_)) {
+        if (globaltimer_ns() - t0 > S_LIMIT_NS) {
+          flag(a.status, ST_TIMEOUT);
+          *(volatile int *)&S.abort_ = 1;
+          ok = false;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
     // a free stage for the next tile (its previous tile consumed)
     auto acquire = [&]() -> uint8_t * {
       const int st = kq % S_NS;
@@ -1316,6 +1357,13 @@ cudaError_t launch_stream(const Args &a, const Shape &sh, int rb, cudaStream_t s
     cudaError_t e = cudaFuncSetAttribute(stream_kernel<SPL_D, SPL_F>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
     if (e != cudaSuccess) return e;
+    // the router grid runs with the streaming kernel's shared-memory split,
+    // so that the SMs need no reconfiguration between the two
+    for (const void *f : {(const void *)route_kernel<uint16_t, uint16_t>, (const void *)route_kernel<float, float>,
+                          (const void *)stream_kernel<SPL_D, SPL_F>})
+      if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+        return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<SPL_D, SPL_F>, S_THREADS, smem);
     if (e != cudaSuccess) return e;
