@@ -321,6 +321,15 @@ struct RouteCache {
   int pos;  // lane p: position of pair p in the route (select_route_warp only)
 };
 
+// fp32 -> unsigned key with the same order (for non-NaN values), and back.
+__device__ __forceinline__ uint32_t ord_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord_val(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // Selection and route by one warp (T * k <= 32): top-k by logit, ties to the
 // lower index, weights = routed_scale * softmax over the selected logits; the
 // stable route puts pair p at #(pairs with a smaller expert, or the same
@@ -364,14 +373,12 @@ __device__ RouteCache select_route_warp(const Args &a, bool publish, volatile in
     };
     rescan();
     for (int j = 0; j < a.k; ++j) {
-      float wv = bv;
-      int wi = bi;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
-        if (ov > wv || (ov == wv && oi < wi)) { wv = ov; wi = oi; }
-      }
+      // the warp's largest logit (as an order-preserving unsigned key, two
+      // hardware reductions), then the lowest index holding it
+      const uint32_t key = ord_key(bv + 0.f);  // -0 as +0: equal logits tie
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+      int wi = (int)__reduce_min_sync(0xffffffffu, key == mk ? (uint32_t)bi : 0x7fffffffu);
+      const float wv = ord_val(mk);
       if (wi < 0 || wi >= a.E) { if (lane == 0 && publish) flag(a.status, ST_BAD_ID); wi = 0; }
       if ((wi & 31) == lane && wi == bi) {
         taken |= 1u << (wi >> 5);
@@ -384,43 +391,55 @@ __device__ RouteCache select_route_warp(const Args &a, bool publish, volatile in
   const int tok = lane / max(a.k, 1), j0 = tok * a.k;
   const float m0 = __shfl_sync(0xffffffffu, my_lg, min(j0, 31));
   float ex = lane < P ? __expf(my_lg - m0) : 0.f;
+  // every pair's expert, exponential and (below) rank in registers: the
+  // shuffles are independent and issue back to back
+  int idq[32];
+#pragma unroll
+  for (int q = 0; q < 32; ++q) idq[q] = __shfl_sync(0xffffffffu, my_id, q);
+  float exj[32];  // the exponentials of this lane's token, pick order
+#pragma unroll
+  for (int j = 0; j < 32; ++j) exj[j] = __shfl_sync(0xffffffffu, ex, min(j0 + j, 31));
   float den = 0.f;
-  for (int j = 0; j < a.k; ++j) den += __shfl_sync(0xffffffffu, ex, min(j0 + j, 31));
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < a.k) den += exj[j];
   const float my_w = lane < P ? a.routed_scale * (ex / den) : 0.f;
   // ranks
   int rank = 0, first = 1, ui = 0;
-  for (int q = 0; q < P; ++q) {
-    const int eq = __shfl_sync(0xffffffffu, my_id, q);
-    rank += (eq < my_id) || (eq == my_id && q < lane);
-    if (eq == my_id && q < lane) first = 0;
-  }
+#pragma unroll
+  for (int q = 0; q < 32; ++q)
+    if (q < P) {
+      rank += (idq[q] < my_id) || (idq[q] == my_id && q < lane);
+      if (idq[q] == my_id && q < lane) first = 0;
+    }
   const unsigned firsts = __ballot_sync(0xffffffffu, lane < P && first);
-  for (int q = 0; q < P; ++q) {  // distinct experts below mine
-    const int eq = __shfl_sync(0xffffffffu, my_id, q);
-    ui += ((firsts >> q) & 1u) && eq < my_id;
-  }
+#pragma unroll
+  for (int q = 0; q < 32; ++q)  // distinct experts below mine
+    if (q < P) ui += ((firsts >> q) & 1u) && idq[q] < my_id;
   RouteCache r;
   r.nu = __popc(firsts);
+  int rkq[32], uiq[32];
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    rkq[q] = __shfl_sync(0xffffffffu, rank, q);
+    uiq[q] = __shfl_sync(0xffffffffu, ui, q);
+  }
   // lane p learns perm[p]: the pair whose rank is p
   int perm_p = 0;
-  for (int q = 0; q < P; ++q) {
-    const int rq = __shfl_sync(0xffffffffu, rank, q);
-    if (rq == lane) perm_p = q;
-  }
+#pragma unroll
+  for (int q = 0; q < 32; ++q)
+    if (q < P && rkq[q] == lane) perm_p = q;
   r.perm = perm_p;
   r.w = my_w;
   r.pos = rank;
   // lane u learns used[u], its first position and its pair count
   int used_u = 0, base_u = 0, cnt_u = 0;
-  for (int q = 0; q < P; ++q) {
-    const int uq = __shfl_sync(0xffffffffu, ui, q), eq = __shfl_sync(0xffffffffu, my_id, q);
-    const int rq = __shfl_sync(0xffffffffu, rank, q);
-    if (((firsts >> q) & 1u) && uq == lane) { used_u = eq; base_u = rq; }
-  }
-  for (int q = 0; q < P; ++q) {
-    const int eq = __shfl_sync(0xffffffffu, my_id, q);  // every lane shuffles
-    cnt_u += (lane < r.nu && eq == used_u) ? 1 : 0;
-  }
+#pragma unroll
+  for (int q = 0; q < 32; ++q)
+    if (q < P && ((firsts >> q) & 1u) && uiq[q] == lane) { used_u = idq[q]; base_u = rkq[q]; }
+#pragma unroll
+  for (int q = 0; q < 32; ++q)
+    if (q < P) cnt_u += (lane < r.nu && idq[q] == used_u) ? 1 : 0;
   r.used = used_u;
   r.base = base_u;
   r.cnt = cnt_u;
