@@ -246,6 +246,17 @@ int ds_moe_layer(const ds_moe_shape *shape, const ds_moe_weights *weights, const
   return run_layer(sh, *weights, x, out, false, wk, dbg, (cudaStream_t)stream, err, errlen);
 }
 
+// The device address of host memory, or null if the device cannot address it.
+static void *device_view(const void *host) {
+  cudaPointerAttributes pa{};
+  if (cudaPointerGetAttributes(&pa, host) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if ((pa.type == cudaMemoryTypeHost || pa.type == cudaMemoryTypeManaged) && pa.devicePointer) return pa.devicePointer;
+  return nullptr;
+}
+
 int ds_moe_layer_hostio(const ds_moe_shape *shape, const ds_moe_weights *weights,
                         const void *x_host, int64_t T, float *out_host, void *workspace,
                         size_t workspace_bytes, void *stream, char *err, size_t errlen) {
@@ -268,6 +279,17 @@ int ds_moe_layer_hostio(const ds_moe_shape *shape, const ds_moe_weights *weights
   layout(sh, T, (char *)workspace, &wk);
   cudaStream_t s = (cudaStream_t)stream;
   const size_t xbytes = (size_t)T * sh.D * (sh.x_dtype == DS_BF16 ? 2 : 4);
+  // one token in host memory the device can address (pinned, or any memory
+  // on a coherent host): the kernels read x and write out there directly,
+  // with one device copy of x made by the router grid; no copy operations
+  if (fused_decode_supported(sh, T) && stream_decode_supported(sh, T)) {
+    const void *xd = device_view(x_host);
+    void *od = device_view(out_host);
+    if (xd && od && aligned(xd, 16)) {
+      cudaError_t ed = launch_decode_fused(sh, *weights, xd, wk, (float *)od, false, s, wk.x_dev);
+      return ed == cudaSuccess ? DS_OK : cuda_fail(err, errlen, ed, "fused decode layer (host buffers)");
+    }
+  }
   cudaError_t e = cudaMemcpyAsync(wk.x_dev, x_host, xbytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(err, errlen, e, "copy x to device");
   rc = run_layer(sh, *weights, wk.x_dev, wk.out_dev, false, wk, nullptr, s, err, errlen);

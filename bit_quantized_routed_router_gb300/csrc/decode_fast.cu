@@ -247,6 +247,7 @@ struct Args {
   int64_t expert_bytes, gate_bytes;
   const void *x;
   int x_f32;
+  void *x_stage;  // non-null: x is host memory; the router grid copies it here for the streaming kernel
   float *logits;
   int32_t *ids;
   float *w;
@@ -282,6 +283,11 @@ __global__ void __launch_bounds__(256) route_kernel(const Args a) {
   // The dependent kernel touches this word only after its griddepcontrol.wait,
   // i.e. after this grid has completed.
   if (blockIdx.x == 0 && threadIdx.x == 0) a.ctrl[C_BAR] = 0u;
+  if (a.x_stage && blockIdx.x == 0) {  // one device copy of x for the next kernel
+    const size_t n16 = (size_t)a.T * a.D * (a.x_f32 ? 4 : 2) / 16;
+    for (size_t i = threadIdx.x; i < n16; i += blockDim.x)
+      reinterpret_cast<uint4 *>(a.x_stage)[i] = __ldg(reinterpret_cast<const uint4 *>(a.x) + i);
+  }
   __shared__ float part[8][4];  // [warp][token] partial logits
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // two expert rows per CTA, a quarter of n_embd per warp, loads issued up front
@@ -1080,14 +1086,20 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
 
   // ------------------------------------------------------------- consumers --
   // x as fp32 (shared-expert rows) and as fixed-point planes (Q2_K rows),
-  // one half-warp per 256-element block, all loads in one round
+  // one half-warp per 256-element block, all loads in one round (from the
+  // router grid's device copy when x is in host memory)
+  const void *xin = a.x;
+  if (a.x_stage) {
+    pdl_wait();
+    xin = a.x_stage;
+  }
   for (int u = warp; u < (nb_d + 1) / 2; u += S_CONS) {
     const int blk = min(2 * u + (lane >> 4), nb_d - 1);
     const int64_t e0 = (int64_t)QK * blk + 16 * (lane & 15);
     float v[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      v[j] = a.x_f32 ? __ldg((const float *)a.x + e0 + j) : bf16_to_f32(__ldg((const uint16_t *)a.x + e0 + j));
+      v[j] = a.x_f32 ? __ldg((const float *)xin + e0 + j) : bf16_to_f32(__ldg((const uint16_t *)xin + e0 + j));
 #pragma unroll
     for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4 *>(xraw + e0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
     digitize_block<SPL_D>(v, blk, xpl, reinterpret_cast<float *>(xpl + 9 * nsb_d), nsb_d);
@@ -1448,7 +1460,7 @@ bool stream_decode_supported(const Shape &sh, int64_t T) {
 }
 
 cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const void *x,
-                                const Work &wk, float *out, bool accumulate, cudaStream_t s) {
+                                const Work &wk, float *out, bool accumulate, cudaStream_t s, void *x_stage) {
   Args a{};
   a.D = sh.D; a.E = sh.E; a.F = sh.F; a.Fs = sh.Fs; a.k = sh.k; a.T = (int)wk.T;
   a.routed_scale = sh.routed_scale;
@@ -1461,6 +1473,11 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
   a.gate_bytes = sh.gate_bytes();
   a.x = x;
   a.x_f32 = sh.x_dtype == DS_F32;
+  a.x_stage = nullptr;
+  if (x_stage) {  // only the one-token kernel reads the staged copy
+    if (!stream_decode_supported(sh, wk.T)) return cudaErrorInvalidValue;
+    a.x_stage = x_stage;
+  }
   a.logits = wk.logits; a.ids = wk.ids; a.w = wk.w;
   a.counts = wk.counts; a.offsets = wk.offsets; a.perm = wk.perm; a.pos = wk.pos; a.used = wk.used;
   a.h = wk.h;

@@ -51,8 +51,12 @@ cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const vo
 bool fused_decode_supported(const Shape &sh, int64_t T);
 // ... and within it, the one-token streaming kernel.
 bool stream_decode_supported(const Shape &sh, int64_t T);
+// x_stage (one token, streaming kernel only): x is host memory the device can
+// read; the router grid copies it there once and the streaming kernel reads
+// the copy.
 cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const void *x,
-                                const Work &wk, float *out, bool accumulate, cudaStream_t s);
+                                const Work &wk, float *out, bool accumulate, cudaStream_t s,
+                                void *x_stage = nullptr);
 // Large batches: the expert FFNs as grouped tcgen05 GEMMs (after
 // launch_route; the combine follows).  tc_ws holds prefill_tc_workspace bytes.
 constexpr int64_t TC_MIN_T = 5;

@@ -151,8 +151,12 @@ int ds_moe_layer(const ds_moe_shape *shape, const ds_moe_weights *weights, const
 /* ds_moe_layer with x and out in HOST memory (pinned for best speed): the
  * host-to-device copy of x and the device-to-host copy of out are issued on
  * `stream` around the layer, using the workspace for the device copies
- * (ds_moe_workspace_bytes covers them).  Returns after enqueueing; the caller
- * synchronises the stream before reading out. */
+ * (ds_moe_workspace_bytes covers them).  When the one-token kernel serves
+ * the call (T == 1 at its widths) and the device can address both buffers
+ * (pinned memory), no copy operation is issued: the router grid reads x in
+ * host memory and keeps a device copy in the workspace for the streaming
+ * kernel, which writes out straight into host memory.  Returns after
+ * enqueueing; the caller synchronises the stream before reading out. */
 int ds_moe_layer_hostio(const ds_moe_shape *shape, const ds_moe_weights *weights,
                         const void *x_host, int64_t T, float *out_host, void *workspace,
                         size_t workspace_bytes, void *stream, char *err, size_t errlen);
