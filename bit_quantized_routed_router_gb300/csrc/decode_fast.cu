@@ -341,6 +341,7 @@ __device__ __forceinline__ float ord_val(uint32_t k) {
 // stable route puts pair p at #(pairs with a smaller expert, or the same
 // expert and a smaller p).  Returns the calling lane's RouteCache entries; with
 // publish, also writes ids, w, counts, offsets, perm, pos and used.
+template <int PMAX>
 __device__ RouteCache select_route_warp(const Args &a, bool publish, volatile int *loaded = nullptr) {
   const int lane = threadIdx.x & 31, P = a.T * a.k;
   int my_id = 0;     // lane p: expert of pair p
@@ -399,41 +400,41 @@ __device__ RouteCache select_route_warp(const Args &a, bool publish, volatile in
   float ex = lane < P ? __expf(my_lg - m0) : 0.f;
   // every pair's expert, exponential and (below) rank in registers: the
   // shuffles are independent and issue back to back
-  int idq[32];
+  int idq[PMAX];  // (PMAX >= T * k)
 #pragma unroll
-  for (int q = 0; q < 32; ++q) idq[q] = __shfl_sync(0xffffffffu, my_id, q);
-  float exj[32];  // the exponentials of this lane's token, pick order
+  for (int q = 0; q < PMAX; ++q) idq[q] = __shfl_sync(0xffffffffu, my_id, q);
+  float exj[PMAX];  // the exponentials of this lane's token, pick order
 #pragma unroll
-  for (int j = 0; j < 32; ++j) exj[j] = __shfl_sync(0xffffffffu, ex, min(j0 + j, 31));
+  for (int j = 0; j < PMAX; ++j) exj[j] = __shfl_sync(0xffffffffu, ex, min(j0 + j, 31));
   float den = 0.f;
 #pragma unroll
-  for (int j = 0; j < 32; ++j)
+  for (int j = 0; j < PMAX; ++j)
     if (j < a.k) den += exj[j];
   const float my_w = lane < P ? a.routed_scale * (ex / den) : 0.f;
   // ranks
   int rank = 0, first = 1, ui = 0;
 #pragma unroll
-  for (int q = 0; q < 32; ++q)
+  for (int q = 0; q < PMAX; ++q)
     if (q < P) {
       rank += (idq[q] < my_id) || (idq[q] == my_id && q < lane);
       if (idq[q] == my_id && q < lane) first = 0;
     }
   const unsigned firsts = __ballot_sync(0xffffffffu, lane < P && first);
 #pragma unroll
-  for (int q = 0; q < 32; ++q)  // distinct experts below mine
+  for (int q = 0; q < PMAX; ++q)  // distinct experts below mine
     if (q < P) ui += ((firsts >> q) & 1u) && idq[q] < my_id;
   RouteCache r;
   r.nu = __popc(firsts);
-  int rkq[32], uiq[32];
+  int rkq[PMAX], uiq[PMAX];
 #pragma unroll
-  for (int q = 0; q < 32; ++q) {
+  for (int q = 0; q < PMAX; ++q) {
     rkq[q] = __shfl_sync(0xffffffffu, rank, q);
     uiq[q] = __shfl_sync(0xffffffffu, ui, q);
   }
   // lane p learns perm[p]: the pair whose rank is p
   int perm_p = 0;
 #pragma unroll
-  for (int q = 0; q < 32; ++q)
+  for (int q = 0; q < PMAX; ++q)
     if (q < P && rkq[q] == lane) perm_p = q;
   r.perm = perm_p;
   r.w = my_w;
@@ -441,10 +442,10 @@ __device__ RouteCache select_route_warp(const Args &a, bool publish, volatile in
   // lane u learns used[u], its first position and its pair count
   int used_u = 0, base_u = 0, cnt_u = 0;
 #pragma unroll
-  for (int q = 0; q < 32; ++q)
+  for (int q = 0; q < PMAX; ++q)
     if (q < P && ((firsts >> q) & 1u) && uiq[q] == lane) { used_u = idq[q]; base_u = rkq[q]; }
 #pragma unroll
-  for (int q = 0; q < 32; ++q)
+  for (int q = 0; q < PMAX; ++q)
     if (q < P) cnt_u += (lane < r.nu && idq[q] == used_u) ? 1 : 0;
   r.used = used_u;
   r.base = base_u;
@@ -529,7 +530,7 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
     // every CTA selects and routes on its own (a few hundred logits); CTA 0
     // also publishes the route for the down kernel and the debug outputs
     pdl_wait();  // the router logits are complete and visible
-    const RouteCache r = select_route_warp(a, blockIdx.x == 0);
+    const RouteCache r = select_route_warp<PMAXD>(a, blockIdx.x == 0);
     s_rt[0][lane] = r.perm; s_rt[1][lane] = r.used; s_rt[2][lane] = r.base; s_rt[3][lane] = r.cnt;
     s_rt[4][lane] = r.nu;
     s_w[lane] = r.w;
@@ -788,6 +789,7 @@ constexpr uint32_t S_STAGE = 32768;              // bytes per ring stage
 constexpr int S_NS = 3;                          // ring stages
 constexpr int S_GU = S_CONS;                     // routed gate/up rows per tile (one per warp)
 constexpr int S_MAXP = 64;                       // slots x rows of a phase-B tile
+constexpr int S_MAXK = 8;                        // top-k at most
 constexpr int S_MAXT = 16;                       // shared or phase-B tiles of one block
 constexpr uint64_t S_LIMIT_NS = 2000000000ull;   // bound of every wait
 
@@ -988,7 +990,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
   // ---------------------------------------------------------------- router --
   if (warp == S_CONS + 1) {
     pdl_wait();  // router logits complete and visible
-    const RouteCache r = select_route_warp(a, bid == 0, &S.lg_loaded);
+    const RouteCache r = select_route_warp<S_MAXK>(a, bid == 0, &S.lg_loaded);  // one token: k pairs
     S.rt_used[lane] = r.used;
     S.rt_pos[lane] = r.pos;
     S.rt_w[lane] = r.w;
@@ -1445,7 +1447,7 @@ bool fused_decode_supported(const Shape &sh, int64_t T) {
 }
 
 bool stream_decode_supported(const Shape &sh, int64_t T) {
-  if (T != 1 || !fused_decode_supported(sh, T)) return false;
+  if (T != 1 || sh.k > S_MAXK || !fused_decode_supported(sh, T)) return false;
   const int nb_d = sh.D / QK, nb_f = sh.F / QK, nslots = std::min(sh.E, sh.k);
   const int rb = stream_rows_b(sh.D, sh.F, sh.Fs, nslots);
   static int sms = 0;
