@@ -268,7 +268,8 @@ def time_stack(cfg, iters, dev, warmup=3):
     """The 43-layer stack (x += layer(bf16(RMSNorm(x))) per layer, T tokens):
     (ms per step, bytes read per step, distinct experts per layer, path).  One
     step = the residual reset to the same input (a 128 KB device copy) + one
-    ds_moe_stack call over every layer, all experts resident.  The experts a
+    ds_moe_stack call over every layer, all experts resident, captured once
+    into a CUDA graph and replayed.  The experts a
     step reads are counted on an untimed pass that advances the same residual
     one layer at a time (bit-identical to the multi-layer call) and reads each
     layer's expert counts from a ds_moe_layer call on the normalised input."""
@@ -295,11 +296,18 @@ def time_stack(cfg, iters, dev, warmup=3):
         x.copy_(x0)
         ds.stack(sh, Ws, x, ws)
     torch.cuda.synchronize(dev)
+    # the step (residual reset + one ds_moe_stack call, 8 launches per layer)
+    # captured once into a CUDA graph and replayed
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        x.copy_(x0)
+        ds.stack(sh, Ws, x, ws)
+    graph.replay()
+    torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(iters):
-        x.copy_(x0)
-        ds.stack(sh, Ws, x, ws)
+        graph.replay()
     e1.record()
     torch.cuda.synchronize(dev)
     ds.sync_status()
