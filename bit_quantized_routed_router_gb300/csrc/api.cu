@@ -68,8 +68,11 @@ int check_shape(const ds_moe_shape *s, char *err, size_t errlen, Shape *out) {
     return fail(err, errlen, DS_ERR_INVALID_ARG, "x_dtype/router_dtype must be DS_F32 or DS_BF16");
   if (!isfinite(s->routed_scale))
     return fail(err, errlen, DS_ERR_INVALID_ARG, "routed_scale is not finite");
+  if (!isfinite(s->logit_scale) || s->logit_scale < 0.f)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "logit_scale must be finite and >= 0");
   *out = Shape{s->n_embd, s->n_expert, s->n_ff, s->n_ff_shared, s->top_k,
-               s->x_dtype, s->router_dtype, s->routed_scale};
+               s->x_dtype, s->router_dtype, s->routed_scale,
+               s->logit_scale == 0.f ? 1.f : s->logit_scale};
   return DS_OK;
 }
 

@@ -238,7 +238,7 @@ __device__ __forceinline__ float shflf(float v, int l) { return __shfl_sync(0xff
 
 struct Args {
   int D, E, F, Fs, k, T;
-  float routed_scale;
+  float routed_scale, logit_scale;
   const void *router_w;
   int router_f32;
   const float *bias;
@@ -337,7 +337,7 @@ __device__ __forceinline__ float ord_val(uint32_t k) {
 }
 
 // Selection and route by one warp (T * k <= 32): top-k by logit, ties to the
-// lower index, weights = routed_scale * softmax over the selected logits; the
+// lower index, weights = routed_scale * softmax over logit_scale * the selected logits; the
 // stable route puts pair p at #(pairs with a smaller expert, or the same
 // expert and a smaller p).  Returns the calling lane's RouteCache entries; with
 // publish, also writes ids, w, counts, offsets, perm, pos and used.
@@ -397,7 +397,7 @@ __device__ RouteCache select_route_warp(const Args &a, bool publish, volatile in
   // weights: softmax over each token's selected logits
   const int tok = lane / max(a.k, 1), j0 = tok * a.k;
   const float m0 = __shfl_sync(0xffffffffu, my_lg, min(j0, 31));
-  float ex = lane < P ? __expf(my_lg - m0) : 0.f;
+  float ex = lane < P ? __expf(a.logit_scale * (my_lg - m0)) : 0.f;
   // every pair's expert, exponential and (below) rank in registers: the
   // shuffles are independent and issue back to back
   int idq[PMAX];  // (PMAX >= T * k)
@@ -1466,6 +1466,7 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
   Args a{};
   a.D = sh.D; a.E = sh.E; a.F = sh.F; a.Fs = sh.Fs; a.k = sh.k; a.T = (int)wk.T;
   a.routed_scale = sh.routed_scale;
+  a.logit_scale = sh.logit_scale;
   a.router_w = W.router_w;
   a.router_f32 = sh.router_dtype == DS_F32;
   a.bias = W.router_bias;

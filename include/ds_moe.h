@@ -71,6 +71,10 @@ typedef struct {
   int32_t x_dtype;      /* ds_dtype of x                                     */
   int32_t router_dtype; /* ds_dtype of router_w                              */
   float routed_scale;   /* multiplies the k routing weights (1.0 default)    */
+  float logit_scale;    /* multiplies the selected logits before their softmax
+                           (the other reading of [UDS] 5.3.5's 1.5 "before
+                           softmax"); 1 = plain softmax, 0 is taken as 1; the
+                           selection does not depend on it                  */
 } ds_moe_shape;
 
 typedef struct {

@@ -247,9 +247,11 @@ void oracle_router_logits(const double *x, int64_t T, int64_t D, const double *w
 /* Top-k selection and weights for each token ([UDS] 5.3.2: the top-k experts
  * by router probability, weighted by the router probabilities).  Selection
  * by logit, ties to the lower index, in descending order; the weights are the
- * softmax over the k selected logits times routed_scale. */
+ * softmax over logit_scale times the k selected logits ([UDS] 5.3.5: a scale
+ * applied "before softmax"; 1 = plain softmax), times routed_scale ([UDS]
+ * 5.3.2: "a multiplier on router probabilities"). */
 void oracle_select(const double *logits, int64_t T, int64_t E, int32_t k, double routed_scale,
-                   int32_t *ids, double *w) {
+                   double logit_scale, int32_t *ids, double *w) {
   char *taken = (char *)malloc((size_t)E);
   for (int64_t t = 0; t < T; ++t) {
     const double *L = logits + t * E;
@@ -262,8 +264,9 @@ void oracle_select(const double *logits, int64_t T, int64_t E, int32_t k, double
       ids[t * k + j] = (int32_t)best;
     }
     double mx = L[ids[t * k]], den = 0.0;
-    for (int32_t j = 0; j < k; ++j) den += exp(L[ids[t * k + j]] - mx);
-    for (int32_t j = 0; j < k; ++j) w[t * k + j] = routed_scale * exp(L[ids[t * k + j]] - mx) / den;
+    for (int32_t j = 0; j < k; ++j) den += exp(logit_scale * (L[ids[t * k + j]] - mx));
+    for (int32_t j = 0; j < k; ++j)
+      w[t * k + j] = routed_scale * exp(logit_scale * (L[ids[t * k + j]] - mx)) / den;
   }
   free(taken);
 }

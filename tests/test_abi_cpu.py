@@ -59,7 +59,9 @@ def test_workspace_bytes_and_validation(L):
            ds.MoEShape(4096, 256, 2000, 2048, 6), ds.MoEShape(4096, 256, 2048, 100, 6),
            ds.MoEShape(4096, 256, 2048, 2048, 0), ds.MoEShape(4096, 4, 2048, 2048, 5),
            ds.MoEShape(4096, 256, 2048, 2048, 6, x_dtype=7),
-           ds.MoEShape(4096, 256, 2048, 2048, 6, routed_scale=float("nan"))]
+           ds.MoEShape(4096, 256, 2048, 2048, 6, routed_scale=float("nan")),
+           ds.MoEShape(4096, 256, 2048, 2048, 6, logit_scale=-1.0),
+           ds.MoEShape(4096, 256, 2048, 2048, 6, logit_scale=float("inf"))]
     for b in bad:
         with pytest.raises(ds.DsMoeError) as ei:
             ds.workspace_bytes(b, 4)

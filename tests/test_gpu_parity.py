@@ -40,10 +40,11 @@ def gpu_quantize(w_np):
     return out.cpu().numpy().reshape(w.shape[0], -1)
 
 
-def run_layer(cfg, W, x, scale=1.0):
+def run_layer(cfg, W, x, scale=1.0, logit_scale=1.0):
     T = x.shape[0]
     sh = synthetic.shape_of(cfg)
     sh.routed_scale = scale
+    sh.logit_scale = logit_scale
     ws = torch.empty(ds.workspace_bytes(sh, T), dtype=torch.uint8, device="cuda")
     out = torch.empty((T, cfg.D), dtype=torch.float32, device="cuda")
     P = T * cfg.k
@@ -157,13 +158,13 @@ def oracle_case(cfg, layer=0):
     return lo, att, x
 
 
-def layer_parity(cfg, tol, scale=1.0):
+def layer_parity(cfg, tol, scale=1.0, logit_scale=1.0):
     lo, att, x64 = oracle_case(cfg)
     W = synthetic.build_layer(cfg)
     x = synthetic.build_x(cfg, att)
-    out, dbg = run_layer(cfg, W, x, scale)
+    out, dbg = run_layer(cfg, W, x, scale, logit_scale)
     L = lo.logits(x64)
-    ids, w = oracle.select(L, cfg.k, scale)
+    ids, w = oracle.select(L, cfg.k, scale, logit_scale)
     check_route_full(dbg, ids, cfg.E)
     res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
     check_close(dbg["logits"], L, 1e-5, "logits")
@@ -175,11 +176,16 @@ def test_tiny_layer_parity():
     layer_parity(dsgen.TINY, DECODE_TOL)
 
 
-@pytest.mark.parametrize("variant", ["k_eq_E", "one_expert", "shared", "scale1.5", "T33", "T1"])
+@pytest.mark.parametrize("variant", ["k_eq_E", "one_expert", "shared", "scale1.5", "logit1.5", "T33",
+                                     "T1", "T2logit1.5"])
 def test_tiny_variants(variant):
+    """Variants of the tiny layer; logit1.5 scales the selected logits before
+    the softmax (the grouped path's selection kernel; T2logit1.5: the
+    three-kernel path's router warp)."""
     from dataclasses import replace
     c = dsgen.TINY
     scale = 1.0
+    logit_scale = 1.0
     if variant == "k_eq_E":
         c = replace(c, k=16)
     elif variant == "one_expert":
@@ -188,11 +194,16 @@ def test_tiny_variants(variant):
         c = replace(c, Fs=128, shared_sigma=0.02)
     elif variant == "scale1.5":
         scale = 1.5
+    elif variant == "logit1.5":
+        logit_scale = 1.5
+    elif variant == "T2logit1.5":
+        c = replace(c, T=2)
+        logit_scale = 1.5
     elif variant == "T33":
         c = replace(c, T=33, k=3)
     elif variant == "T1":
         c = replace(c, T=1)
-    layer_parity(c, DECODE_TOL, scale)
+    layer_parity(c, DECODE_TOL, scale, logit_scale)
 
 
 def _small(T, Fs, k=2, E=16, dtype="f32"):
@@ -268,6 +279,20 @@ def test_decode_b1_parity(decode1):
     (res, ids, w, L) = lo.forward(x64)
     check_route_full(dbg, ids, cfg.E)
     check_close(dbg["logits"], L, 1e-5, "logits")
+    check_close(out, res, DECODE_TOL)
+
+
+def test_decode_b1_logit_scale(decode1):
+    """Flash decode B=1 (the one-token kernel's router warp) with both
+    readings of the pages' 1.5: weights scaled, and logits scaled before the
+    softmax."""
+    cfg, lo, att, x64, W = decode1
+    out, dbg = run_layer(cfg, W, synthetic.build_x(cfg, att), 1.5, 1.5)
+    L = lo.logits(x64)
+    ids, w = oracle.select(L, cfg.k, 1.5, 1.5)
+    check_route_full(dbg, ids, cfg.E)
+    assert np.max(np.abs(dbg["w"] - w)) <= 1e-5
+    res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
     check_close(out, res, DECODE_TOL)
 
 

@@ -290,6 +290,31 @@ def test_select_k_equals_E_is_full_softmax_and_scale():
     assert np.allclose(w15, 1.5 * w, rtol=1e-15, atol=0)
 
 
+def test_select_logit_scale():
+    """The logit scale ([UDS] 5.3.5's reading of the 1.5 as a scale applied
+    before the softmax): the picks do not change; for k = 2 the first weight
+    is the logistic function of s times the gap (closed form); s = 1 is the
+    plain softmax; a large s puts all the weight on the top logit."""
+    rng = np.random.default_rng(11)
+    L = rng.normal(size=(6, 40))
+    ids1, w1 = oracle.select(L, 6)
+    for s_ in (0.5, 1.5, 3.0):
+        ids_s, w_s = oracle.select(L, 6, logit_scale=s_)
+        assert np.array_equal(ids_s, ids1)
+        assert np.allclose(w_s.sum(1), 1.0, rtol=0, atol=1e-14)
+    _, w_one = oracle.select(L, 6, logit_scale=1.0)
+    assert np.array_equal(w_one, w1)
+    ids2, w2 = oracle.select(L, 2, logit_scale=1.5)
+    gap = np.take_along_axis(L, ids2[:, :1], 1) - np.take_along_axis(L, ids2[:, 1:], 1)
+    assert np.allclose(w2[:, :1], 1.0 / (1.0 + np.exp(-1.5 * gap)), rtol=1e-14, atol=0)
+    Ls = np.array([[0.0, 3.0, 1.0, 2.0]])
+    _, w_big = oracle.select(Ls, 3, logit_scale=60.0)
+    assert w_big[0, 0] >= 1 - 1e-15 and w_big[0, 1] < 1e-25 and w_big[0, 2] < 1e-50
+    _, w_mix = oracle.select(L, 6, routed_scale=1.5, logit_scale=1.5)
+    _, w_l = oracle.select(L, 6, logit_scale=1.5)
+    assert np.allclose(w_mix, 1.5 * w_l, rtol=1e-15, atol=0)
+
+
 def test_route_matches_stable_sort():
     rng = np.random.default_rng(5)
     for T, k, E in ((1, 6, 256), (37, 6, 256), (8, 2, 16), (200, 4, 7)):
