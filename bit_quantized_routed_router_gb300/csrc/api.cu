@@ -144,9 +144,15 @@ int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *ou
     if ((e = cudaMemsetAsync(wk.ctrl, 0, 256, s)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "workspace control reset");
     if (wk.tc && aligned(x, 16) && prefill_tc_supported(sh, wk.T)) {
-      if ((e = launch_router_tc(sh, W, x, wk, s)) != cudaSuccess)
-        return cuda_fail(err, errlen, e, "router (tensor cores)");
-      if ((e = launch_select_route(sh, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
+      // the router GEMM's tiles hold 256 tokens x 128 experts: below 256
+      // tokens it would run on a couple of SMs, so the GEMV router serves
+      if (wk.T < 256) {
+        if ((e = launch_route(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
+      } else {
+        if ((e = launch_router_tc(sh, W, x, wk, s)) != cudaSuccess)
+          return cuda_fail(err, errlen, e, "router (tensor cores)");
+        if ((e = launch_select_route(sh, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
+      }
       if ((e = launch_prefill_tc(sh, W, x, wk, wk.tc, s)) != cudaSuccess)
         return cuda_fail(err, errlen, e, "expert FFN (tensor cores)");
     } else {

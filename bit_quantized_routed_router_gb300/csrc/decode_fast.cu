@@ -327,15 +327,6 @@ struct RouteCache {
   int pos;  // lane p: position of pair p in the route (select_route_warp only)
 };
 
-// fp32 -> unsigned key with the same order (for non-NaN values), and back.
-__device__ __forceinline__ uint32_t ord_key(float f) {
-  const uint32_t b = __float_as_uint(f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float ord_val(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 // Selection and route by one warp (T * k <= 32): top-k by logit, ties to the
 // lower index, weights = routed_scale * softmax over logit_scale * the selected logits; the
 // stable route puts pair p at #(pairs with a smaller expert, or the same

@@ -74,27 +74,35 @@ __device__ void select_token(const float *__restrict__ L, int E, int k, float ro
   uint32_t taken = 0;  // bit i: element lane + 32 i already selected
   int sel[16];
   float selv[16];
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+  // each lane's best remaining candidate; a pick is the warp's largest
+  // order-preserving key (two hardware reductions: the key, then the lowest
+  // index holding it), and only the lane that supplied it rescans
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  auto rescan = [&]() {
+    bv = -INFINITY;
+    bi = 0x7fffffff;
     for (int i = 0, e = lane; e < E; ++i, e += 32) {
       if (taken & (1u << i)) continue;
-      float v = L[e];
+      const float v = L[e];
       if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-    }
-    if (bi < 0 || bi >= E) {  // only possible with NaN logits
+  };
+  rescan();
+  for (int j = 0; j < k; ++j) {
+    const uint32_t key = ord_key(bv + 0.f);  // -0 as +0: equal logits tie
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+    int wi = (int)__reduce_min_sync(0xffffffffu, key == mk ? (uint32_t)bi : 0x7fffffffu);
+    if (wi < 0 || wi >= E) {  // only possible with NaN logits
       if (lane == 0) flag(st, ST_BAD_ID);
-      bi = 0;
+      wi = 0;
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    sel[j] = bi;
-    selv[j] = bv;
+    if ((wi & 31) == lane && wi == bi) {
+      taken |= 1u << (wi >> 5);
+      rescan();
+    }
+    sel[j] = wi;
+    selv[j] = ord_val(mk);
   }
   if (lane == 0) {
     const float m = selv[0];
@@ -293,7 +301,7 @@ cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x
   const int64_t T = wk.T;
   const int E = sh.E, D = sh.D;
   unsigned *st = status_word();
-  const int tb = T <= 64 ? (int)T : 16;
+  const int tb = T <= 4 ? (int)T : T <= 64 ? 4 : 16;  // tokens per warp (the router row stays in L1)
   dim3 g((E + 7) / 8, (unsigned)((T + tb - 1) / tb));
   if (sh.x_dtype == DS_BF16) {
     if (sh.router_dtype == DS_BF16)
