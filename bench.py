@@ -219,7 +219,7 @@ def gpu_arm(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": "decode step: route_kernel + stream_kernel (both timed as one launch)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": pk_kind,
-                     "traffic": None, "algorithmic_bytes": bytes_per_step},
+                     "traffic": DECODE_STEP_DRAM_BYTES, "algorithmic_bytes": bytes_per_step},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.D * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.D * 4},
         "gpu_launches": args.steps * LAUNCHES_PER_DECODE_STEP,
@@ -229,6 +229,11 @@ def gpu_arm(args, rank, world, local_rank):
 
 
 LAUNCHES_PER_DECODE_STEP = 2  # router logits; the one-token streaming kernel
+# DRAM bytes read + written by one decode step (route_kernel 2,117,888 read;
+# stream_kernel 99,979,008 read + 76,288 written), from one ncu capture of
+# these kernels as they stand (the command is in the decode profile summary);
+# to be set back to None whenever either kernel changes
+DECODE_STEP_DRAM_BYTES = 2_117_888 + 99_979_008 + 76_288
 
 PREFILL_FLOPS = 1.4517e12  # 4096 x (6*3*2*D*F + 3*2*D*F + 2*D*E) at the Flash shape
 
