@@ -23,7 +23,7 @@
  *          (yashdatta.dev), "Where the parameters actually are" (gate, up
  *          and down per expert; 3 x 4096 x 2048 parameters per expert).
  *
- * Readings where the pages are silent (all stated again in the design doc):
+ * Readings where the pages are silent:
  *   - Block byte layout: bytes [0,16) hold sub-block s's scale (low nibble)
  *     and min (high nibble); [16,80) the 2-bit codes, weight j at byte
  *     16 + j/4, bits 2*(j%4); [80,82) d and [82,84) dmin, fp16 little-endian.
