@@ -65,6 +65,51 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX *__restrict
   }
 }
 
+// Small batches (T <= 64, D a multiple of 1024): two experts per block and a
+// quarter of n_embd per warp.  The warp keeps its quarter of the router row
+// in registers and walks the tokens, so the row is read once; the quarters
+// are added in a fixed order.
+template <typename TX, typename TW>
+__global__ void __launch_bounds__(256) router_small_kernel(const TX *__restrict__ x,
+                                                           const TW *__restrict__ wr,
+                                                           const float *__restrict__ bias, int T,
+                                                           int D, int E, float *__restrict__ logits) {
+  __shared__ float part[8][64];  // [warp][token] partial logits
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 2 + (warp >> 2), len = D / 4, c0 = (warp & 3) * len;
+  const int nch = len / 256;  // 8-element chunks per lane (<= 8)
+  if (e < E) {
+    float wv[8][8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (c < nch) load8<TW>(wr + (int64_t)e * D + c0 + 256 * c + 8 * lane, wv[c]);
+#pragma unroll 2
+    for (int t = 0; t < T; ++t) {
+      const TX *xr = x + (int64_t)t * D + c0 + 8 * lane;
+      float xv[8][8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if (c < nch) load8<TX>(xr + 256 * c, xv[c]);
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if (c < nch) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc = fmaf(xv[c][i], wv[c][i], acc);
+        }
+      acc = warp_sum(acc);
+      if (lane == 0) part[warp][t] = acc;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 2 * T; i += blockDim.x) {
+    const int r = i / T, t = i % T, ee = blockIdx.x * 2 + r;
+    if (ee < E)
+      logits[(int64_t)t * E + ee] =
+          ((part[4 * r][t] + part[4 * r + 1][t]) + part[4 * r + 2][t]) + part[4 * r + 3][t] + (bias ? bias[ee] : 0.f);
+  }
+}
+
 // Top-k of one token's logits in the calling warp: ids in descending logit
 // order, ties to the lower index; weights = routed_scale * softmax over
 // logit_scale * the selected logits.  E <= 1024, k <= 16.
@@ -301,9 +346,23 @@ cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x
   const int64_t T = wk.T;
   const int E = sh.E, D = sh.D;
   unsigned *st = status_word();
-  const int tb = T <= 4 ? (int)T : T <= 64 ? 4 : 16;  // tokens per warp (the router row stays in L1)
+  const int tb = T <= 64 ? (int)T : 16;
   dim3 g((E + 7) / 8, (unsigned)((T + tb - 1) / tb));
-  if (sh.x_dtype == DS_BF16) {
+  if (T <= 64 && D % 1024 == 0 && D <= 8192) {
+    const dim3 g2((E + 1) / 2);
+    if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16)
+      router_small_kernel<uint16_t, uint16_t><<<g2, 256, 0, s>>>(
+          (const uint16_t *)x, (const uint16_t *)W.router_w, W.router_bias, (int)T, D, E, wk.logits);
+    else if (sh.x_dtype == DS_BF16)
+      router_small_kernel<uint16_t, float><<<g2, 256, 0, s>>>(
+          (const uint16_t *)x, (const float *)W.router_w, W.router_bias, (int)T, D, E, wk.logits);
+    else if (sh.router_dtype == DS_BF16)
+      router_small_kernel<float, uint16_t><<<g2, 256, 0, s>>>(
+          (const float *)x, (const uint16_t *)W.router_w, W.router_bias, (int)T, D, E, wk.logits);
+    else
+      router_small_kernel<float, float><<<g2, 256, 0, s>>>(
+          (const float *)x, (const float *)W.router_w, W.router_bias, (int)T, D, E, wk.logits);
+  } else if (sh.x_dtype == DS_BF16) {
     if (sh.router_dtype == DS_BF16)
       router_logits_kernel<uint16_t, uint16_t><<<g, 256, 0, s>>>(
           (const uint16_t *)x, (const uint16_t *)W.router_w, W.router_bias, T, D, E, tb, wk.logits);
