@@ -67,38 +67,48 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX *__restrict
 
 // Small batches (T <= 64, D a multiple of 1024): two experts per block and a
 // quarter of n_embd per warp.  The warp keeps its quarter of the router row
-// in registers and walks the tokens, so the row is read once; the quarters
-// are added in a fixed order.
-template <typename TX, typename TW>
+// in registers (NCH 8-element chunks per lane) and walks the tokens in
+// batches of 16 / NCH, all of a batch's loads issued before any use; the
+// quarters are added in a fixed order.
+template <typename TX, typename TW, int NCH>
 __global__ void __launch_bounds__(256) router_small_kernel(const TX *__restrict__ x,
                                                            const TW *__restrict__ wr,
                                                            const float *__restrict__ bias, int T,
                                                            int D, int E, float *__restrict__ logits) {
+  constexpr int TB = 16 / NCH;  // tokens per batch
   __shared__ float part[8][64];  // [warp][token] partial logits
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 2 + (warp >> 2), len = D / 4, c0 = (warp & 3) * len;
-  const int nch = len / 256;  // 8-element chunks per lane (<= 8)
+  const int e = blockIdx.x * 2 + (warp >> 2), c0 = (warp & 3) * (D / 4);
   if (e < E) {
-    float wv[8][8];
+    float wv[NCH][8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      if (c < nch) load8<TW>(wr + (int64_t)e * D + c0 + 256 * c + 8 * lane, wv[c]);
-#pragma unroll 2
-    for (int t = 0; t < T; ++t) {
-      const TX *xr = x + (int64_t)t * D + c0 + 8 * lane;
-      float xv[8][8];
+    for (int c = 0; c < NCH; ++c) load8<TW>(wr + (int64_t)e * D + c0 + 256 * c + 8 * lane, wv[c]);
+    for (int t0 = 0; t0 < T; t0 += TB) {
+      float xv[TB][NCH][8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        if (c < nch) load8<TX>(xr + 256 * c, xv[c]);
-      float acc = 0.f;
+      for (int u = 0; u < TB; ++u)
+        if (t0 + u < T) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        if (c < nch) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc = fmaf(xv[c][i], wv[c][i], acc);
+          for (int c = 0; c < NCH; ++c) load8<TX>(x + (int64_t)(t0 + u) * D + c0 + 256 * c + 8 * lane, xv[u][c]);
         }
-      acc = warp_sum(acc);
-      if (lane == 0) part[warp][t] = acc;
+      float acc[TB];
+#pragma unroll
+      for (int u = 0; u < TB; ++u) {
+        acc[u] = 0.f;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[u] = fmaf(xv[u][c][i], wv[c][i], acc[u]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int u = 0; u < TB; ++u) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+      if (lane == 0) {
+#pragma unroll
+        for (int u = 0; u < TB; ++u)
+          if (t0 + u < T) part[warp][t0 + u] = acc[u];
+      }
     }
   }
   __syncthreads();
@@ -108,6 +118,20 @@ __global__ void __launch_bounds__(256) router_small_kernel(const TX *__restrict_
       logits[(int64_t)t * E + ee] =
           ((part[4 * r][t] + part[4 * r + 1][t]) + part[4 * r + 2][t]) + part[4 * r + 3][t] + (bias ? bias[ee] : 0.f);
   }
+}
+
+template <typename TX, typename TW>
+cudaError_t launch_router_small(const TX *x, const TW *wr, const float *bias, int T, int D, int E, float *logits,
+                                cudaStream_t s) {
+  const dim3 g((E + 1) / 2);
+  switch (D / 1024) {  // 8-element chunks per lane: D / 4 / 256
+    case 1: router_small_kernel<TX, TW, 1><<<g, 256, 0, s>>>(x, wr, bias, T, D, E, logits); break;
+    case 2: router_small_kernel<TX, TW, 2><<<g, 256, 0, s>>>(x, wr, bias, T, D, E, logits); break;
+    case 4: router_small_kernel<TX, TW, 4><<<g, 256, 0, s>>>(x, wr, bias, T, D, E, logits); break;
+    case 8: router_small_kernel<TX, TW, 8><<<g, 256, 0, s>>>(x, wr, bias, T, D, E, logits); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 // Top-k of one token's logits in the calling warp: ids in descending logit
@@ -348,20 +372,14 @@ cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x
   unsigned *st = status_word();
   const int tb = T <= 64 ? (int)T : 16;
   dim3 g((E + 7) / 8, (unsigned)((T + tb - 1) / tb));
-  if (T <= 64 && D % 1024 == 0 && D <= 8192) {
-    const dim3 g2((E + 1) / 2);
-    if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16)
-      router_small_kernel<uint16_t, uint16_t><<<g2, 256, 0, s>>>(
-          (const uint16_t *)x, (const uint16_t *)W.router_w, W.router_bias, (int)T, D, E, wk.logits);
-    else if (sh.x_dtype == DS_BF16)
-      router_small_kernel<uint16_t, float><<<g2, 256, 0, s>>>(
-          (const uint16_t *)x, (const float *)W.router_w, W.router_bias, (int)T, D, E, wk.logits);
-    else if (sh.router_dtype == DS_BF16)
-      router_small_kernel<float, uint16_t><<<g2, 256, 0, s>>>(
-          (const float *)x, (const uint16_t *)W.router_w, W.router_bias, (int)T, D, E, wk.logits);
-    else
-      router_small_kernel<float, float><<<g2, 256, 0, s>>>(
-          (const float *)x, (const float *)W.router_w, W.router_bias, (int)T, D, E, wk.logits);
+  const int dq = D / 1024;
+  if (T <= 64 && D % 1024 == 0 && (dq == 1 || dq == 2 || dq == 4 || dq == 8) && sh.x_dtype == sh.router_dtype) {
+    cudaError_t e2 = sh.x_dtype == DS_BF16
+                         ? launch_router_small<uint16_t, uint16_t>((const uint16_t *)x, (const uint16_t *)W.router_w,
+                                                                   W.router_bias, (int)T, D, E, wk.logits, s)
+                         : launch_router_small<float, float>((const float *)x, (const float *)W.router_w,
+                                                             W.router_bias, (int)T, D, E, wk.logits, s);
+    if (e2 != cudaSuccess) return e2;
   } else if (sh.x_dtype == DS_BF16) {
     if (sh.router_dtype == DS_BF16)
       router_logits_kernel<uint16_t, uint16_t><<<g, 256, 0, s>>>(
