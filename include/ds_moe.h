@@ -140,8 +140,9 @@ int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, 
  *   dbg  optional debug outputs (NULL to skip)
  * Tokens are independent: row t of out depends only on row t of x.
  * T == 0 is a no-op.  The kernels that run depend on T and the shape (see
- * ds_moe_layer_path): one token at the instantiated widths streams the whole
- * layer through one cooperative kernel; up to four tokens use a three-kernel
+ * ds_moe_layer_path): one token at the instantiated widths with top_k <= 8
+ * streams the whole layer through one cooperative kernel; up to four tokens
+ * (and one token otherwise) use a three-kernel
  * decode chain; T >= 5 with bf16 x and router and n_embd, n_ff multiples of
  * 1024 runs the expert FFNs as grouped tcgen05 GEMMs with fp16 operands
  * (dequantised weights and activations rounded once to fp16; an |x| or
