@@ -99,6 +99,20 @@ class Clocks:
 
 # ----------------------------------------------------------------- GPU arm --
 
+def replica_throughput(ms_local: float, steps: int, tokens_per_step: int, world: int, device):
+    """Whole-job (ms, tokens/s) of `world` independent replicas that each ran
+    `steps` steps of tokens_per_step tokens in ms_local: the job takes as long
+    as its slowest replica (max over ranks), and every replica's tokens count.
+    With world > 1 the process group must be initialised (nccl with a CUDA
+    device, gloo with the CPU)."""
+    import torch
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, world * steps * tokens_per_step / (ms_max / 1e3)
+
+
 def gpu_arm(args, rank, world, local_rank):
     import torch
     import bit_quantized_routed_router_gb300 as ds
@@ -174,12 +188,8 @@ def gpu_arm(args, rank, world, local_rank):
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
     ds.sync_status(s)
-    t = torch.tensor([ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max, value = replica_throughput(ms, args.steps, cfg.T, world, dev)
     ms_per_step = ms_max / args.steps
-    value = world * args.steps * cfg.T / (ms_max / 1e3)
 
     # end to end through the host-buffer entry point: x H2D, layer, out D2H per step
     xh = [x.cpu().pin_memory() for x in xs]
@@ -188,6 +198,9 @@ def gpu_arm(args, rank, world, local_rank):
     for i in range(args.warmup):
         ds.layer_hostio(sh, layers[i % R], xh[i % R], oh, ws_h, stream=s)
     torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
@@ -195,10 +208,7 @@ def gpu_arm(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    te = torch.tensor([e2e_ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_value = world * args.steps * cfg.T / (float(te.item()) / 1e3)
+    _, e2e_value = replica_throughput(e2e_ms, args.steps, cfg.T, world, dev)
 
     pk, pk_kind = peaks()
     hbm = float(pk.get("hbm_gbs", HBM_FALLBACK_GBS))
