@@ -110,7 +110,11 @@ def test_quantize_rejects_bad_arguments_on_host(L):
 def test_layer_path_host_checks(L):
     sh = ds.MoEShape(4096, 256, 2048, 2048, 6)
     assert ds.layer_path(sh, 0) == ds.PATH_NONE
-    assert ds.layer_path(sh, 8) in (ds.PATH_DECODE3, ds.PATH_GROUPED_GEMV)
+    # 8 tokens: the tensor cores where the device has them (and the driver
+    # can build tensor maps), the grouped GEMV path on a host without a GPU
+    import torch
+    expect = ds.PATH_TENSOR_CORE if torch.cuda.is_available() else ds.PATH_GROUPED_GEMV
+    assert ds.layer_path(sh, 8) == expect
     with pytest.raises(ds.DsMoeError):
         ds.layer_path(ds.MoEShape(4000, 256, 2048, 2048, 6), 4)
     with pytest.raises(ds.DsMoeError):
