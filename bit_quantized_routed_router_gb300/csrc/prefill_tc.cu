@@ -427,9 +427,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else if (warp >= TC_DQ0) {
     // ------------------------------------------------------ dequant warps --
-    // Thread dt owns one weight row of every stage: gate/up: row dt (gate
-    // rows, then up rows), all four sub-blocks; down: row dt % 128, sub-blocks
-    // 2 (dt / 128) and the next.  Its raw and destination offsets are fixed.
+    // Thread dt owns one weight row of every stage, all four of its
+    // sub-blocks: gate/up: row dt (gate rows 0-127, then up rows); down: row
+    // dt of the two 128-row blocks.  Its raw and destination offsets are fixed.
     constexpr int NSUB = 4;
     const int dt = threadIdx.x - TC_DQ0 * 32;  // 0 .. 255
     const int r = dt;
