@@ -42,7 +42,7 @@ class Shape(ctypes.Structure):
                 ("n_ff", ctypes.c_int32), ("n_ff_shared", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("x_dtype", ctypes.c_int32),
                 ("router_dtype", ctypes.c_int32), ("routed_scale", ctypes.c_float),
-                ("logit_scale", ctypes.c_float)]
+                ("logit_scale", ctypes.c_float), ("bias_select_only", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -127,10 +127,12 @@ class MoEShape:
     router_dtype: int = DS_BF16
     routed_scale: float = 1.0
     logit_scale: float = 1.0
+    bias_select_only: int = 0
 
     def c(self) -> Shape:
         return Shape(self.n_embd, self.n_expert, self.n_ff, self.n_ff_shared, self.top_k,
-                     self.x_dtype, self.router_dtype, self.routed_scale, self.logit_scale)
+                     self.x_dtype, self.router_dtype, self.routed_scale, self.logit_scale,
+                     self.bias_select_only)
 
 
 @dataclass

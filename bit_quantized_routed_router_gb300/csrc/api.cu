@@ -70,9 +70,11 @@ int check_shape(const ds_moe_shape *s, char *err, size_t errlen, Shape *out) {
     return fail(err, errlen, DS_ERR_INVALID_ARG, "routed_scale is not finite");
   if (!isfinite(s->logit_scale) || s->logit_scale < 0.f)
     return fail(err, errlen, DS_ERR_INVALID_ARG, "logit_scale must be finite and >= 0");
+  if (s->bias_select_only != 0 && s->bias_select_only != 1)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "bias_select_only must be 0 or 1");
   *out = Shape{s->n_embd, s->n_expert, s->n_ff, s->n_ff_shared, s->top_k,
                s->x_dtype, s->router_dtype, s->routed_scale,
-               s->logit_scale == 0.f ? 1.f : s->logit_scale};
+               s->logit_scale == 0.f ? 1.f : s->logit_scale, s->bias_select_only};
   return DS_OK;
 }
 
@@ -151,7 +153,8 @@ int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *ou
       } else {
         if ((e = launch_router_tc(sh, W, x, wk, s)) != cudaSuccess)
           return cuda_fail(err, errlen, e, "router (tensor cores)");
-        if ((e = launch_select_route(sh, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
+        if ((e = launch_select_route(sh, wk, W.router_bias, s)) != cudaSuccess)
+          return cuda_fail(err, errlen, e, "route");
       }
       if ((e = launch_prefill_tc(sh, W, x, wk, wk.tc, s)) != cudaSuccess)
         return cuda_fail(err, errlen, e, "expert FFN (tensor cores)");

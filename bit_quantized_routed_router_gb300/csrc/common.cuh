@@ -61,6 +61,7 @@ struct Shape {
   int x_dtype, router_dtype;
   float routed_scale;
   float logit_scale;  // 1: plain softmax over the selected logits
+  int bias_select_only;  // 1: the router bias steers the selection only
   int64_t nb_D() const { return (D + QK - 1) / QK; }
   int64_t nb_F() const { return (F + QK - 1) / QK; }
   int64_t gate_bytes() const { return (int64_t)F * nb_D() * QB; }

@@ -239,6 +239,7 @@ __device__ __forceinline__ float shflf(float v, int l) { return __shfl_sync(0xff
 struct Args {
   int D, E, F, Fs, k, T;
   float routed_scale, logit_scale;
+  int bias_select_only;  // the router bias steers the selection only
   const void *router_w;
   int router_f32;
   const float *bias;
@@ -387,8 +388,10 @@ __device__ RouteCache select_route_warp(const Args &a, bool publish, volatile in
   }
   // weights: softmax over each token's selected logits
   const int tok = lane / max(a.k, 1), j0 = tok * a.k;
-  const float m0 = __shfl_sync(0xffffffffu, my_lg, min(j0, 31));
-  float ex = lane < P ? __expf(a.logit_scale * (my_lg - m0)) : 0.f;
+  // (with the bias steering the selection only, it is taken back out here)
+  const float my_u = a.bias_select_only && a.bias && lane < P ? my_lg - __ldg(a.bias + my_id) : my_lg;
+  const float m0 = __shfl_sync(0xffffffffu, my_u, min(j0, 31));
+  float ex = lane < P ? __expf(a.logit_scale * (my_u - m0)) : 0.f;
   // every pair's expert, exponential and (below) rank in registers: the
   // shuffles are independent and issue back to back
   int idq[PMAX];  // (PMAX >= T * k)
@@ -1458,6 +1461,7 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
   a.D = sh.D; a.E = sh.E; a.F = sh.F; a.Fs = sh.Fs; a.k = sh.k; a.T = (int)wk.T;
   a.routed_scale = sh.routed_scale;
   a.logit_scale = sh.logit_scale;
+  a.bias_select_only = sh.bias_select_only;
   a.router_w = W.router_w;
   a.router_f32 = sh.router_dtype == DS_F32;
   a.bias = W.router_bias;

@@ -41,7 +41,10 @@ cudaError_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t in_dim, fl
 cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
                          cudaStream_t s);
 // The part of launch_route after the logits: selection and route.
-cudaError_t launch_select_route(const Shape &sh, const Work &wk, cudaStream_t s);
+// bias: the router bias the logits include (or null); with
+// sh.bias_select_only it is taken back out of the selected logits before the
+// softmax of the weights.
+cudaError_t launch_select_route(const Shape &sh, const Work &wk, const float *bias, cudaStream_t s);
 
 // Decode path: grouped dequantising GEMVs and the combine.
 cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const void *x,

@@ -136,9 +136,11 @@ cudaError_t launch_router_small(const TX *x, const TW *wr, const float *bias, in
 
 // Top-k of one token's logits in the calling warp: ids in descending logit
 // order, ties to the lower index; weights = routed_scale * softmax over
-// logit_scale * the selected logits.  E <= 1024, k <= 16.
+// logit_scale * the selected logits, from which `unbias` (the router bias,
+// when it steers the selection only; else null) is taken back out.
+// E <= 1024, k <= 16.
 __device__ void select_token(const float *__restrict__ L, int E, int k, float routed_scale, float logit_scale,
-                             int32_t *ids, float *w, unsigned *st) {
+                             const float *__restrict__ unbias, int32_t *ids, float *w, unsigned *st) {
   const int lane = threadIdx.x & 31;
   uint32_t taken = 0;  // bit i: element lane + 32 i already selected
   int sel[16];
@@ -174,6 +176,8 @@ __device__ void select_token(const float *__restrict__ L, int E, int k, float ro
     selv[j] = ord_val(mk);
   }
   if (lane == 0) {
+    if (unbias)
+      for (int j = 0; j < k; ++j) selv[j] -= unbias[sel[j]];
     const float m = selv[0];
     float den = 0.0f;
     for (int j = 0; j < k; ++j) den += __expf(logit_scale * (selv[j] - m));
@@ -186,11 +190,11 @@ __device__ void select_token(const float *__restrict__ L, int E, int k, float ro
 
 __global__ void __launch_bounds__(256) select_kernel(const float *__restrict__ logits, int64_t T,
                                                      int E, int k, float routed_scale, float logit_scale,
-                                                     int32_t *__restrict__ ids,
+                                                     const float *__restrict__ unbias, int32_t *__restrict__ ids,
                                                      float *__restrict__ w, unsigned *st) {
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  select_token(logits + t * E, E, k, routed_scale, logit_scale, ids + t * k, w + t * k, st);
+  select_token(logits + t * E, E, k, routed_scale, logit_scale, unbias, ids + t * k, w + t * k, st);
 }
 
 // Stable rank of each pair of one chunk inside its expert, in ascending pair
@@ -216,7 +220,7 @@ __device__ int chunk_rank(int e, bool valid, int *wtab, int E) {
 // exclusive scan, stable permutation and used-expert list, all in one block.
 __global__ void __launch_bounds__(ROUTE_CHUNK) select_route_small_kernel(
     const float *__restrict__ logits, int64_t T, int E, int k, float routed_scale, float logit_scale,
-    int32_t *__restrict__ ids, float *__restrict__ w, int32_t *__restrict__ counts,
+    const float *__restrict__ unbias, int32_t *__restrict__ ids, float *__restrict__ w, int32_t *__restrict__ counts,
     int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ pos,
     int32_t *__restrict__ used, unsigned *st) {
   extern __shared__ int sm[];
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(ROUTE_CHUNK) select_route_small_kernel(
   int *wtab = off + E + 1; // [32][E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int64_t t = warp; t < T; t += blockDim.x / 32)
-    select_token(logits + t * E, E, k, routed_scale, logit_scale, ids + t * k, w + t * k, st);
+    select_token(logits + t * E, E, k, routed_scale, logit_scale, unbias, ids + t * k, w + t * k, st);
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
   const int64_t P = T * k;
@@ -397,10 +401,11 @@ cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  return launch_select_route(sh, wk, s);
+  return launch_select_route(sh, wk, W.router_bias, s);
 }
 
-cudaError_t launch_select_route(const Shape &sh, const Work &wk, cudaStream_t s) {
+cudaError_t launch_select_route(const Shape &sh, const Work &wk, const float *bias, cudaStream_t s) {
+  const float *unbias = sh.bias_select_only ? bias : nullptr;
   const int64_t T = wk.T;
   const int E = sh.E, k = sh.k;
   unsigned *st = status_word();
@@ -418,12 +423,12 @@ cudaError_t launch_select_route(const Shape &sh, const Work &wk, cudaStream_t s)
   }
   if (P <= ROUTE_CHUNK) {
     size_t smem = sizeof(int) * (size_t)(E + E + 1 + 32 * E);
-    select_route_small_kernel<<<1, ROUTE_CHUNK, smem, s>>>(wk.logits, T, E, k, sh.routed_scale, sh.logit_scale,
+    select_route_small_kernel<<<1, ROUTE_CHUNK, smem, s>>>(wk.logits, T, E, k, sh.routed_scale, sh.logit_scale, unbias,
                                                            wk.ids, wk.w, wk.counts, wk.offsets,
                                                            wk.perm, wk.pos, wk.used, st);
     return cudaGetLastError();
   }
-  select_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(wk.logits, T, E, k, sh.routed_scale, sh.logit_scale, wk.ids,
+  select_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(wk.logits, T, E, k, sh.routed_scale, sh.logit_scale, unbias, wk.ids,
                                                         wk.w, st);
   const int64_t nc = (P + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
   route_hist_kernel<<<(unsigned)nc, ROUTE_CHUNK, sizeof(int) * E, s>>>(wk.ids, P, E, wk.chunk, st);

@@ -75,6 +75,9 @@ typedef struct {
                            (the other reading of [UDS] 5.3.5's 1.5 "before
                            softmax"); 1 = plain softmax, 0 is taken as 1; the
                            selection does not depend on it                  */
+  int32_t bias_select_only; /* 0: router_bias is part of the logits (selection
+                           and weights); 1: it steers the selection only and
+                           the weights use the logits without it            */
 } ds_moe_shape;
 
 typedef struct {

@@ -249,10 +249,13 @@ void oracle_router_logits(const double *x, int64_t T, int64_t D, const double *w
  * by logit, ties to the lower index, in descending order; the weights are the
  * softmax over logit_scale times the k selected logits ([UDS] 5.3.5: a scale
  * applied "before softmax"; 1 = plain softmax), times routed_scale ([UDS]
- * 5.3.2: "a multiplier on router probabilities"). */
+ * 5.3.2: "a multiplier on router probabilities").  unbias (or null): the
+ * router bias, taken back out of the selected logits for the weights when it
+ * is to steer the selection only. */
 void oracle_select(const double *logits, int64_t T, int64_t E, int32_t k, double routed_scale,
-                   double logit_scale, int32_t *ids, double *w) {
+                   double logit_scale, const double *unbias, int32_t *ids, double *w) {
   char *taken = (char *)malloc((size_t)E);
+  double *u = (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
   for (int64_t t = 0; t < T; ++t) {
     const double *L = logits + t * E;
     memset(taken, 0, (size_t)E);
@@ -263,11 +266,18 @@ void oracle_select(const double *logits, int64_t T, int64_t E, int32_t k, double
       taken[best] = 1;
       ids[t * k + j] = (int32_t)best;
     }
-    double mx = L[ids[t * k]], den = 0.0;
-    for (int32_t j = 0; j < k; ++j) den += exp(logit_scale * (L[ids[t * k + j]] - mx));
-    for (int32_t j = 0; j < k; ++j)
-      w[t * k + j] = routed_scale * exp(logit_scale * (L[ids[t * k + j]] - mx)) / den;
+    /* the weights' logits: with unbias (the router bias, when it steers the
+     * selection only) the bias is taken back out of the selected logits */
+    double mx = 0.0, den = 0.0;
+    for (int32_t j = 0; j < k; ++j) {
+      const int32_t e = ids[t * k + j];
+      u[j] = L[e] - (unbias ? unbias[e] : 0.0);
+      if (j == 0 || u[j] > mx) mx = u[j];
+    }
+    for (int32_t j = 0; j < k; ++j) den += exp(logit_scale * (u[j] - mx));
+    for (int32_t j = 0; j < k; ++j) w[t * k + j] = routed_scale * exp(logit_scale * (u[j] - mx)) / den;
   }
+  free(u);
   free(taken);
 }
 

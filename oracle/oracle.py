@@ -61,7 +61,7 @@ def lib():
         L.oracle_router_logits.restype = None
         L.oracle_router_logits.argtypes = [vp, i64, i64, vp, i64, vp, vp]
         L.oracle_select.restype = None
-        L.oracle_select.argtypes = [vp, i64, i64, i32, dbl, dbl, vp, vp]
+        L.oracle_select.argtypes = [vp, i64, i64, i32, dbl, dbl, vp, vp, vp]
         L.oracle_route.restype = None
         L.oracle_route.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp]
         L.oracle_moe_layer.restype = ctypes.c_int
@@ -122,12 +122,17 @@ def router_logits(x: np.ndarray, wr: np.ndarray, bias=None) -> np.ndarray:
     return out
 
 
-def select(logits: np.ndarray, k: int, routed_scale: float = 1.0, logit_scale: float = 1.0):
+def select(logits: np.ndarray, k: int, routed_scale: float = 1.0, logit_scale: float = 1.0,
+           unbias=None):
+    """unbias: the router bias the logits include, when it is to steer the
+    selection only (the weights then use the logits without it)."""
     L = _c(logits, np.float64)
     T, E = L.shape
     ids = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
-    lib().oracle_select(_ptr(L), T, E, k, routed_scale, logit_scale, _ptr(ids), _ptr(w))
+    ub = None if unbias is None else _c(unbias, np.float64)
+    lib().oracle_select(_ptr(L), T, E, k, routed_scale, logit_scale, None if ub is None else _ptr(ub),
+                        _ptr(ids), _ptr(w))
     return ids, w
 
 

@@ -61,7 +61,8 @@ def test_workspace_bytes_and_validation(L):
            ds.MoEShape(4096, 256, 2048, 2048, 6, x_dtype=7),
            ds.MoEShape(4096, 256, 2048, 2048, 6, routed_scale=float("nan")),
            ds.MoEShape(4096, 256, 2048, 2048, 6, logit_scale=-1.0),
-           ds.MoEShape(4096, 256, 2048, 2048, 6, logit_scale=float("inf"))]
+           ds.MoEShape(4096, 256, 2048, 2048, 6, logit_scale=float("inf")),
+           ds.MoEShape(4096, 256, 2048, 2048, 6, bias_select_only=2)]
     for b in bad:
         with pytest.raises(ds.DsMoeError) as ei:
             ds.workspace_bytes(b, 4)

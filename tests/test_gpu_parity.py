@@ -40,11 +40,12 @@ def gpu_quantize(w_np):
     return out.cpu().numpy().reshape(w.shape[0], -1)
 
 
-def run_layer(cfg, W, x, scale=1.0, logit_scale=1.0):
+def run_layer(cfg, W, x, scale=1.0, logit_scale=1.0, bias_select_only=0):
     T = x.shape[0]
     sh = synthetic.shape_of(cfg)
     sh.routed_scale = scale
     sh.logit_scale = logit_scale
+    sh.bias_select_only = bias_select_only
     ws = torch.empty(ds.workspace_bytes(sh, T), dtype=torch.uint8, device="cuda")
     out = torch.empty((T, cfg.D), dtype=torch.float32, device="cuda")
     P = T * cfg.k
@@ -158,13 +159,13 @@ def oracle_case(cfg, layer=0):
     return lo, att, x
 
 
-def layer_parity(cfg, tol, scale=1.0, logit_scale=1.0):
+def layer_parity(cfg, tol, scale=1.0, logit_scale=1.0, bias_select_only=0, W=None):
     lo, att, x64 = oracle_case(cfg)
-    W = synthetic.build_layer(cfg)
+    W = synthetic.build_layer(cfg) if W is None else W
     x = synthetic.build_x(cfg, att)
-    out, dbg = run_layer(cfg, W, x, scale, logit_scale)
+    out, dbg = run_layer(cfg, W, x, scale, logit_scale, bias_select_only)
     L = lo.logits(x64)
-    ids, w = oracle.select(L, cfg.k, scale, logit_scale)
+    ids, w = oracle.select(L, cfg.k, scale, logit_scale, lo.bias if bias_select_only else None)
     check_route_full(dbg, ids, cfg.E)
     res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
     check_close(dbg["logits"], L, 1e-5, "logits")
@@ -177,7 +178,7 @@ def test_tiny_layer_parity():
 
 
 @pytest.mark.parametrize("variant", ["k_eq_E", "one_expert", "shared", "scale1.5", "logit1.5", "T33",
-                                     "T1", "T2logit1.5"])
+                                     "T1", "T2logit1.5", "zipf", "zipf_select_only"])
 def test_tiny_variants(variant):
     """Variants of the tiny layer; logit1.5 scales the selected logits before
     the softmax (the grouped path's selection kernel; T2logit1.5: the
@@ -199,6 +200,11 @@ def test_tiny_variants(variant):
     elif variant == "T2logit1.5":
         c = replace(c, T=2)
         logit_scale = 1.5
+    elif variant in ("zipf", "zipf_select_only"):
+        c = replace(c, zipf_s=1.1)
+        if variant == "zipf_select_only":
+            layer_parity(c, DECODE_TOL, bias_select_only=1)
+            return
     elif variant == "T33":
         c = replace(c, T=33, k=3)
     elif variant == "T1":
@@ -294,6 +300,16 @@ def test_decode_b1_logit_scale(decode1):
     assert np.max(np.abs(dbg["w"] - w)) <= 1e-5
     res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
     check_close(out, res, DECODE_TOL)
+
+
+def test_zipf_bias_for_selection_only_decode_paths():
+    """The Flash layer with the Zipf router bias steering the selection only,
+    on the one-token kernel (T=1), the three-kernel chain (T=3) and the
+    tensor-core path (T=8): weights from the unbiased selected logits."""
+    from dataclasses import replace
+    W = synthetic.build_layer(dsgen.DECODE32_ZIPF)
+    for T, tol in ((1, DECODE_TOL), (3, DECODE_TOL), (8, PREFILL_TOL)):
+        layer_parity(replace(dsgen.DECODE32_ZIPF, T=T), tol, bias_select_only=1, W=W)
 
 
 @pytest.mark.parametrize("pinned", [True, False])

@@ -315,6 +315,30 @@ def test_select_logit_scale():
     assert np.allclose(w_mix, 1.5 * w_l, rtol=1e-15, atol=0)
 
 
+def test_select_bias_for_selection_only():
+    """A router bias that steers the selection only: the picks are those of
+    the biased logits, and the weights are the softmax of the selected logits
+    with the bias taken back out (k = 2: the logistic function of the
+    unbiased gap); a zero bias changes nothing."""
+    rng = np.random.default_rng(13)
+    L0 = rng.normal(size=(7, 24))
+    b = -1.1 * np.log(rng.permutation(24) + 1.0)
+    Lb = L0 + b
+    ids_b, w_b = oracle.select(Lb, 6)
+    ids_s, w_s = oracle.select(Lb, 6, unbias=b)
+    assert np.array_equal(ids_s, ids_b)
+    assert np.allclose(w_s.sum(1), 1.0, rtol=0, atol=1e-14)
+    assert not np.allclose(w_s, w_b)
+    u = np.take_along_axis(L0, ids_s, 1)
+    p = np.exp(u - u.max(1, keepdims=True))
+    assert np.allclose(w_s, p / p.sum(1, keepdims=True), rtol=1e-13, atol=0)
+    ids2, w2 = oracle.select(Lb, 2, unbias=b)
+    gap = np.take_along_axis(L0, ids2[:, :1], 1) - np.take_along_axis(L0, ids2[:, 1:], 1)
+    assert np.allclose(w2[:, :1], 1.0 / (1.0 + np.exp(-gap)), rtol=1e-13, atol=0)
+    _, w_zero = oracle.select(Lb, 6, unbias=np.zeros(24))
+    assert np.array_equal(w_zero, w_b)
+
+
 def test_route_matches_stable_sort():
     rng = np.random.default_rng(5)
     for T, k, E in ((1, 6, 256), (37, 6, 256), (8, 2, 16), (200, 4, 7)):
