@@ -172,18 +172,137 @@ static void q2k_dequantize_block(const uint8_t *blk, double *w) {
   }
 }
 
+/* ----------------------------------------------------------- Q4_K block --- */
+/* [UDS] 2.3.2 "K-Quant Formats (Q2_K, Q3_K, Q4_K, etc.)": a 144-byte block of
+ * 256 values (4.5 bits per value): an fp16 super-block scale d at offset 0,
+ * an fp16 minimum dmin at offset 2, eight 6-bit scales and eight 6-bit mins
+ * packed into the 12 bytes at offset 4, and the 256 4-bit values in the 128
+ * bytes at offset 16; eight sub-blocks of 32 values.
+ * Readings (the page gives the fields, not their packing or the search):
+ *   - the sixteen 6-bit fields sc_0..sc_7, m_0..m_7 form one 96-bit
+ *     little-endian integer in bytes 4..15, field i in bits [6i, 6i + 6);
+ *   - the code of value j sits in byte 16 + j/2, low nibble for even j;
+ *   - the quantiser follows the Q2_K rules with 16 levels and 6-bit fields:
+ *     dmin = smallest fp16 with 63 dmin >= max_s(-lo_s); m_s = smallest
+ *     integer with m_s dmin >= -lo_s; b_s = m_s dmin; d = smallest fp16 with
+ *     945 d >= hi_s + b_s for every s; sc_s = smallest integer with
+ *     15 d sc_s >= hi_s + b_s; q_j = clamp(floor((x_j + b_s)/(d sc_s) + 1/2),
+ *     0, 15) (0 when sc_s = 0); w_j = d sc_s q_j - dmin m_s.  All exact. */
+#define Q4BYTES 144
+#define Q4SUB 8
+
+static int q4k_get6(const uint8_t *blk, int i) {
+  int v = 0;
+  for (int k = 0; k < 6; ++k) {
+    const int bit = 6 * i + k;
+    v |= ((blk[4 + bit / 8] >> (bit % 8)) & 1) << k;
+  }
+  return v;
+}
+
+static void q4k_put6(uint8_t *blk, int i, int v) {
+  for (int k = 0; k < 6; ++k) {
+    const int bit = 6 * i + k;
+    blk[4 + bit / 8] |= (uint8_t)(((v >> k) & 1) << (bit % 8));
+  }
+}
+
+/* 63*h >= max_s(-lo_s) over the 8 sub-blocks; 63*h is exact in fp64. */
+static int q4_dmin_ok(double h, const void *c) {
+  const dmin_ctx *x = (const dmin_ctx *)c;
+  for (int s = 0; s < Q4SUB; ++s) if (63.0 * h < x->neg_lo[s]) return 0;
+  return 1;
+}
+
+/* 945*h - b_s >= hi_s for every sub-block; exact in fp64 (fp16 values times
+ * integers below 1024, so each side spans well under 53 bits). */
+static int q4_d_ok(double h, const void *c) {
+  const d_ctx *x = (const d_ctx *)c;
+  for (int s = 0; s < Q4SUB; ++s) if (945.0 * h - x->b[s] < x->hi[s]) return 0;
+  return 1;
+}
+
+/* Quantise one super-block of 256 values (reading above).  Returns 0, or -1
+ * when a value is not finite or |v| > 65504. */
+static int q4k_quantize_block(const double *x, uint8_t *out) {
+  double lo[Q4SUB], hi[Q4SUB], neg_lo[Q4SUB], b[Q4SUB];
+  int m[Q4SUB], sc[Q4SUB];
+  for (int s = 0; s < Q4SUB; ++s) {
+    double mn = 0.0, mx = -INFINITY;
+    for (int j = 0; j < 32; ++j) {
+      double v = x[32 * s + j];
+      if (!(fabs(v) <= 65504.0)) return -1;
+      if (v < mn) mn = v;
+      if (v > mx) mx = v;
+    }
+    lo[s] = mn;
+    hi[s] = mx;
+    neg_lo[s] = -mn;
+  }
+  dmin_ctx dc = {neg_lo};
+  int dmin_bits = fp16_smallest(q4_dmin_ok, &dc);
+  if (dmin_bits < 0) return -1;
+  double dmin = oracle_fp16_value((uint16_t)dmin_bits);
+  for (int s = 0; s < Q4SUB; ++s) {
+    int mm = 0;
+    while (mm < 63 && (double)mm * dmin < -lo[s]) ++mm;
+    m[s] = mm;
+    b[s] = (double)mm * dmin; /* exact */
+  }
+  d_ctx cx = {hi, b};
+  int d_bits = fp16_smallest(q4_d_ok, &cx);
+  if (d_bits < 0) return -1;
+  double d = oracle_fp16_value((uint16_t)d_bits);
+  for (int s = 0; s < Q4SUB; ++s) {
+    int c = 0;
+    while (c < 63 && 15.0 * d * (double)c - b[s] < hi[s]) ++c; /* exact */
+    sc[s] = c;
+  }
+  memset(out, 0, Q4BYTES);
+  out[0] = (uint8_t)(d_bits & 0xFF);
+  out[1] = (uint8_t)(d_bits >> 8);
+  out[2] = (uint8_t)(dmin_bits & 0xFF);
+  out[3] = (uint8_t)(dmin_bits >> 8);
+  for (int s = 0; s < Q4SUB; ++s) {
+    q4k_put6(out, s, sc[s]);
+    q4k_put6(out, Q4SUB + s, m[s]);
+  }
+  for (int j = 0; j < QK; ++j) {
+    int s = j / 32, q = 0;
+    if (sc[s] > 0)
+      for (int i = 1; i <= 15; ++i) {
+        double thr = ((double)i - 0.5) * d * (double)sc[s] - b[s]; /* exact */
+        if (x[j] >= thr) ++q;
+      }
+    out[16 + j / 2] |= (uint8_t)(q << (4 * (j % 2)));
+  }
+  return 0;
+}
+
+/* w_j = d*sc_s*q_j - dmin*m_s, exact in fp64. */
+static void q4k_dequantize_block(const uint8_t *blk, double *w) {
+  double d = oracle_fp16_value((uint16_t)(blk[0] | (blk[1] << 8)));
+  double dmin = oracle_fp16_value((uint16_t)(blk[2] | (blk[3] << 8)));
+  for (int j = 0; j < QK; ++j) {
+    int s = j / 32;
+    int q = (blk[16 + j / 2] >> (4 * (j % 2))) & 15;
+    w[j] = d * (double)q4k_get6(blk, s) * (double)q - dmin * (double)q4k_get6(blk, Q4SUB + s);
+  }
+}
+
 int64_t oracle_q2k_blocks_per_row(int64_t in_dim) { return (in_dim + QK - 1) / QK; }
 int64_t oracle_q2k_bytes(int64_t rows, int64_t in_dim) {
   return rows * oracle_q2k_blocks_per_row(in_dim) * QBYTES;
 }
 
 typedef struct {
-  const float *w; int64_t r0, r1, in_dim; uint8_t *out; int err;
+  const float *w; int64_t r0, r1, in_dim; uint8_t *out; int err; int q4;
 } qjob;
 
 static void *quant_worker(void *p) {
   qjob *j = (qjob *)p;
   int64_t nb = oracle_q2k_blocks_per_row(j->in_dim);
+  const int64_t bb = j->q4 ? Q4BYTES : QBYTES;
   double buf[QK];
   for (int64_t r = j->r0; r < j->r1; ++r) {
     for (int64_t b = 0; b < nb; ++b) {
@@ -191,22 +310,21 @@ static void *quant_worker(void *p) {
         int64_t c = b * QK + i;
         buf[i] = c < j->in_dim ? (double)j->w[r * j->in_dim + c] : 0.0; /* zero pad */
       }
-      if (q2k_quantize_block(buf, j->out + (r * nb + b) * QBYTES)) j->err = 1;
+      uint8_t *o = j->out + (r * nb + b) * bb;
+      if (j->q4 ? q4k_quantize_block(buf, o) : q2k_quantize_block(buf, o)) j->err = 1;
     }
   }
   return NULL;
 }
 
-/* Quantise a row-major fp32 matrix [rows][in_dim] along its rows.
- * out: rows * ceil(in_dim/256) * 84 bytes.  Returns 0 or -1. */
-int oracle_q2k_quantize(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, int nthreads) {
+static int quantize_rows(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, int nthreads, int q4) {
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;
   if (rows < nthreads) nthreads = rows > 0 ? (int)rows : 1;
   pthread_t th[256];
   qjob jobs[256];
   for (int t = 0; t < nthreads; ++t) {
-    qjob j = {w, rows * t / nthreads, rows * (t + 1) / nthreads, in_dim, out, 0};
+    qjob j = {w, rows * t / nthreads, rows * (t + 1) / nthreads, in_dim, out, 0, q4};
     jobs[t] = j;
   }
   for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, quant_worker, &jobs[t]);
@@ -214,6 +332,35 @@ int oracle_q2k_quantize(const float *w, int64_t rows, int64_t in_dim, uint8_t *o
   int err = jobs[0].err;
   for (int t = 1; t < nthreads; ++t) { pthread_join(th[t], NULL); err |= jobs[t].err; }
   return err ? -1 : 0;
+}
+
+/* Quantise a row-major fp32 matrix [rows][in_dim] along its rows.
+ * out: rows * ceil(in_dim/256) * 84 bytes.  Returns 0 or -1. */
+int oracle_q2k_quantize(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, int nthreads) {
+  return quantize_rows(w, rows, in_dim, out, nthreads, 0);
+}
+
+/* The same with Q4_K blocks: rows * ceil(in_dim/256) * 144 bytes. */
+int oracle_q4k_quantize(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, int nthreads) {
+  return quantize_rows(w, rows, in_dim, out, nthreads, 1);
+}
+
+int64_t oracle_q4k_bytes(int64_t rows, int64_t in_dim) {
+  return rows * oracle_q2k_blocks_per_row(in_dim) * Q4BYTES;
+}
+
+/* Dequantise Q4_K rows [rows][in_dim] (padding dropped) into fp64. */
+void oracle_q4k_dequantize(const uint8_t *q, int64_t rows, int64_t in_dim, double *out) {
+  int64_t nb = oracle_q2k_blocks_per_row(in_dim);
+  double buf[QK];
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < nb; ++b) {
+      q4k_dequantize_block(q + (r * nb + b) * Q4BYTES, buf);
+      for (int i = 0; i < QK; ++i) {
+        int64_t c = b * QK + i;
+        if (c < in_dim) out[r * in_dim + c] = buf[i];
+      }
+    }
 }
 
 /* Dequantise [rows][in_dim] (padding dropped) into fp64. */

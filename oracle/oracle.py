@@ -58,6 +58,12 @@ def lib():
         L.oracle_q2k_quantize.argtypes = [vp, i64, i64, vp, ctypes.c_int]
         L.oracle_q2k_dequantize.restype = None
         L.oracle_q2k_dequantize.argtypes = [vp, i64, i64, vp]
+        L.oracle_q4k_bytes.restype = i64
+        L.oracle_q4k_bytes.argtypes = [i64, i64]
+        L.oracle_q4k_quantize.restype = ctypes.c_int
+        L.oracle_q4k_quantize.argtypes = [vp, i64, i64, vp, ctypes.c_int]
+        L.oracle_q4k_dequantize.restype = None
+        L.oracle_q4k_dequantize.argtypes = [vp, i64, i64, vp]
         L.oracle_router_logits.restype = None
         L.oracle_router_logits.argtypes = [vp, i64, i64, vp, i64, vp, vp]
         L.oracle_select.restype = None
@@ -109,6 +115,27 @@ def dequantize(q: np.ndarray, rows: int, in_dim: int) -> np.ndarray:
     q = _c(q, np.uint8)
     out = np.empty((rows, in_dim), np.float64)
     lib().oracle_q2k_dequantize(_ptr(q), rows, in_dim, _ptr(out))
+    return out
+
+
+def q4k_bytes(rows: int, in_dim: int) -> int:
+    return lib().oracle_q4k_bytes(rows, in_dim)
+
+
+def quantize_q4k(w: np.ndarray) -> np.ndarray:
+    """Q4_K blocks of a [rows][in_dim] fp32 matrix, uint8 [rows][nb*144]."""
+    w = _c(w, np.float32)
+    rows, in_dim = w.shape
+    out = np.zeros(q4k_bytes(rows, in_dim), np.uint8)
+    if lib().oracle_q4k_quantize(_ptr(w), rows, in_dim, _ptr(out), NTHREADS):
+        raise ValueError("Q4_K quantiser: non-finite or out-of-range input")
+    return out.reshape(rows, -1)
+
+
+def dequantize_q4k(q: np.ndarray, rows: int, in_dim: int) -> np.ndarray:
+    q = _c(q, np.uint8)
+    out = np.empty((rows, in_dim), np.float64)
+    lib().oracle_q4k_dequantize(_ptr(q), rows, in_dim, _ptr(out))
     return out
 
 

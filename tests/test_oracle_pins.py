@@ -511,3 +511,163 @@ def test_tiny_config_resampling_leaves_clear_gaps():
     out, ids, w, _ = lo.forward(x)
     assert out.shape == (cfg.T, cfg.D) and np.isfinite(out).all()
     assert np.all(np.diff(ids, axis=1) != 0)
+
+
+# ------------------------------------------------------------------- Q4_K --
+# The 144-byte Q4_K block of "Understanding Dwarf Star" 2.3.2 (the next
+# expert format); readings of the packing as stated in the oracle.
+
+def q4k_handbuilt(d_bits, dm_bits, sc, m, q):
+    """A Q4_K block from its fields, packed here independently of the oracle:
+    fp16 d, fp16 dmin, the sixteen 6-bit fields (sc_0..7, m_0..7) as a 96-bit
+    little-endian integer, codes two per byte with the even value low."""
+    blk = np.zeros(144, np.uint8)
+    blk[0], blk[1] = d_bits & 0xFF, d_bits >> 8
+    blk[2], blk[3] = dm_bits & 0xFF, dm_bits >> 8
+    bits = 0
+    for i, v in enumerate(list(sc) + list(m)):
+        assert 0 <= v < 64
+        bits |= int(v) << (6 * i)
+    blk[4:16] = np.frombuffer(bits.to_bytes(12, "little"), np.uint8)
+    for j in range(256):
+        blk[16 + j // 2] |= int(q[j]) << (4 * (j % 2))
+    return blk
+
+
+def q4k_fields(blk):
+    bits = int.from_bytes(bytes(blk[4:16]), "little")
+    f = [(bits >> (6 * i)) & 63 for i in range(16)]
+    q = [(int(blk[16 + j // 2]) >> (4 * (j % 2))) & 15 for j in range(256)]
+    return f[:8], f[8:], q, int(blk[0]) | (int(blk[1]) << 8), int(blk[2]) | (int(blk[3]) << 8)
+
+
+def test_q4k_block_size_matches_pages():
+    f = facts()["q4k_block"]
+    assert oracle.q4k_bytes(1, 256) == f["bytes_per_block"] == 144
+    assert f["bytes_per_block"] * 8 / f["weights_per_block"] == f["bits_per_weight"] == 4.5
+    assert f["sub_blocks"] * f["weights_per_sub_block"] == 256
+    assert f["scales_offset"] + f["scales_bytes"] == f["codes_offset"]
+    assert f["codes_offset"] + f["codes_bytes"] == f["bytes_per_block"]
+    assert f["scales_bytes"] * 8 == 2 * f["sub_blocks"] * 6      # 8 scales + 8 mins, 6 bits each
+    assert f["codes_bytes"] * 8 == 4 * f["weights_per_block"]     # 4-bit values
+    assert oracle.q4k_bytes(3, 257) == 3 * 2 * 144
+
+
+def test_q4k_dequant_closed_form_handbuilt():
+    # d = 1, dmin = 0.5, sc = 3, m = 2  ->  w = 3q - 1 for q = 0..15
+    q = [j % 16 for j in range(256)]
+    blk = q4k_handbuilt(0x3C00, 0x3800, [3] * 8, [2] * 8, q)
+    w = oracle.dequantize_q4k(blk, 1, 256)[0]
+    assert list(w[:16]) == [3.0 * v - 1.0 for v in range(16)]
+    # 6-bit fields beyond a nibble, per sub-block: sub-block 5 has sc = 40, m = 33
+    sc, m = [3] * 8, [2] * 8
+    sc[5], m[5] = 40, 33
+    blk = q4k_handbuilt(0x3C00, 0x3800, sc, m, q)
+    w = oracle.dequantize_q4k(blk, 1, 256)[0]
+    assert w[32 * 5 + 7] == 40.0 * 7 - 0.5 * 33
+    assert w[32 * 4 + 7] == 3.0 * 7 - 1.0
+    # the packing itself: field 0 in the low bits of byte 4, field 8 (m_0) at bit 48
+    blk = q4k_handbuilt(0x3C00, 0x3C00, [63, 0, 0, 0, 0, 0, 0, 0], [1, 0, 0, 0, 0, 0, 0, 0], [0] * 256)
+    assert blk[4] == 0x3F and blk[5] == 0 and blk[10] == 1 and not blk[11:16].any()
+    # code order: value 1 is the high nibble of byte 16
+    q1 = [0] * 256
+    q1[1] = 7
+    blk = q4k_handbuilt(0x3C00, 0x0000, [1] * 8, [0] * 8, q1)
+    assert blk[16] == 0x70
+    w = oracle.dequantize_q4k(blk, 1, 256)[0]
+    assert w[1] == 7.0 and np.count_nonzero(w) == 1
+
+
+def test_q4k_dequant_matches_fraction_arithmetic_random_blocks():
+    rng = np.random.default_rng(21)
+    for _ in range(20):
+        blk = rng.integers(0, 256, 144).astype(np.uint8)
+        for o in (0, 2):
+            v = int(rng.integers(0, 0x7BFF))
+            blk[o], blk[o + 1] = v & 0xFF, v >> 8
+        w = oracle.dequantize_q4k(blk, 1, 256)[0]
+        sc, m, q, d_bits, dm_bits = q4k_fields(blk)
+        d, dm = _h(d_bits), _h(dm_bits)
+        for j in range(0, 256, 5):
+            s = j // 32
+            assert Fraction(w[j]) == d * sc[s] * q[j] - dm * m[s]
+
+
+@pytest.mark.parametrize("scale", [0.02, 1.0, 300.0, 1e-4])
+def test_q4k_quantizer_invariants_exact(scale):
+    """Minimality of every scale, range coverage, the half-step bound and the
+    round-half-up code, in exact rational arithmetic."""
+    rng = np.random.default_rng(int(scale * 1e4) + 5)
+    x = (rng.normal(size=(5, 256)) * scale).astype(np.float32)
+    x[1, :32] = np.abs(x[1, :32])
+    x[2, 64:96] = -np.abs(x[2, 64:96])
+    x[3, 128:160] = 0.0
+    qb = oracle.quantize_q4k(x)
+    deq = oracle.dequantize_q4k(qb, 5, 256)
+    for r in range(5):
+        sc, m, qq, d_bits, dm_bits = q4k_fields(qb[r])
+        d, dmin = _h(d_bits), _h(dm_bits)
+        X = [Fraction(float(v)) for v in x[r]]
+        lo = [min(Fraction(0), min(X[32 * s:32 * s + 32])) for s in range(8)]
+        hi = [max(X[32 * s:32 * s + 32]) for s in range(8)]
+        assert 63 * dmin >= max(-l for l in lo)
+        if dm_bits > 0:
+            assert 63 * _h(dm_bits - 1) < max(-l for l in lo)
+        b = []
+        for s in range(8):
+            assert m[s] * dmin >= -lo[s]
+            if m[s] > 0:
+                assert (m[s] - 1) * dmin < -lo[s]
+            b.append(m[s] * dmin)
+        assert all(945 * d >= hi[s] + b[s] for s in range(8))
+        if d_bits > 0:
+            assert any(945 * _h(d_bits - 1) < hi[s] + b[s] for s in range(8))
+        for s in range(8):
+            assert 15 * d * sc[s] >= hi[s] + b[s]
+            if sc[s] > 0:
+                assert 15 * d * (sc[s] - 1) < hi[s] + b[s]
+            step = d * sc[s]
+            for j in range(32 * s, 32 * s + 32):
+                assert -b[s] <= X[j] <= -b[s] + 15 * step
+                assert abs(X[j] - Fraction(deq[r, j])) <= step / 2
+                if step > 0:
+                    assert qq[j] == min(15, math.floor((X[j] + b[s]) / step + Fraction(1, 2)))
+
+
+def test_q4k_quantizer_edge_cases():
+    assert not oracle.quantize_q4k(np.zeros((2, 256), np.float32)).any()
+    for bad in (np.nan, np.inf, 65505.0):
+        x = np.zeros((1, 256), np.float32)
+        x[0, 9] = bad
+        with pytest.raises(ValueError):
+            oracle.quantize_q4k(x)
+    rng = np.random.default_rng(3)
+    x = (rng.normal(size=(3, 128)) * 0.02).astype(np.float32)
+    q = oracle.quantize_q4k(x)
+    assert q.shape == (3, 144)
+    for r in range(3):
+        sc, m, _, _, _ = q4k_fields(q[r])
+        assert sc[4:] == [0] * 4 and m[4:] == [0] * 4  # padded sub-blocks
+    assert np.array_equal(oracle.quantize_q4k(np.concatenate([x, np.zeros((3, 128), np.float32)], 1)), q)
+
+
+def test_q4k_quantizer_roundtrip_on_grid_is_byte_exact():
+    """A block whose values lie on its own grid (a sub-block with scale 63,
+    one with min 63, codes 0 and 15 in every sub-block) quantises back to the
+    same bytes."""
+    rng = np.random.default_rng(17)
+    for trial in range(25):
+        d_bits = int(rng.integers(0x2C00, 0x3000))   # d and dmin share an exponent:
+        dm_bits = int(rng.integers(0x2C00, 0x3000))  # the grid values are fp32-exact
+        sc = list(rng.integers(1, 64, 8))
+        m = list(rng.integers(0, 64, 8))
+        sc[int(rng.integers(8))] = 63
+        m[int(rng.integers(8))] = 63
+        q = list(rng.integers(0, 16, 256))
+        for s in range(8):
+            q[32 * s], q[32 * s + 1] = 0, 15
+        blk = q4k_handbuilt(d_bits, dm_bits, sc, m, q)
+        w = oracle.dequantize_q4k(blk, 1, 256)
+        w32 = w.astype(np.float32)
+        assert np.array_equal(w32.astype(np.float64), w)
+        assert np.array_equal(oracle.quantize_q4k(w32)[0], blk), trial
