@@ -413,7 +413,8 @@ def oracle_sample(n_tokens: int = 2, budget_s: float = 12.0):
         t0 = time.perf_counter()
         L = lo.logits(xs[i])
         ids, w = oracle.select(L, cfg.k)
-        oracle.moe_layer(xs[i], exps[i], lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
+        oracle.moe_layer(xs[i], exps[i], lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs,
+                         fmt=cfg.expert_fmt)
         times.append(time.perf_counter() - t0)
         used_threads = max(used_threads, min(oracle.NTHREADS, len(set(ids.ravel())) + 1))
     tot = sum(times)

@@ -21,11 +21,13 @@ LIB_PATH = os.path.join(PKG, "libds_moe.so")
 DS_OK, DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED = 0, -1, -2
 DS_ERR_CUDA, DS_ERR_TIMEOUT, DS_ERR_DEVICE_CHECK = -3, -4, -5
 DS_F32, DS_BF16 = 0, 1
+DS_Q2_K, DS_Q4_K = 0, 1
 
 SYMBOLS = ["ds_moe_q2k_bytes", "ds_moe_expert_bytes", "ds_moe_quantize_q2k",
            "ds_moe_dequantize_q2k", "ds_moe_workspace_bytes", "ds_moe_layer",
            "ds_moe_layer_hostio", "ds_moe_stack", "ds_moe_sync_status", "ds_moe_version",
-           "ds_moe_layer_noalloc", "ds_moe_layer_path"]
+           "ds_moe_layer_noalloc", "ds_moe_layer_path", "ds_moe_q4k_bytes",
+           "ds_moe_expert_bytes_fmt", "ds_moe_quantize_q4k", "ds_moe_dequantize_q4k"]
 
 # ds_moe_layer_path results
 PATH_NONE, PATH_STREAM, PATH_DECODE3, PATH_GROUPED_GEMV, PATH_TENSOR_CORE = 0, 1, 2, 3, 4
@@ -42,13 +44,14 @@ class Shape(ctypes.Structure):
                 ("n_ff", ctypes.c_int32), ("n_ff_shared", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("x_dtype", ctypes.c_int32),
                 ("router_dtype", ctypes.c_int32), ("routed_scale", ctypes.c_float),
-                ("logit_scale", ctypes.c_float), ("bias_select_only", ctypes.c_int32)]
+                ("logit_scale", ctypes.c_float), ("bias_select_only", ctypes.c_int32),
+                ("expert_format", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
     _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("shared_gate", ctypes.c_void_p), ("shared_up", ctypes.c_void_p),
-                ("shared_down", ctypes.c_void_p), ("experts_q2k", ctypes.c_void_p)]
+                ("shared_down", ctypes.c_void_p), ("experts", ctypes.c_void_p)]
 
 
 class Debug(ctypes.Structure):
@@ -71,9 +74,14 @@ def lib():
         vp, i64, sz, cp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_char_p
         L.ds_moe_q2k_bytes.restype = sz
         L.ds_moe_q2k_bytes.argtypes = [i64, i64]
+        L.ds_moe_q4k_bytes.restype = sz
+        L.ds_moe_q4k_bytes.argtypes = [i64, i64]
         L.ds_moe_expert_bytes.restype = sz
         L.ds_moe_expert_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
-        for f in (L.ds_moe_quantize_q2k, L.ds_moe_dequantize_q2k):
+        L.ds_moe_expert_bytes_fmt.restype = sz
+        L.ds_moe_expert_bytes_fmt.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+        for f in (L.ds_moe_quantize_q2k, L.ds_moe_dequantize_q2k, L.ds_moe_quantize_q4k,
+                  L.ds_moe_dequantize_q4k):
             f.restype = ctypes.c_int
             f.argtypes = [vp, i64, i64, vp, vp, cp, sz]
         L.ds_moe_workspace_bytes.restype = ctypes.c_int
@@ -128,18 +136,19 @@ class MoEShape:
     routed_scale: float = 1.0
     logit_scale: float = 1.0
     bias_select_only: int = 0
+    expert_format: int = 0  # DS_Q2_K or DS_Q4_K
 
     def c(self) -> Shape:
         return Shape(self.n_embd, self.n_expert, self.n_ff, self.n_ff_shared, self.top_k,
                      self.x_dtype, self.router_dtype, self.routed_scale, self.logit_scale,
-                     self.bias_select_only)
+                     self.bias_select_only, self.expert_format)
 
 
 @dataclass
 class MoEWeights:
     """Device tensors of one layer (see include/ds_moe.h for layouts)."""
     router_w: object
-    experts_q2k: object
+    experts: object
     router_bias: object = None
     shared_gate: object = None
     shared_up: object = None
@@ -147,7 +156,7 @@ class MoEWeights:
 
     def c(self) -> Weights:
         return Weights(_ptr(self.router_w), _ptr(self.router_bias), _ptr(self.shared_gate),
-                       _ptr(self.shared_up), _ptr(self.shared_down), _ptr(self.experts_q2k))
+                       _ptr(self.shared_up), _ptr(self.shared_down), _ptr(self.experts))
 
 
 def version() -> str:
@@ -158,8 +167,12 @@ def q2k_bytes(rows: int, in_dim: int) -> int:
     return lib().ds_moe_q2k_bytes(rows, in_dim)
 
 
-def expert_bytes(n_embd: int, n_ff: int) -> int:
-    return lib().ds_moe_expert_bytes(n_embd, n_ff)
+def q4k_bytes(rows: int, in_dim: int) -> int:
+    return lib().ds_moe_q4k_bytes(rows, in_dim)
+
+
+def expert_bytes(n_embd: int, n_ff: int, expert_format: int = 0) -> int:
+    return lib().ds_moe_expert_bytes_fmt(expert_format, n_embd, n_ff)
 
 
 def quantize_q2k(w, out, stream=None):
@@ -170,6 +183,16 @@ def quantize_q2k(w, out, stream=None):
 
 def dequantize_q2k(q, rows, in_dim, out, stream=None):
     _call(lib().ds_moe_dequantize_q2k, q.data_ptr(), rows, in_dim, out.data_ptr(), _stream(stream))
+
+
+def quantize_q4k(w, out, stream=None):
+    """w: fp32 device tensor [rows][in_dim]; out: uint8 device tensor of q4k_bytes."""
+    rows, in_dim = w.shape
+    _call(lib().ds_moe_quantize_q4k, w.data_ptr(), rows, in_dim, out.data_ptr(), _stream(stream))
+
+
+def dequantize_q4k(q, rows, in_dim, out, stream=None):
+    _call(lib().ds_moe_dequantize_q4k, q.data_ptr(), rows, in_dim, out.data_ptr(), _stream(stream))
 
 
 def layer_path(shape: MoEShape, T: int, x=None) -> int:

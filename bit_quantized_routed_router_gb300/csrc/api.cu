@@ -72,9 +72,12 @@ int check_shape(const ds_moe_shape *s, char *err, size_t errlen, Shape *out) {
     return fail(err, errlen, DS_ERR_INVALID_ARG, "logit_scale must be finite and >= 0");
   if (s->bias_select_only != 0 && s->bias_select_only != 1)
     return fail(err, errlen, DS_ERR_INVALID_ARG, "bias_select_only must be 0 or 1");
+  if (s->expert_format != DS_Q2_K && s->expert_format != DS_Q4_K)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "expert_format must be DS_Q2_K or DS_Q4_K");
   *out = Shape{s->n_embd, s->n_expert, s->n_ff, s->n_ff_shared, s->top_k,
                s->x_dtype, s->router_dtype, s->routed_scale,
-               s->logit_scale == 0.f ? 1.f : s->logit_scale, s->bias_select_only};
+               s->logit_scale == 0.f ? 1.f : s->logit_scale, s->bias_select_only,
+               s->expert_format};
   return DS_OK;
 }
 
@@ -120,10 +123,10 @@ size_t layout(const Shape &sh, int64_t T, char *base, Work *wk) {
 
 int check_weights(const Shape &sh, const ds_moe_weights *W, char *err, size_t errlen) {
   if (!W) return fail(err, errlen, DS_ERR_INVALID_ARG, "weights is NULL");
-  if (!W->router_w || !W->experts_q2k)
-    return fail(err, errlen, DS_ERR_INVALID_ARG, "router_w and experts_q2k are required");
-  if (!aligned(W->router_w, 16) || !aligned(W->experts_q2k, 16))
-    return fail(err, errlen, DS_ERR_INVALID_ARG, "router_w / experts_q2k must be 16-byte aligned");
+  if (!W->router_w || !W->experts)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "router_w and experts are required");
+  if (!aligned(W->router_w, 16) || !aligned(W->experts, 16))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "router_w / experts must be 16-byte aligned");
   if (W->router_bias && !aligned(W->router_bias, 4))
     return fail(err, errlen, DS_ERR_INVALID_ARG, "router_bias must be 4-byte aligned");
   if (sh.Fs > 0) {
@@ -196,31 +199,62 @@ size_t ds_moe_q2k_bytes(int64_t rows, int64_t in_dim) {
   return (size_t)rows * (size_t)((in_dim + QK - 1) / QK) * QB;
 }
 
-size_t ds_moe_expert_bytes(int32_t n_embd, int32_t n_ff) {
-  if (n_embd <= 0 || n_ff <= 0) return 0;
-  return 2 * ds_moe_q2k_bytes(n_ff, n_embd) + ds_moe_q2k_bytes(n_embd, n_ff);
+size_t ds_moe_q4k_bytes(int64_t rows, int64_t in_dim) {
+  if (rows < 0 || in_dim < 0) return 0;
+  return (size_t)rows * (size_t)((in_dim + QK - 1) / QK) * Q4B;
 }
 
-int ds_moe_quantize_q2k(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, void *stream,
-                        char *err, size_t errlen) {
+size_t ds_moe_expert_bytes(int32_t n_embd, int32_t n_ff) {
+  return ds_moe_expert_bytes_fmt(DS_Q2_K, n_embd, n_ff);
+}
+
+size_t ds_moe_expert_bytes_fmt(int32_t expert_format, int32_t n_embd, int32_t n_ff) {
+  if (n_embd <= 0 || n_ff <= 0) return 0;
+  if (expert_format == DS_Q2_K) return 2 * ds_moe_q2k_bytes(n_ff, n_embd) + ds_moe_q2k_bytes(n_embd, n_ff);
+  if (expert_format == DS_Q4_K) return 2 * ds_moe_q4k_bytes(n_ff, n_embd) + ds_moe_q4k_bytes(n_embd, n_ff);
+  return 0;
+}
+
+static int quantize_fmt(int fmt, const float *w, int64_t rows, int64_t in_dim, uint8_t *out,
+                        void *stream, char *err, size_t errlen) {
   if (rows < 0 || in_dim < 0) return fail(err, errlen, DS_ERR_INVALID_ARG, "negative size");
   if (rows == 0 || in_dim == 0) return DS_OK;
   if (!w || !out) return fail(err, errlen, DS_ERR_INVALID_ARG, "NULL pointer");
   if (!aligned(w, 4) || !aligned(out, 4))
     return fail(err, errlen, DS_ERR_INVALID_ARG, "w and out must be 4-byte aligned");
   if (!status_word()) return fail(err, errlen, DS_ERR_CUDA, "no CUDA device");
-  cudaError_t e = launch_quantize(w, rows, in_dim, out, (cudaStream_t)stream);
+  cudaError_t e = launch_quantize(fmt, w, rows, in_dim, out, (cudaStream_t)stream);
   return e == cudaSuccess ? DS_OK : cuda_fail(err, errlen, e, "quantize");
 }
 
-int ds_moe_dequantize_q2k(const uint8_t *q, int64_t rows, int64_t in_dim, float *out, void *stream,
-                          char *err, size_t errlen) {
+static int dequantize_fmt(int fmt, const uint8_t *q, int64_t rows, int64_t in_dim, float *out,
+                          void *stream, char *err, size_t errlen) {
   if (rows < 0 || in_dim < 0) return fail(err, errlen, DS_ERR_INVALID_ARG, "negative size");
   if (rows == 0 || in_dim == 0) return DS_OK;
   if (!q || !out) return fail(err, errlen, DS_ERR_INVALID_ARG, "NULL pointer");
   if (!aligned(out, 4)) return fail(err, errlen, DS_ERR_INVALID_ARG, "out must be 4-byte aligned");
-  cudaError_t e = launch_dequantize(q, rows, in_dim, out, (cudaStream_t)stream);
+  cudaError_t e = launch_dequantize(fmt, q, rows, in_dim, out, (cudaStream_t)stream);
   return e == cudaSuccess ? DS_OK : cuda_fail(err, errlen, e, "dequantize");
+}
+
+int ds_moe_quantize_q2k(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, void *stream,
+                        char *err, size_t errlen) {
+  return quantize_fmt(DS_Q2_K, w, rows, in_dim, out, stream, err, errlen);
+}
+
+int ds_moe_dequantize_q2k(const uint8_t *q, int64_t rows, int64_t in_dim, float *out, void *stream,
+                          char *err, size_t errlen) {
+  return dequantize_fmt(DS_Q2_K, q, rows, in_dim, out, stream, err, errlen);
+}
+
+int ds_moe_quantize_q4k(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, void *stream,
+                        char *err, size_t errlen) {
+  return quantize_fmt(DS_Q4_K, w, rows, in_dim, out, stream, err, errlen);
+}
+
+int ds_moe_dequantize_q4k(const uint8_t *q, int64_t rows, int64_t in_dim, float *out, void *stream,
+                          char *err, size_t errlen) {
+  return dequantize_fmt(DS_Q4_K, q, rows, in_dim, out, stream, err, errlen);
 }
 
 int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, char *err,

@@ -11,6 +11,7 @@ namespace dsm {
 
 constexpr int QK = 256;      // weights per Q2_K super-block
 constexpr int QB = 84;       // bytes per Q2_K super-block
+constexpr int Q4B = 144;     // bytes per Q4_K super-block
 constexpr int NUM_SMS = 152; // GB300
 
 // Sticky status bits (per device, read by ds_moe_sync_status).
@@ -62,10 +63,12 @@ struct Shape {
   float routed_scale;
   float logit_scale;  // 1: plain softmax over the selected logits
   int bias_select_only;  // 1: the router bias steers the selection only
+  int fmt;               // ds_expert_format of the routed experts
+  int block_bytes() const { return fmt == DS_Q4_K ? Q4B : QB; }
   int64_t nb_D() const { return (D + QK - 1) / QK; }
   int64_t nb_F() const { return (F + QK - 1) / QK; }
-  int64_t gate_bytes() const { return (int64_t)F * nb_D() * QB; }
-  int64_t down_bytes() const { return (int64_t)D * nb_F() * QB; }
+  int64_t gate_bytes() const { return (int64_t)F * nb_D() * block_bytes(); }
+  int64_t down_bytes() const { return (int64_t)D * nb_F() * block_bytes(); }
   int64_t expert_bytes() const { return 2 * gate_bytes() + down_bytes(); }
 };
 

@@ -87,6 +87,59 @@ __device__ __forceinline__ void q2k_row_dot(const uint8_t *__restrict__ row, int
   }
 }
 
+// Partial dot products of one Q4_K row ("Understanding Dwarf Star", 2.3.2:
+// 8 sub-blocks of 32 weights, 6-bit scales and mins, 4-bit codes); this
+// lane's sub-blocks sb = lane + 32 i.  Weights formed exactly as above.
+template <int NTOK>
+__device__ __forceinline__ void q4k_row_dot(const uint8_t *__restrict__ row, int in_dim,
+                                            const float4 *__restrict__ xs, int stride4, int nt,
+                                            float acc[NTOK]) {
+  const int lane = threadIdx.x & 31;
+  const int nsb = in_dim >> 5;
+  for (int sb = lane; sb < nsb; sb += 32) {
+    const uint8_t *blk = row + (sb >> 3) * Q4B;
+    const int s = sb & 7;
+    const uint4 codes = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * s);
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);  // d, dmin, 12 field bytes
+    // the 96-bit field integer = hdr.y | hdr.z << 32 | hdr.w << 64
+    const uint64_t f_lo = (uint64_t)hdr.y | ((uint64_t)hdr.z << 32);
+    const int sc = (int)((f_lo >> (6 * s)) & 63u);
+    const int pm = 48 + 6 * s;  // min field 8 + s
+    const int mm = pm + 6 <= 64 ? (int)((f_lo >> pm) & 63u)
+                   : pm >= 64   ? (int)((hdr.w >> (pm - 64)) & 63u)
+                                : (int)(((f_lo >> pm) | ((uint64_t)hdr.w << (64 - pm))) & 63u);
+    const float dsc = fp16_to_f32((uint16_t)(hdr.x & 0xFFFF)) * (float)sc;
+    const float dmm = fp16_to_f32((uint16_t)(hdr.x >> 16)) * (float)mm;
+    const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      float w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = __fmaf_rn(dsc, (float)((cw[jj >> 1] >> (4 * (4 * (jj & 1) + i))) & 15u), -dmm);
+      const int slot = swz(8 * sb + jj);
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) {
+        if (t < nt) {
+          const float4 xv = xs[t * stride4 + slot];
+          acc[t] = fmaf(w[0], xv.x, acc[t]);
+          acc[t] = fmaf(w[1], xv.y, acc[t]);
+          acc[t] = fmaf(w[2], xv.z, acc[t]);
+          acc[t] = fmaf(w[3], xv.w, acc[t]);
+        }
+      }
+    }
+  }
+}
+
+template <int FMT, int NTOK>
+__device__ __forceinline__ void q_row_dot(const uint8_t *__restrict__ row, int in_dim,
+                                          const float4 *__restrict__ xs, int stride4, int nt,
+                                          float acc[NTOK]) {
+  if (FMT == DS_Q4_K) q4k_row_dot<NTOK>(row, in_dim, xs, stride4, nt, acc);
+  else q2k_row_dot<NTOK>(row, in_dim, xs, stride4, nt, acc);
+}
+
 // Same for a bf16 row (the shared expert); lane covers elements 8*lane + 256 i.
 template <int NTOK>
 __device__ __forceinline__ void bf16_row_dot(const uint16_t *__restrict__ row, int in_dim,
@@ -119,7 +172,7 @@ __device__ __forceinline__ void bf16_row_dot(const uint16_t *__restrict__ row, i
 // grid.x: blocks of RPB output rows; grid.y: expert slot (used[slot]), the
 // last y being the shared expert when Fs > 0.  Each block walks its slot's
 // tokens in groups of NT, staging their inputs in shared memory as fp32.
-template <int MODE, typename TX>
+template <int MODE, typename TX, int FMT>
 __global__ void __launch_bounds__(256) grouped_gemv_kernel(GemvArgs a) {
   extern __shared__ float4 xs[];
   const int slot = blockIdx.y;
@@ -140,7 +193,7 @@ __global__ void __launch_bounds__(256) grouped_gemv_kernel(GemvArgs a) {
   const int stride4 = in_dim >> 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint8_t *blob = a.experts + (int64_t)e * a.expert_bytes;
-  const int64_t row_bytes = (int64_t)((in_dim + QK - 1) / QK) * QB;
+  const int64_t row_bytes = (int64_t)((in_dim + QK - 1) / QK) * (FMT == DS_Q4_K ? Q4B : QB);
 
   for (int g0 = 0; g0 < n_tok; g0 += NT) {
     const int nt = min(NT, n_tok - g0);
@@ -166,8 +219,8 @@ __global__ void __launch_bounds__(256) grouped_gemv_kernel(GemvArgs a) {
           bf16_row_dot<NT>(a.sh_a + (int64_t)r * a.D, in_dim, xs, stride4, nt, g);
           bf16_row_dot<NT>(a.sh_b + (int64_t)r * a.D, in_dim, xs, stride4, nt, u);
         } else {
-          q2k_row_dot<NT>(blob + a.off_a + r * row_bytes, in_dim, xs, stride4, nt, g);
-          q2k_row_dot<NT>(blob + a.off_b + r * row_bytes, in_dim, xs, stride4, nt, u);
+          q_row_dot<FMT, NT>(blob + a.off_a + r * row_bytes, in_dim, xs, stride4, nt, g);
+          q_row_dot<FMT, NT>(blob + a.off_b + r * row_bytes, in_dim, xs, stride4, nt, u);
         }
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -181,7 +234,7 @@ __global__ void __launch_bounds__(256) grouped_gemv_kernel(GemvArgs a) {
       } else {
         float y[NT] = {};
         if (shared) bf16_row_dot<NT>(a.sh_a + (int64_t)r * a.Fs, in_dim, xs, stride4, nt, y);
-        else q2k_row_dot<NT>(blob + a.off_a + r * row_bytes, in_dim, xs, stride4, nt, y);
+        else q_row_dot<FMT, NT>(blob + a.off_a + r * row_bytes, in_dim, xs, stride4, nt, y);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const float ys = warp_sum(y[t]);
@@ -242,21 +295,26 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float *__restri
     out[(int64_t)blockIdx.x * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(xr[d] * inv));
 }
 
-template <int MODE, typename TX>
-cudaError_t launch_gemv(const GemvArgs &a, int out_rows_max, int in_dim_max, cudaStream_t s) {
+template <int MODE, typename TX, int FMT>
+cudaError_t launch_gemv1(const GemvArgs &a, int out_rows_max, int in_dim_max, cudaStream_t s) {
   const size_t smem = (size_t)NT * in_dim_max * sizeof(float);
-  static bool attr_set[2][2] = {};
-  auto kern = grouped_gemv_kernel<MODE, TX>;
-  const int ti = sizeof(TX) == 2;
-  if (!attr_set[MODE][ti]) {
+  static bool attr_set = false;
+  auto kern = grouped_gemv_kernel<MODE, TX, FMT>;
+  if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
     if (e != cudaSuccess) return e;
-    attr_set[MODE][ti] = true;
+    attr_set = true;
   }
   dim3 g((out_rows_max + RPB - 1) / RPB, a.n_slots + (a.Fs > 0 ? 1 : 0));
   kern<<<g, 256, smem, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int MODE, typename TX>
+cudaError_t launch_gemv(int fmt, const GemvArgs &a, int out_rows_max, int in_dim_max, cudaStream_t s) {
+  return fmt == DS_Q4_K ? launch_gemv1<MODE, TX, DS_Q4_K>(a, out_rows_max, in_dim_max, s)
+                        : launch_gemv1<MODE, TX, DS_Q2_K>(a, out_rows_max, in_dim_max, s);
 }
 
 }  // namespace
@@ -264,7 +322,7 @@ cudaError_t launch_gemv(const GemvArgs &a, int out_rows_max, int in_dim_max, cud
 cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const void *x,
                               const Work &wk, cudaStream_t s) {
   GemvArgs a{};
-  a.experts = W.experts_q2k;
+  a.experts = W.experts;
   a.expert_bytes = sh.expert_bytes();
   a.offsets = wk.offsets;
   a.perm = wk.perm;
@@ -282,8 +340,8 @@ cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const vo
   a.out_shared = wk.hs;
   cudaError_t err;
   const int rows1 = std::max(sh.F, sh.Fs);
-  if (sh.x_dtype == DS_BF16) err = launch_gemv<MODE_GATEUP, uint16_t>(a, rows1, sh.D, s);
-  else err = launch_gemv<MODE_GATEUP, float>(a, rows1, sh.D, s);
+  if (sh.x_dtype == DS_BF16) err = launch_gemv<MODE_GATEUP, uint16_t>(sh.fmt, a, rows1, sh.D, s);
+  else err = launch_gemv<MODE_GATEUP, float>(sh.fmt, a, rows1, sh.D, s);
   if (err != cudaSuccess) return err;
   // down
   a.off_a = 2 * sh.gate_bytes();
@@ -294,7 +352,7 @@ cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const vo
   a.in_shared = wk.hs;
   a.out = wk.y;
   a.out_shared = wk.ys;
-  return launch_gemv<MODE_DOWN, float>(a, sh.D, std::max(sh.F, sh.Fs), s);
+  return launch_gemv<MODE_DOWN, float>(sh.fmt, a, sh.D, std::max(sh.F, sh.Fs), s);
 }
 
 cudaError_t launch_combine(const Shape &sh, const Work &wk, float *out, bool accumulate,

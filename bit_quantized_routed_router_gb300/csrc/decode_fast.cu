@@ -1432,6 +1432,7 @@ static bool fast_shape_ok(int nb_d, int nb_f) {
 }
 
 bool fused_decode_supported(const Shape &sh, int64_t T) {
+  if (sh.fmt != DS_Q2_K) return false;  // the kernels read Q2_K blocks
   if (T < 1 || T > 4 || (int64_t)T * sh.k > PMAXD) return false;
   if (sh.D % QK || sh.F % QK || !fast_shape_ok(sh.D / QK, sh.F / QK)) return false;
   if (sh.x_dtype != sh.router_dtype || sh.E > 1024) return false;
@@ -1466,7 +1467,7 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
   a.router_f32 = sh.router_dtype == DS_F32;
   a.bias = W.router_bias;
   a.sg = W.shared_gate; a.su = W.shared_up; a.sd = W.shared_down;
-  a.experts = W.experts_q2k;
+  a.experts = W.experts;
   a.expert_bytes = sh.expert_bytes();
   a.gate_bytes = sh.gate_bytes();
   a.x = x;

@@ -31,9 +31,10 @@ struct Work {
   int64_t n_chunks;
 };
 
-cudaError_t launch_quantize(const float *w, int64_t rows, int64_t in_dim, uint8_t *out,
+// fmt: DS_Q2_K or DS_Q4_K.
+cudaError_t launch_quantize(int fmt, const float *w, int64_t rows, int64_t in_dim, uint8_t *out,
                             cudaStream_t s);
-cudaError_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t in_dim, float *out,
+cudaError_t launch_dequantize(int fmt, const uint8_t *q, int64_t rows, int64_t in_dim, float *out,
                               cudaStream_t s);
 
 // Router logits, top-k selection and the expert route (histogram, scan,

@@ -806,6 +806,7 @@ cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const voi
 }
 
 bool prefill_tc_supported(const Shape &sh, int64_t T) {
+  if (sh.fmt != DS_Q2_K) return false;  // the dequantising warps read Q2_K blocks
   if (T < TC_MIN_T || T > (int64_t)1 << 24) return false;
   if (sh.x_dtype != DS_BF16 || sh.router_dtype != DS_BF16) return false;
   if (sh.D % 1024 || sh.F % 1024 || sh.Fs % TC_BM) return false;  // whole 4-block groups: raw copies stay inside rows
@@ -876,7 +877,7 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
 
   TcArgs a{};
   a.D = sh.D; a.F = sh.F; a.Fs = sh.Fs; a.P = (int)P; a.T = (int)T;
-  a.experts = W.experts_q2k;
+  a.experts = W.experts;
   a.expert_bytes = sh.expert_bytes();
   a.gate_bytes = sh.gate_bytes();
   a.h16 = h16;
@@ -887,14 +888,14 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
   CUtensorMap m_xp, m_x, m_sg, m_su, m_h, m_sd;
   const int fs1 = std::max(sh.Fs, TC_BM);
   if (!make_map(&m_xp, xp, P, sh.D, TC_NGU, false) || !make_map(&m_x, x, T, sh.D, TC_NGU, true) ||
-      !make_map(&m_sg, sh.Fs > 0 ? (const void *)W.shared_gate : (const void *)W.experts_q2k, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
-      !make_map(&m_su, sh.Fs > 0 ? (const void *)W.shared_up : (const void *)W.experts_q2k, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
+      !make_map(&m_sg, sh.Fs > 0 ? (const void *)W.shared_gate : (const void *)W.experts, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
+      !make_map(&m_su, sh.Fs > 0 ? (const void *)W.shared_up : (const void *)W.experts, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
       !make_map(&m_h, h16, P, sh.F, TC_NDN, false) ||
       !make_map(&m_sd, sd16, sh.D, fs1, TC_BM, false))
     return cudaErrorInvalidValue;
   CUtensorMap m_rgu, m_rdn;
-  if (!make_raw_map(&m_rgu, W.experts_q2k, (int64_t)(sh.D / QK) * QB, 2 * (int64_t)sh.F, sh.E, sh.expert_bytes()) ||
-      !make_raw_map(&m_rdn, W.experts_q2k + 2 * sh.gate_bytes(), (int64_t)(sh.F / QK) * QB, sh.D, sh.E,
+  if (!make_raw_map(&m_rgu, W.experts, (int64_t)(sh.D / QK) * QB, 2 * (int64_t)sh.F, sh.E, sh.expert_bytes()) ||
+      !make_raw_map(&m_rdn, W.experts + 2 * sh.gate_bytes(), (int64_t)(sh.F / QK) * QB, sh.D, sh.E,
                     sh.expert_bytes()))
     return cudaErrorInvalidValue;
   a.tiles = tiles_gu;

@@ -27,6 +27,7 @@ T_SHARED_GATE, T_SHARED_UP, T_SHARED_DOWN = 4, 5, 6
 T_EXPERT_GATE, T_EXPERT_UP, T_EXPERT_DOWN = 7, 8, 9
 
 QK, QBYTES = 256, 84
+BLOCK_BYTES = {"q2k": 84, "q4k": 144}  # bytes per 256-weight block of each expert format
 
 
 @dataclass(frozen=True)
@@ -48,13 +49,18 @@ class Config:
     zipf_s: float           # 0 = no popularity bias
     seed: int
     layers: int = 1
+    expert_fmt: str = "q2k"  # "q2k" | "q4k"
 
     def rows_blocks(self, in_dim: int) -> int:
         return (in_dim + QK - 1) // QK
 
     @property
+    def block_bytes(self) -> int:
+        return BLOCK_BYTES[self.expert_fmt]
+
+    @property
     def expert_bytes(self) -> int:
-        return QBYTES * (2 * self.F * self.rows_blocks(self.D) + self.D * self.rows_blocks(self.F))
+        return self.block_bytes * (2 * self.F * self.rows_blocks(self.D) + self.D * self.rows_blocks(self.F))
 
 
 TINY = Config("tiny T=8 D=256 E=16 k=2 F=128", 8, 256, 16, 2, 128, 0, "f32", "f32", "normal",

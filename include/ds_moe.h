@@ -1,5 +1,5 @@
-/* ds_moe: one routed mixture-of-experts layer with 2-bit (Q2_K) routed
- * experts, computed on one GB300 (sm_103a) GPU.
+/* ds_moe: one routed mixture-of-experts layer with 2-bit (Q2_K) or 4-bit
+ * (Q4_K) routed experts, computed on one GB300 (sm_103a) GPU.
  *
  * The layer ("Understanding Dwarf Star", 5.3.2 "The MoE Architecture" and
  * 5.3.7 "The MoE Kernel in Metal"):
@@ -9,7 +9,7 @@
  *     out     = y_shared(x) + sum_j w_j y_{ids_j}(x)        combine, fp32
  * with the routed expert matrices stored as Q2_K super-blocks ("Understanding
  * Dwarf Star", 3.3.3 "Q2_K: 2.625 Bits Per Element"): 84 bytes per 256
- * weights along each matrix's input dimension.  Shapes of the DeepSeek V4
+ * weights along each matrix's input dimension (or Q4_K, below).  Shapes of the DeepSeek V4
  * Flash layer: n_embd 4096, 256 experts, top-6, one shared expert, expert
  * width 2048 ("Understanding Dwarf Star", 2.4.3 shape table).
  *
@@ -36,10 +36,19 @@
  *   bytes [16,80)  2-bit codes; weight j at byte 16 + j/4, bits 2*(j%4)
  *   bytes [80,82)  d, fp16 little-endian;  bytes [82,84) dmin, fp16
  *   weight j = d*sc_s*q_j - dmin*m_s  (s = j/16)
+ * Q4_K super-block (144 bytes, 256 weights; "Understanding Dwarf Star",
+ * 2.3.2 "K-Quant Formats": d at 0, dmin at 2, 12 bytes of 6-bit scales and
+ * mins at 4, 128 bytes of 4-bit codes at 16, 8 sub-blocks of 32):
+ *   bytes [0,2) d, [2,4) dmin, fp16 little-endian
+ *   bytes [4,16)   one 96-bit little-endian integer: field i in bits
+ *                  [6i, 6i+6); fields 0..7 = sc_s, 8..15 = m_s
+ *   bytes [16,144) 4-bit codes; weight j at byte 16 + j/2, low nibble for
+ *                  even j
+ *   weight j = d*sc_s*q_j - dmin*m_s  (s = j/32)
  * A row of in_dim weights uses ceil(in_dim/256) blocks (zero-padded).
  * Packed expert e = gate [n_ff rows][n_embd] | up [n_ff][n_embd] |
  * down [n_embd rows][n_ff], each row-major in blocks; experts are contiguous
- * in expert order, each ds_moe_expert_bytes() long; base 16-byte aligned.
+ * in expert order, each ds_moe_expert_bytes_fmt() long; base 16-byte aligned.
  */
 #ifndef DS_MOE_H
 #define DS_MOE_H
@@ -62,6 +71,9 @@ typedef enum {
 
 typedef enum { DS_F32 = 0, DS_BF16 = 1 } ds_dtype;
 
+/* Storage format of the routed experts. */
+typedef enum { DS_Q2_K = 0, DS_Q4_K = 1 } ds_expert_format;
+
 typedef struct {
   int32_t n_embd;       /* D: model width, multiple of 256, <= 8192          */
   int32_t n_expert;     /* E: routed experts, 1..1024                        */
@@ -78,6 +90,7 @@ typedef struct {
   int32_t bias_select_only; /* 0: router_bias is part of the logits (selection
                            and weights); 1: it steers the selection only and
                            the weights use the logits without it            */
+  int32_t expert_format; /* ds_expert_format of the routed experts (0 = Q2_K) */
 } ds_moe_shape;
 
 typedef struct {
@@ -86,7 +99,7 @@ typedef struct {
   const uint16_t *shared_gate; /* [Fs][D] bf16 bits (NULL when Fs == 0)        */
   const uint16_t *shared_up;   /* [Fs][D] bf16 bits                             */
   const uint16_t *shared_down; /* [D][Fs] bf16 bits                             */
-  const uint8_t *experts_q2k; /* [E] packed experts, 16-byte aligned           */
+  const uint8_t *experts;    /* [E] packed experts in expert_format, 16-byte aligned */
 } ds_moe_weights;
 
 /* Optional debug outputs of ds_moe_layer (device pointers; NULL fields and a
@@ -105,10 +118,17 @@ typedef struct {
  * Returns 0 for negative sizes. */
 size_t ds_moe_q2k_bytes(int64_t rows, int64_t in_dim);
 
+/* Bytes of a Q4_K matrix: rows * ceil(in_dim/256) * 144 ("Understanding
+ * Dwarf Star", 2.3.2).  Returns 0 for negative sizes. */
+size_t ds_moe_q4k_bytes(int64_t rows, int64_t in_dim);
+
 /* Bytes of one packed routed expert (gate, up and down; "The sparsity that
  * pays for everything else in DwarfStar", "Where the parameters actually
- * are": gate, up and down per expert). */
+ * are": gate, up and down per expert), Q2_K. */
 size_t ds_moe_expert_bytes(int32_t n_embd, int32_t n_ff);
+
+/* The same in a given ds_expert_format; 0 for an unknown format. */
+size_t ds_moe_expert_bytes_fmt(int32_t expert_format, int32_t n_embd, int32_t n_ff);
 
 /* Quantise an fp32 matrix w [rows][in_dim] (row-major, device) to Q2_K
  * blocks in out (ds_moe_q2k_bytes(rows, in_dim) bytes, device, 4-byte
@@ -128,6 +148,21 @@ int ds_moe_quantize_q2k(const float *w, int64_t rows, int64_t in_dim, uint8_t *o
  * rounded once ("Understanding Dwarf Star", 2.8.1: weights are rebuilt from
  * the stored scales and mins).  A test and inspection aid. */
 int ds_moe_dequantize_q2k(const uint8_t *q, int64_t rows, int64_t in_dim, float *out, void *stream,
+                          char *err, size_t errlen);
+
+/* Quantise to Q4_K blocks (ds_moe_q4k_bytes(rows, in_dim) bytes, device,
+ * 4-byte aligned).  The same search as for Q2_K with 4-bit codes and 6-bit
+ * scales and mins, per 32-weight sub-block: the smallest fp16 dmin with
+ * 63*dmin >= max(-min), the smallest m_s <= 63 covering each sub-block's
+ * minimum, the smallest fp16 d with 945*d >= max(hi_s + b_s), the smallest
+ * sc_s <= 63 with 15*d*sc_s >= hi_s + b_s, then the nearest of the 16 levels,
+ * ties upward ("Understanding Dwarf Star", 2.3.2 layout; 2.3.5 evenly spaced
+ * levels).  Exact, like the Q2_K quantiser; the same input checks. */
+int ds_moe_quantize_q4k(const float *w, int64_t rows, int64_t in_dim, uint8_t *out, void *stream,
+                        char *err, size_t errlen);
+
+/* Dequantise Q4_K blocks to fp32: fp32(d*sc*q - dmin*m), rounded once. */
+int ds_moe_dequantize_q4k(const uint8_t *q, int64_t rows, int64_t in_dim, float *out, void *stream,
                           char *err, size_t errlen);
 
 /* Workspace bytes ds_moe_layer needs for T tokens of this shape (host call,
@@ -151,7 +186,8 @@ int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, 
  * (dequantised weights and activations rounded once to fp16; an |x| or
  * intermediate above 65504 is saturated and reported by ds_moe_sync_status
  * as DS_ERR_DEVICE_CHECK); every other case uses the grouped dequantising
- * GEMV path with fp32 arithmetic. */
+ * GEMV path with fp32 arithmetic.  Q4_K experts use the grouped GEMV path
+ * at every T. */
 int ds_moe_layer(const ds_moe_shape *shape, const ds_moe_weights *weights, const void *x, int64_t T,
                  float *out, void *workspace, size_t workspace_bytes, const ds_moe_debug *dbg,
                  void *stream, char *err, size_t errlen);

@@ -452,25 +452,39 @@ void oracle_route(const int32_t *ids, int64_t T, int32_t k, int64_t E, int32_t *
 
 static double silu(double z) { return z / (1.0 + exp(-z)); } /* [UDS] 5.2.4 */
 
-/* Bytes of one routed expert: gate [F][D], up [F][D], down [D][F], each
- * Q2_K along its input dimension ([YD]: gate, up and down per expert). */
-int64_t oracle_expert_bytes(int64_t D, int64_t F) {
-  return 2 * oracle_q2k_bytes(F, D) + oracle_q2k_bytes(D, F);
+/* Expert storage formats: 0 = Q2_K (84-byte blocks), 1 = Q4_K (144-byte
+ * blocks).  Both store a matrix row by row along its input dimension. */
+static int64_t fmt_bytes(int fmt, int64_t rows, int64_t in_dim) {
+  return fmt ? oracle_q4k_bytes(rows, in_dim) : oracle_q2k_bytes(rows, in_dim);
 }
+
+static void fmt_dequantize(int fmt, const uint8_t *q, int64_t rows, int64_t in_dim, double *out) {
+  if (fmt) oracle_q4k_dequantize(q, rows, in_dim, out);
+  else oracle_q2k_dequantize(q, rows, in_dim, out);
+}
+
+/* Bytes of one routed expert: gate [F][D], up [F][D], down [D][F], each
+ * in the expert format along its input dimension ([YD]: gate, up and down
+ * per expert). */
+int64_t oracle_expert_bytes_fmt(int fmt, int64_t D, int64_t F) {
+  return 2 * fmt_bytes(fmt, F, D) + fmt_bytes(fmt, D, F);
+}
+
+int64_t oracle_expert_bytes(int64_t D, int64_t F) { return oracle_expert_bytes_fmt(0, D, F); }
 
 /* SwiGLU expert applied to n input rows:
  *   h = SiLU(Wg x) * (Wu x),  y = Wd h   ([UDS] 5.3.7 steps 3-4). */
-static void expert_ffn_q2k(const uint8_t *blob, int64_t D, int64_t F, const double *const *xs,
-                           double *const *ys, int64_t n) {
-  const uint8_t *gq = blob, *uq = blob + oracle_q2k_bytes(F, D), *dq = uq + oracle_q2k_bytes(F, D);
+static void expert_ffn(int fmt, const uint8_t *blob, int64_t D, int64_t F, const double *const *xs,
+                       double *const *ys, int64_t n) {
+  const uint8_t *gq = blob, *uq = blob + fmt_bytes(fmt, F, D), *dq = uq + fmt_bytes(fmt, F, D);
   double *rowg = (double *)malloc(sizeof(double) * (size_t)D);
   double *rowu = (double *)malloc(sizeof(double) * (size_t)D);
   double *rowd = (double *)malloc(sizeof(double) * (size_t)F);
   double *h = (double *)malloc(sizeof(double) * (size_t)(F * n));
-  int64_t bpr_d = oracle_q2k_blocks_per_row(D) * QBYTES, bpr_f = oracle_q2k_blocks_per_row(F) * QBYTES;
+  int64_t bpr_d = fmt_bytes(fmt, 1, D), bpr_f = fmt_bytes(fmt, 1, F);
   for (int64_t f = 0; f < F; ++f) {
-    oracle_q2k_dequantize(gq + f * bpr_d, 1, D, rowg);
-    oracle_q2k_dequantize(uq + f * bpr_d, 1, D, rowu);
+    fmt_dequantize(fmt, gq + f * bpr_d, 1, D, rowg);
+    fmt_dequantize(fmt, uq + f * bpr_d, 1, D, rowu);
     for (int64_t i = 0; i < n; ++i) {
       double g = 0.0, u = 0.0;
       for (int64_t d = 0; d < D; ++d) { g += rowg[d] * xs[i][d]; u += rowu[d] * xs[i][d]; }
@@ -478,7 +492,7 @@ static void expert_ffn_q2k(const uint8_t *blob, int64_t D, int64_t F, const doub
     }
   }
   for (int64_t d = 0; d < D; ++d) {
-    oracle_q2k_dequantize(dq + d * bpr_f, 1, F, rowd);
+    fmt_dequantize(fmt, dq + d * bpr_f, 1, F, rowd);
     for (int64_t i = 0; i < n; ++i) {
       double y = 0.0;
       for (int64_t f = 0; f < F; ++f) y += rowd[f] * h[i * F + f];
@@ -508,6 +522,7 @@ static void dense_ffn(const double *wg, const double *wu, const double *wd, int6
 /* ----------------------------------------------------------------- layer --- */
 
 typedef struct {
+  int fmt;
   int64_t T, D, E, F, Fs; int32_t k;
   const double *x; const uint8_t *const *experts;
   const double *sg, *su, *sd;
@@ -534,7 +549,7 @@ static void *layer_worker(void *p) {
         xs[r] = j->x + (pair / j->k) * j->D;
         ys[r] = j->y + pair * j->D;
       }
-      expert_ffn_q2k(j->experts[e], j->D, j->F, xs, ys, n);
+      expert_ffn(j->fmt, j->experts[e], j->D, j->F, xs, ys, n);
       free(xs); free(ys);
     } else {
       int64_t t = it - j->n_used;
@@ -549,12 +564,13 @@ static void *layer_worker(void *p) {
  * summed in that order.  experts[e] points at expert e's packed gate|up|down
  * (may be NULL for an expert no token selects).  sg/su/sd: shared expert
  * weights (ignored when Fs == 0).  ids, w: from oracle_select.  y_pairs
- * [T*k][D] and y_shared [T][D] are optional outputs.
+ * [T*k][D] and y_shared [T][D] are optional outputs.  fmt: the routed
+ * experts' format (0 = Q2_K, 1 = Q4_K).
  * Returns 0, or -1 when a selected expert's weights are missing. */
-int oracle_moe_layer(int64_t T, int64_t D, int64_t E, int64_t F, int64_t Fs, int32_t k,
-                     const double *x, const uint8_t *const *experts, const double *sg,
-                     const double *su, const double *sd, const int32_t *ids, const double *w,
-                     double *out, double *y_pairs, double *y_shared, int nthreads) {
+int oracle_moe_layer_fmt(int fmt, int64_t T, int64_t D, int64_t E, int64_t F, int64_t Fs, int32_t k,
+                         const double *x, const uint8_t *const *experts, const double *sg,
+                         const double *su, const double *sd, const int32_t *ids, const double *w,
+                         double *out, double *y_pairs, double *y_shared, int nthreads) {
   if (T == 0) return 0;
   int32_t *counts = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
   int32_t *offsets = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
@@ -574,7 +590,7 @@ int oracle_moe_layer(int64_t T, int64_t D, int64_t E, int64_t F, int64_t Fs, int
     pthread_t th[256];
     layer_job jobs[256];
     for (int t = 0; t < nthreads; ++t) {
-      layer_job j = {T, D, E, F, Fs, k, x, experts, sg, su, sd, offsets, perm, used, n_used,
+      layer_job j = {fmt, T, D, E, F, Fs, k, x, experts, sg, su, sd, offsets, perm, used, n_used,
                      y, ys, t, nthreads};
       jobs[t] = j;
     }
@@ -592,6 +608,15 @@ int oracle_moe_layer(int64_t T, int64_t D, int64_t E, int64_t F, int64_t Fs, int
   if (!y_shared) free(ys);
   free(used); free(counts); free(offsets); free(perm);
   return bad ? -1 : 0;
+}
+
+/* The layer with Q2_K experts. */
+int oracle_moe_layer(int64_t T, int64_t D, int64_t E, int64_t F, int64_t Fs, int32_t k,
+                     const double *x, const uint8_t *const *experts, const double *sg,
+                     const double *su, const double *sd, const int32_t *ids, const double *w,
+                     double *out, double *y_pairs, double *y_shared, int nthreads) {
+  return oracle_moe_layer_fmt(0, T, D, E, F, Fs, k, x, experts, sg, su, sd, ids, w, out, y_pairs,
+                              y_shared, nthreads);
 }
 
 /* ------------------------------------------------------------ RMSNorm --- */

@@ -70,6 +70,11 @@ def lib():
         L.oracle_select.argtypes = [vp, i64, i64, i32, dbl, dbl, vp, vp, vp]
         L.oracle_route.restype = None
         L.oracle_route.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp]
+        L.oracle_expert_bytes_fmt.restype = i64
+        L.oracle_expert_bytes_fmt.argtypes = [ctypes.c_int, i64, i64]
+        L.oracle_moe_layer_fmt.restype = ctypes.c_int
+        L.oracle_moe_layer_fmt.argtypes = [ctypes.c_int, i64, i64, i64, i64, i64, i32, vp, vp, vp,
+                                           vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
         L.oracle_moe_layer.restype = ctypes.c_int
         L.oracle_moe_layer.argtypes = [i64, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp,
                                        vp, vp, vp, ctypes.c_int]
@@ -174,9 +179,12 @@ def route(ids: np.ndarray, E: int):
     return counts, offsets, perm, pos
 
 
-def moe_layer(x, experts, shared, ids, w, D, E, F, Fs, want_parts=False):
-    """out[T][D] fp64.  experts: dict e -> packed uint8 blob (gate|up|down);
-    shared: (gate, up, down) fp64 arrays or None."""
+FORMATS = {"q2k": 0, "q4k": 1}
+
+
+def moe_layer(x, experts, shared, ids, w, D, E, F, Fs, want_parts=False, fmt="q2k"):
+    """out[T][D] fp64.  experts: dict e -> packed uint8 blob (gate|up|down) in
+    format fmt ("q2k" | "q4k"); shared: (gate, up, down) fp64 arrays or None."""
     x = _c(x, np.float64)
     T = x.shape[0]
     ids = _c(ids, np.int32)
@@ -194,9 +202,10 @@ def moe_layer(x, experts, shared, ids, w, D, E, F, Fs, want_parts=False):
     out = np.empty((T, D), np.float64)
     yp = np.empty((T * k, D), np.float64) if want_parts else None
     ys = np.empty((T, D), np.float64) if want_parts else None
-    rc = lib().oracle_moe_layer(T, D, E, F, Fs, k, _ptr(x), ctypes.cast(ptrs, ctypes.c_void_p),
-                                _ptr(sg), _ptr(su), _ptr(sd), _ptr(ids), _ptr(w), _ptr(out),
-                                _ptr(yp), _ptr(ys), NTHREADS)
+    rc = lib().oracle_moe_layer_fmt(FORMATS[fmt], T, D, E, F, Fs, k, _ptr(x),
+                                    ctypes.cast(ptrs, ctypes.c_void_p), _ptr(sg), _ptr(su),
+                                    _ptr(sd), _ptr(ids), _ptr(w), _ptr(out), _ptr(yp), _ptr(ys),
+                                    NTHREADS)
     if rc:
         raise ValueError("oracle_moe_layer: a selected expert has no weights")
     return (out, yp, ys) if want_parts else out
@@ -220,9 +229,11 @@ def as_f64(a, dtype: str) -> np.ndarray:
 
 
 def expert_blob(cfg: dsgen.Config, e: int, layer: int = 0) -> np.ndarray:
-    """Expert e regenerated from its counters and packed by the oracle's quantiser."""
+    """Expert e regenerated from its counters and packed by the oracle's quantiser
+    in the workload's expert format."""
     g, u, d = dsgen.host_expert_f32(cfg, e, layer)
-    return np.concatenate([quantize(g).ravel(), quantize(u).ravel(), quantize(d).ravel()])
+    q = quantize_q4k if cfg.expert_fmt == "q4k" else quantize
+    return np.concatenate([q(g).ravel(), q(u).ravel(), q(d).ravel()])
 
 
 class LayerOracle:
@@ -253,7 +264,7 @@ class LayerOracle:
         L = self.logits(x64)
         ids, w = select(L, c.k)
         res = moe_layer(x64, self.experts(ids), self.shared, ids, w, c.D, c.E, c.F, c.Fs,
-                        want_parts=want_parts)
+                        want_parts=want_parts, fmt=c.expert_fmt)
         return res, ids, w, L
 
 

@@ -47,6 +47,12 @@ def test_sizes(L):
     assert ds.expert_bytes(4096, 2048) == 8_257_536
     assert ds.expert_bytes(256, 128) == 84 * (2 * 128 + 256)
     assert ds.version().startswith("ds_moe")
+    assert ds.q4k_bytes(1, 256) == 144
+    assert ds.q4k_bytes(4096, 128) == 4096 * 144
+    assert ds.q4k_bytes(3, -1) == 0
+    assert ds.expert_bytes(4096, 2048, ds.DS_Q4_K) == 3 * 2048 * 16 * 144
+    assert ds.expert_bytes(256, 128, ds.DS_Q4_K) == 144 * (2 * 128 + 256)
+    assert ds.expert_bytes(4096, 2048, 7) == 0
 
 
 def test_workspace_bytes_and_validation(L):
@@ -62,7 +68,9 @@ def test_workspace_bytes_and_validation(L):
            ds.MoEShape(4096, 256, 2048, 2048, 6, routed_scale=float("nan")),
            ds.MoEShape(4096, 256, 2048, 2048, 6, logit_scale=-1.0),
            ds.MoEShape(4096, 256, 2048, 2048, 6, logit_scale=float("inf")),
-           ds.MoEShape(4096, 256, 2048, 2048, 6, bias_select_only=2)]
+           ds.MoEShape(4096, 256, 2048, 2048, 6, bias_select_only=2),
+           ds.MoEShape(4096, 256, 2048, 2048, 6, expert_format=2),
+           ds.MoEShape(4096, 256, 2048, 2048, 6, expert_format=-1)]
     for b in bad:
         with pytest.raises(ds.DsMoeError) as ei:
             ds.workspace_bytes(b, 4)
@@ -120,3 +128,7 @@ def test_layer_path_host_checks(L):
         ds.layer_path(ds.MoEShape(4000, 256, 2048, 2048, 6), 4)
     with pytest.raises(ds.DsMoeError):
         ds.layer_path(sh, -1)
+    # Q4_K experts: the grouped GEMV path at every batch size
+    q4 = ds.MoEShape(4096, 256, 2048, 2048, 6, expert_format=ds.DS_Q4_K)
+    for T in (1, 4, 8, 4096):
+        assert ds.layer_path(q4, T) == ds.PATH_GROUPED_GEMV

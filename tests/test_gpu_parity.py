@@ -167,7 +167,8 @@ def layer_parity(cfg, tol, scale=1.0, logit_scale=1.0, bias_select_only=0, W=Non
     L = lo.logits(x64)
     ids, w = oracle.select(L, cfg.k, scale, logit_scale, lo.bias if bias_select_only else None)
     check_route_full(dbg, ids, cfg.E)
-    res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
+    res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs,
+                           fmt=cfg.expert_fmt)
     check_close(dbg["logits"], L, 1e-5, "logits")
     assert np.max(np.abs(dbg["w"] - w)) <= 1e-5
     return check_close(out, res, tol)
@@ -298,7 +299,8 @@ def test_decode_b1_logit_scale(decode1):
     ids, w = oracle.select(L, cfg.k, 1.5, 1.5)
     check_route_full(dbg, ids, cfg.E)
     assert np.max(np.abs(dbg["w"] - w)) <= 1e-5
-    res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
+    res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs,
+                           fmt=cfg.expert_fmt)
     check_close(out, res, DECODE_TOL)
 
 
@@ -395,7 +397,7 @@ def test_prefill_parity_sampled():
     rows = np.sort(rng.choice(cfg.T, 6, replace=False))
     rows = np.unique(np.concatenate([rows, [0, cfg.T - 1]]))
     res = oracle.moe_layer(x64[rows], lo.experts(ids[rows]), lo.shared, ids[rows], w[rows], cfg.D,
-                           cfg.E, cfg.F, cfg.Fs)
+                           cfg.E, cfg.F, cfg.Fs, fmt=cfg.expert_fmt)
     check_close(out[rows], res, PREFILL_TOL)
 
 
@@ -466,3 +468,89 @@ def test_stack_equals_layer_by_layer():
         assert not torch.equal(xb, xb_in)
     ds.sync_status()
     assert torch.equal(xa, xb)
+
+
+# ------------------------------------------------------------------ Q4_K --
+# The 144-byte Q4_K experts ("Understanding Dwarf Star", 2.3.2): quantiser
+# and dequantiser bit-exact, the layer at the decode tolerance (the grouped
+# dequantising GEMV path with fp32 arithmetic serves every batch size).
+
+def gpu_quantize_q4k(w_np):
+    w = torch.from_numpy(np.ascontiguousarray(w_np, np.float32)).cuda()
+    out = torch.zeros(ds.q4k_bytes(*w.shape), dtype=torch.uint8, device="cuda")
+    ds.quantize_q4k(w, out)
+    ds.sync_status()
+    return out.cpu().numpy().reshape(w.shape[0], -1)
+
+
+@pytest.mark.parametrize("rows,in_dim,scale", [(3, 256, 0.02), (5, 128, 1.0), (4, 300, 5.0),
+                                               (64, 1024, 0.02), (2, 256, 1e4), (2, 512, 1e-30)])
+def test_q4k_quantize_bit_exact_random(rows, in_dim, scale):
+    rng = np.random.default_rng(rows * 1000 + in_dim + 1)
+    x = (rng.normal(size=(rows, in_dim)) * scale).astype(np.float32)
+    x[0, :32] = np.abs(x[0, :32])
+    if rows > 1:
+        x[1, 32:64] = 0.0
+        x[1, 64:96] = -np.abs(x[1, 64:96])
+    assert np.array_equal(gpu_quantize_q4k(x), oracle.quantize_q4k(x))
+
+
+def test_q4k_quantize_domain_edges_and_status():
+    x = np.zeros((3, 256), np.float32)
+    x[0, 0], x[0, 1] = 65504.0, -65504.0
+    x[1, 7] = 1e-45
+    x[2, :] = np.linspace(-3.0, 7.0, 256)
+    assert np.array_equal(gpu_quantize_q4k(x), oracle.quantize_q4k(x))
+    g, _, d = dsgen.host_expert_f32(dsgen.DECODE1, 17)
+    assert np.array_equal(gpu_quantize_q4k(d), oracle.quantize_q4k(d))
+    bad = np.zeros((2, 256), np.float32)
+    bad[1, 5] = np.nan
+    w = torch.from_numpy(bad).cuda()
+    out = torch.full((ds.q4k_bytes(2, 256),), 7, dtype=torch.uint8, device="cuda")
+    ds.quantize_q4k(w, out)
+    with pytest.raises(ds.DsMoeError) as ei:
+        ds.sync_status()
+    assert ei.value.code == ds.DS_ERR_DEVICE_CHECK
+    o = out.cpu().numpy()
+    assert not o[144:].any() and not o[:144].any()   # bad block zeroed; the zero block is all zero
+    ds.sync_status()
+
+
+def test_q4k_dequantize_bit_exact():
+    rng = np.random.default_rng(4)
+    x = (rng.normal(size=(16, 512)) * 0.02).astype(np.float32)
+    q = oracle.quantize_q4k(x)
+    blocks = rng.integers(0, 256, (4, 3 * 144)).astype(np.uint8)
+    for r in range(4):
+        for b in range(3):
+            for o in (0, 2):
+                v = int(rng.integers(0, 0x7BFF))
+                blocks[r, 144 * b + o], blocks[r, 144 * b + o + 1] = v & 0xFF, v >> 8
+    for qq, rows, in_dim in ((q, 16, 512), (blocks, 4, 700)):
+        ref = oracle.dequantize_q4k(qq, rows, in_dim).astype(np.float32)
+        out = torch.empty((rows, in_dim), dtype=torch.float32, device="cuda")
+        ds.dequantize_q4k(torch.from_numpy(qq).cuda(), rows, in_dim, out)
+        ds.sync_status()
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("T,Fs,k,E,dtype", [(8, 0, 2, 16, "f32"), (1, 512, 6, 16, "bf16"),
+                                            (3, 256, 2, 16, "f32"), (33, 1024, 4, 40, "bf16")])
+def test_q4k_layer_parity(T, Fs, k, E, dtype):
+    from dataclasses import replace
+    cfg = replace(_small(T, Fs, k, E, dtype), expert_fmt="q4k")
+    assert ds.layer_path(synthetic.shape_of(cfg), T) == ds.PATH_GROUPED_GEMV
+    layer_parity(cfg, DECODE_TOL)
+
+
+def test_q4k_tiny_ragged_width():
+    """n_ff = 128: half a Q4_K block per down row (zero-padded sub-blocks)."""
+    from dataclasses import replace
+    layer_parity(replace(dsgen.TINY, expert_fmt="q4k"), DECODE_TOL)
+
+
+def test_q4k_decode_b1_flash_shape():
+    from dataclasses import replace
+    cfg = replace(dsgen.DECODE1, expert_fmt="q4k")
+    assert ds.expert_bytes(cfg.D, cfg.F, ds.DS_Q4_K) == cfg.expert_bytes == 3 * 2048 * 16 * 144
+    layer_parity(cfg, DECODE_TOL)

@@ -671,3 +671,44 @@ def test_q4k_quantizer_roundtrip_on_grid_is_byte_exact():
         w32 = w.astype(np.float32)
         assert np.array_equal(w32.astype(np.float64), w)
         assert np.array_equal(oracle.quantize_q4k(w32)[0], blk), trial
+
+
+def test_q4k_swiglu_closed_form_handbuilt_expert():
+    """The hand-built SwiGLU expert again, stored as Q4_K blocks packed by
+    the test: y_d = SiLU(x_0) * 2 x_0 for every d."""
+    D, F = 256, 256
+    e0 = [1] + [0] * 255
+    one = q4k_handbuilt(0x3C00, 0, [1] * 8, [0] * 8, e0)   # w_0 = 1
+    two = q4k_handbuilt(0x4000, 0, [1] * 8, [0] * 8, e0)   # w_0 = 2
+    zero = np.zeros(144, np.uint8)
+    gate = np.stack([one] + [zero] * (F - 1))
+    up = np.stack([two] + [zero] * (F - 1))
+    down = np.stack([one] * D)
+    blob = np.concatenate([gate.ravel(), up.ravel(), down.ravel()])
+    assert blob.size == oracle.lib().oracle_expert_bytes_fmt(1, D, F)
+    x = np.zeros((3, D))
+    x[:, 0] = [2.0, -1.5, 0.0]
+    out = oracle.moe_layer(x, {0: blob}, None, np.zeros((3, 1), np.int32), np.ones((3, 1)), D, 1,
+                           F, 0, fmt="q4k")
+    for t, x0 in enumerate([2.0, -1.5, 0.0]):
+        assert np.allclose(out[t], x0 / (1 + math.exp(-x0)) * 2 * x0, rtol=1e-15, atol=0)
+
+
+def test_q4k_layer_top1_single_expert_is_swiglu_ffn():
+    rng = np.random.default_rng(12)
+    D, F = 256, 128
+    g, u = (rng.normal(size=(F, D)) * 0.02).astype(np.float32), (rng.normal(size=(F, D)) * 0.02).astype(np.float32)
+    dn = (rng.normal(size=(D, F)) * 0.02).astype(np.float32)
+    qg, qu, qd = oracle.quantize_q4k(g), oracle.quantize_q4k(u), oracle.quantize_q4k(dn)
+    blob = np.concatenate([qg.ravel(), qu.ravel(), qd.ravel()])
+    G, U, DN = (oracle.dequantize_q4k(qg, F, D), oracle.dequantize_q4k(qu, F, D),
+                oracle.dequantize_q4k(qd, D, F))
+    x = rng.normal(size=(4, D))
+    out = oracle.moe_layer(x, {0: blob}, None, np.zeros((4, 1), np.int32), np.ones((4, 1)), D, 1,
+                           F, 0, fmt="q4k")
+    ref = (_silu(x @ G.T) * (x @ U.T)) @ DN.T
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-15)
+    # 4-bit codes track the fp32 weights closer than 2-bit ones
+    e4 = np.abs(G - g).max() / np.abs(g).max()
+    e2 = np.abs(oracle.dequantize(oracle.quantize(g), F, D) - g).max() / np.abs(g).max()
+    assert e4 < e2 / 3
