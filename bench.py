@@ -279,6 +279,49 @@ def time_layer(cfg, iters, dev, warmup=3):
     return e0.elapsed_time(e1) / iters, used, path
 
 
+def time_decode_rotating(cfg, R, iters, dev, warmup=3):
+    """(ms per one-token layer call, mean used experts, path) with the calls
+    rotating over R independently generated layers (so that one call's
+    experts are not in L2 from the previous one), captured into a CUDA graph
+    of 10 R calls and replayed."""
+    import torch
+    import bit_quantized_routed_router_gb300 as ds
+    from bit_quantized_routed_router_gb300 import synthetic
+
+    sh = synthetic.shape_of(cfg)
+    layers = [synthetic.build_layer(cfg, layer=r, device=dev) for r in range(R)]
+    xs = [synthetic.build_x(cfg, layer=r, device=dev) for r in range(R)]
+    out = torch.empty((cfg.T, cfg.D), dtype=torch.float32, device=dev)
+    ws = torch.empty(ds.workspace_bytes(sh, cfg.T), dtype=torch.uint8, device=dev)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    used = []
+    for r in range(R):
+        ds.layer(sh, layers[r], xs[r], out, ws, debug={"counts": counts})
+        used.append(int((counts > 0).sum().item()))
+    for i in range(warmup):
+        ds.layer(sh, layers[i % R], xs[i % R], out, ws)
+    torch.cuda.synchronize(dev)
+    g = 10 * R
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(g):
+            ds.layer(sh, layers[i % R], xs[i % R], out, ws)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(1, iters // g)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ds.sync_status()
+    path = ds.layer_path(sh, cfg.T, xs[0])
+    del layers, ws, out
+    torch.cuda.empty_cache()
+    return e0.elapsed_time(e1) / (reps * g), statistics.mean(used), path
+
+
 def time_stack(cfg, iters, dev, warmup=3):
     """The 43-layer stack (x += layer(bf16(RMSNorm(x))) per layer, T tokens):
     (ms per step, bytes read per step, distinct experts per layer, path).  One
@@ -337,7 +380,8 @@ def time_stack(cfg, iters, dev, warmup=3):
 def extra_workloads(args, dev):
     """The other timed workloads of the metric (not the headline line):
     prefill T=4096 (uniform and Zipf router) against the bf16 tensor roofline,
-    decode T=32 Zipf and the 43-layer stack at T=8 against the HBM roofline.  Each on its own layer, inputs
+    decode T=32 Zipf, decode T=1 with Q4_K experts and the 43-layer stack at
+    T=8 against the HBM roofline.  Each on its own layer, inputs
     resident, CUDA events over `iters` layer calls after warm-up."""
     import torch
     import bit_quantized_routed_router_gb300 as ds
@@ -362,6 +406,16 @@ def extra_workloads(args, dev):
             entry["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                                  "frac": gbs / hbm, "peak_source": pk_kind, "algorithmic_bytes": b}
         res[cfg.name] = entry
+    cfg = dsgen.DECODE1_Q4K
+    ms, used, path = time_decode_rotating(cfg, 2, 400, dev)
+    b = algorithmic_bytes(cfg, used, cfg.T)
+    gbs = b / (ms / 1e3) / 1e9
+    hbm = float(pk.get("hbm_gbs", HBM_FALLBACK_GBS))
+    res[cfg.name] = {"tokens_per_s": cfg.T / (ms / 1e3), "ms_per_layer": ms, "T": cfg.T,
+                     "used_experts": used, "path": path,
+                     "timing": "CUDA graph of 20 calls rotating over 2 layers",
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                  "frac": gbs / hbm, "peak_source": pk_kind, "algorithmic_bytes": b}}
     cfg = dsgen.STACK
     ms, b, used, path = time_stack(cfg, 20, dev)
     gbs = b / (ms / 1e3) / 1e9
@@ -382,6 +436,7 @@ WORKLOADS = {
     "prefill_zipf": dsgen.PREFILL_ZIPF,
     "decode32": dsgen.DECODE32_ZIPF,
     "stack": dsgen.STACK,
+    "decode_q4k": dsgen.DECODE1_Q4K,
     # same shapes at 1/4 of the experts and tokens (about 96 tokens per
     # expert as at full size): a case small enough for full profiler captures
     "prefill_small": None,
@@ -464,6 +519,12 @@ def main():
         libbuild.build()
         cfg = WORKLOADS[args.workload] or replace(dsgen.PREFILL, name="prefill T=1024 E=64 (profiling case)",
                                                    T=1024, E=64)
+        if args.workload == "decode_q4k":
+            ms, used, path = time_decode_rotating(cfg, 2, args.steps, torch.device("cuda", 0),
+                                                  warmup=args.warmup)
+            print(json.dumps({"workload": cfg.name, "ms_per_layer": ms, "tokens_per_s": cfg.T / (ms / 1e3),
+                              "used_experts": used, "path": path, "steps": args.steps}), flush=True)
+            return
         if args.workload == "stack":
             ms, b, used, path = time_stack(cfg, args.steps, torch.device("cuda", 0), warmup=args.warmup)
             print(json.dumps({"workload": cfg.name, "ms_per_step": ms, "tokens_per_s": cfg.T / (ms / 1e3),

@@ -27,7 +27,8 @@ SYMBOLS = ["ds_moe_q2k_bytes", "ds_moe_expert_bytes", "ds_moe_quantize_q2k",
            "ds_moe_dequantize_q2k", "ds_moe_workspace_bytes", "ds_moe_layer",
            "ds_moe_layer_hostio", "ds_moe_stack", "ds_moe_sync_status", "ds_moe_version",
            "ds_moe_layer_noalloc", "ds_moe_layer_path", "ds_moe_q4k_bytes",
-           "ds_moe_expert_bytes_fmt", "ds_moe_quantize_q4k", "ds_moe_dequantize_q4k"]
+           "ds_moe_expert_bytes_fmt", "ds_moe_quantize_q4k", "ds_moe_dequantize_q4k",
+           "ds_moe_stack_mixed"]
 
 # ds_moe_layer_path results
 PATH_NONE, PATH_STREAM, PATH_DECODE3, PATH_GROUPED_GEMV, PATH_TENSOR_CORE = 0, 1, 2, 3, 4
@@ -95,6 +96,9 @@ def lib():
         L.ds_moe_stack.restype = ctypes.c_int
         L.ds_moe_stack.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), ctypes.c_int32,
                                    vp, i64, ctypes.c_float, vp, sz, vp, cp, sz]
+        L.ds_moe_stack_mixed.restype = ctypes.c_int
+        L.ds_moe_stack_mixed.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp,
+                                         ctypes.c_int32, vp, i64, ctypes.c_float, vp, sz, vp, cp, sz]
         L.ds_moe_layer_noalloc.restype = ctypes.c_int
         L.ds_moe_layer_noalloc.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64,
                                            vp, vp, cp, sz]
@@ -241,11 +245,20 @@ def layer_noalloc(shape: MoEShape, weights: MoEWeights, x, out, stream=None, T: 
           x.data_ptr(), T, out.data_ptr(), _stream(stream))
 
 
-def stack(shape: MoEShape, layers, x, workspace, eps: float = 1e-6, stream=None):
-    """x[T][D] fp32 residual, updated in place through len(layers) layers."""
+def stack(shape: MoEShape, layers, x, workspace, eps: float = 1e-6, stream=None, formats=None):
+    """x[T][D] fp32 residual, updated in place through len(layers) layers.
+    formats: optional per-layer expert formats (DS_Q2_K / DS_Q4_K)."""
     arr = (Weights * len(layers))(*[w.c() for w in layers])
-    _call(lib().ds_moe_stack, ctypes.byref(shape.c()), arr, len(layers), x.data_ptr(), x.shape[0],
-          eps, workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    if formats is None:
+        _call(lib().ds_moe_stack, ctypes.byref(shape.c()), arr, len(layers), x.data_ptr(),
+              x.shape[0], eps, *ws, _stream(stream))
+        return
+    if len(formats) != len(layers):
+        raise ValueError("one format per layer")
+    fm = (ctypes.c_int32 * len(layers))(*formats)
+    _call(lib().ds_moe_stack_mixed, ctypes.byref(shape.c()), arr, fm, len(layers), x.data_ptr(),
+          x.shape[0], eps, *ws, _stream(stream))
 
 
 def sync_status(stream=None):

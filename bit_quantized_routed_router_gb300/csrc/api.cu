@@ -344,9 +344,10 @@ int ds_moe_layer_hostio(const ds_moe_shape *shape, const ds_moe_weights *weights
   return e == cudaSuccess ? DS_OK : cuda_fail(err, errlen, e, "copy out to host");
 }
 
-int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_t n_layers,
-                 float *x, int64_t T, float eps, void *workspace, size_t workspace_bytes,
-                 void *stream, char *err, size_t errlen) {
+int ds_moe_stack_mixed(const ds_moe_shape *shape, const ds_moe_weights *layers,
+                       const int32_t *formats, int32_t n_layers, float *x, int64_t T, float eps,
+                       void *workspace, size_t workspace_bytes, void *stream, char *err,
+                       size_t errlen) {
   Shape sh{};
   int rc = check_shape(shape, err, errlen, &sh);
   if (rc) return rc;
@@ -354,6 +355,18 @@ int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_
     return fail(err, errlen, DS_ERR_INVALID_ARG, "the stack feeds bf16 normalised inputs: x_dtype must be DS_BF16");
   if (n_layers < 0 || (n_layers > 0 && !layers))
     return fail(err, errlen, DS_ERR_INVALID_ARG, "bad layer array");
+  // the workspace serves every layer: laid out for Q2_K when any layer is
+  // Q2_K (its tensor-core scratch comes last and the other regions do not
+  // depend on the format)
+  bool any_q2 = false;
+  for (int l = 0; l < n_layers; ++l) {
+    const int f = formats ? formats[l] : sh.fmt;
+    if (f != DS_Q2_K && f != DS_Q4_K)
+      return fail(err, errlen, DS_ERR_INVALID_ARG, "formats[%d]=%d: need DS_Q2_K or DS_Q4_K", l, f);
+    any_q2 = any_q2 || f == DS_Q2_K;
+  }
+  Shape sh_ws = sh;
+  sh_ws.fmt = any_q2 ? DS_Q2_K : DS_Q4_K;
   for (int l = 0; l < n_layers; ++l)
     if ((rc = check_weights(sh, &layers[l], err, errlen))) return rc;
   if (T < 0 || T > (1 << 24)) return fail(err, errlen, DS_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
@@ -362,21 +375,30 @@ int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_
   if (!aligned(x, 16) || !aligned(workspace, ALIGN))
     return fail(err, errlen, DS_ERR_INVALID_ARG, "x must be 16-byte and workspace 256-byte aligned");
   if (!(eps > 0.0f) || !isfinite(eps)) return fail(err, errlen, DS_ERR_INVALID_ARG, "eps must be > 0");
-  const size_t need = layout(sh, T, nullptr, nullptr);
+  const size_t need = layout(sh_ws, T, nullptr, nullptr);
   if (workspace_bytes < need)
     return fail(err, errlen, DS_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes",
                 workspace_bytes, need);
   if (!status_word()) return fail(err, errlen, DS_ERR_CUDA, "no CUDA device");
   Work wk;
-  layout(sh, T, (char *)workspace, &wk);
+  layout(sh_ws, T, (char *)workspace, &wk);
   cudaStream_t s = (cudaStream_t)stream;
   for (int l = 0; l < n_layers; ++l) {
+    Shape sl = sh;
+    if (formats) sl.fmt = formats[l];
     cudaError_t e = launch_rmsnorm_bf16(x, T, sh.D, eps, wk.xn, s);
     if (e != cudaSuccess) return cuda_fail(err, errlen, e, "rmsnorm");
-    rc = run_layer(sh, layers[l], wk.xn, x, true, wk, nullptr, s, err, errlen);
+    rc = run_layer(sl, layers[l], wk.xn, x, true, wk, nullptr, s, err, errlen);
     if (rc) return rc;
   }
   return DS_OK;
+}
+
+int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_t n_layers,
+                 float *x, int64_t T, float eps, void *workspace, size_t workspace_bytes,
+                 void *stream, char *err, size_t errlen) {
+  return ds_moe_stack_mixed(shape, layers, nullptr, n_layers, x, T, eps, workspace,
+                            workspace_bytes, stream, err, errlen);
 }
 
 int ds_moe_sync_status(void *stream, char *err, size_t errlen) {

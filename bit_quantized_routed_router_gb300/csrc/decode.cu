@@ -87,57 +87,95 @@ __device__ __forceinline__ void q2k_row_dot(const uint8_t *__restrict__ row, int
   }
 }
 
-// Partial dot products of one Q4_K row ("Understanding Dwarf Star", 2.3.2:
-// 8 sub-blocks of 32 weights, 6-bit scales and mins, 4-bit codes); this
-// lane's sub-blocks sb = lane + 32 i.  Weights formed exactly as above.
-template <int NTOK>
-__device__ __forceinline__ void q4k_row_dot(const uint8_t *__restrict__ row, int in_dim,
-                                            const float4 *__restrict__ xs, int stride4, int nt,
-                                            float acc[NTOK]) {
+// Partial dot products of NR Q4_K rows ("Understanding Dwarf Star", 2.3.2:
+// 8 sub-blocks of 32 weights, 6-bit scales and mins, 4-bit codes) with nt
+// staged inputs; this lane's sub-blocks sb = lane + 32 i.  The code and
+// header loads of all NR rows for one sub-block are issued
+// before their use.  Weights formed exactly as for Q2_K.
+template <int NR, int NTOK>
+__device__ __forceinline__ void q4k_rows_dot(const uint8_t *const *rows, int in_dim,
+                                             const float4 *__restrict__ xs, int stride4, int nt,
+                                             float (*acc)[NTOK]) {
   const int lane = threadIdx.x & 31;
   const int nsb = in_dim >> 5;
   for (int sb = lane; sb < nsb; sb += 32) {
-    const uint8_t *blk = row + (sb >> 3) * Q4B;
     const int s = sb & 7;
-    const uint4 codes = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * s);
-    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);  // d, dmin, 12 field bytes
-    // the 96-bit field integer = hdr.y | hdr.z << 32 | hdr.w << 64
-    const uint64_t f_lo = (uint64_t)hdr.y | ((uint64_t)hdr.z << 32);
-    const int sc = (int)((f_lo >> (6 * s)) & 63u);
-    const int pm = 48 + 6 * s;  // min field 8 + s
-    const int mm = pm + 6 <= 64 ? (int)((f_lo >> pm) & 63u)
-                   : pm >= 64   ? (int)((hdr.w >> (pm - 64)) & 63u)
-                                : (int)(((f_lo >> pm) | ((uint64_t)hdr.w << (64 - pm))) & 63u);
-    const float dsc = fp16_to_f32((uint16_t)(hdr.x & 0xFFFF)) * (float)sc;
-    const float dmm = fp16_to_f32((uint16_t)(hdr.x >> 16)) * (float)mm;
-    const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+    uint4 codes[NR], hdr[NR];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      float w[4];
+    for (int r = 0; r < NR; ++r) {
+      const uint8_t *blk = rows[r] + (sb >> 3) * Q4B;
+      codes[r] = __ldg(reinterpret_cast<const uint4 *>(blk + 16 + 16 * s));
+      hdr[r] = __ldg(reinterpret_cast<const uint4 *>(blk));  // d, dmin, 12 field bytes
+    }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        w[i] = __fmaf_rn(dsc, (float)((cw[jj >> 1] >> (4 * (4 * (jj & 1) + i))) & 15u), -dmm);
-      const int slot = swz(8 * sb + jj);
+    for (int r = 0; r < NR; ++r) {
+      // the 96-bit field integer = hdr.y | hdr.z << 32 | hdr.w << 64
+      const uint64_t f_lo = (uint64_t)hdr[r].y | ((uint64_t)hdr[r].z << 32);
+      const int sc = (int)((f_lo >> (6 * s)) & 63u);
+      const int pm = 48 + 6 * s;  // min field 8 + s
+      const int mm = pm + 6 <= 64 ? (int)((f_lo >> pm) & 63u)
+                     : pm >= 64   ? (int)((hdr[r].w >> (pm - 64)) & 63u)
+                                  : (int)(((f_lo >> pm) | ((uint64_t)hdr[r].w << (64 - pm))) & 63u);
+      const float dsc = fp16_to_f32((uint16_t)(hdr[r].x & 0xFFFF)) * (float)sc;
+      const float dmm = fp16_to_f32((uint16_t)(hdr[r].x >> 16)) * (float)mm;
 #pragma unroll
-      for (int t = 0; t < NTOK; ++t) {
-        if (t < nt) {
-          const float4 xv = xs[t * stride4 + slot];
-          acc[t] = fmaf(w[0], xv.x, acc[t]);
-          acc[t] = fmaf(w[1], xv.y, acc[t]);
-          acc[t] = fmaf(w[2], xv.z, acc[t]);
-          acc[t] = fmaf(w[3], xv.w, acc[t]);
+      for (int jj = 0; jj < 8; ++jj) {
+        const uint32_t cw = jj < 2 ? codes[r].x : jj < 4 ? codes[r].y : jj < 6 ? codes[r].z : codes[r].w;
+        float w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          w[i] = __fmaf_rn(dsc, (float)((cw >> (4 * (4 * (jj & 1) + i))) & 15u), -dmm);
+        const int slot = swz(8 * sb + jj);
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t) {
+          if (t < nt) {
+            const float4 xv = xs[t * stride4 + slot];
+            acc[r][t] = fmaf(w[0], xv.x, acc[r][t]);
+            acc[r][t] = fmaf(w[1], xv.y, acc[r][t]);
+            acc[r][t] = fmaf(w[2], xv.z, acc[r][t]);
+            acc[r][t] = fmaf(w[3], xv.w, acc[r][t]);
+          }
         }
       }
     }
   }
 }
 
+// Two rows (gate and up) in the format FMT.
 template <int FMT, int NTOK>
-__device__ __forceinline__ void q_row_dot(const uint8_t *__restrict__ row, int in_dim,
-                                          const float4 *__restrict__ xs, int stride4, int nt,
-                                          float acc[NTOK]) {
-  if (FMT == DS_Q4_K) q4k_row_dot<NTOK>(row, in_dim, xs, stride4, nt, acc);
-  else q2k_row_dot<NTOK>(row, in_dim, xs, stride4, nt, acc);
+__device__ __forceinline__ void q_rows_dot2(const uint8_t *__restrict__ ra, const uint8_t *__restrict__ rb,
+                                            int in_dim, const float4 *__restrict__ xs, int stride4,
+                                            int nt, float acc_a[NTOK], float acc_b[NTOK]) {
+  if (FMT == DS_Q4_K) {
+    float acc[2][NTOK];
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) { acc[0][t] = acc_a[t]; acc[1][t] = acc_b[t]; }
+    const uint8_t *rows[2] = {ra, rb};
+    q4k_rows_dot<2, NTOK>(rows, in_dim, xs, stride4, nt, acc);
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) { acc_a[t] = acc[0][t]; acc_b[t] = acc[1][t]; }
+  } else {
+    q2k_row_dot<NTOK>(ra, in_dim, xs, stride4, nt, acc_a);
+    q2k_row_dot<NTOK>(rb, in_dim, xs, stride4, nt, acc_b);
+  }
+}
+
+// One row in the format FMT.
+template <int FMT, int NTOK>
+__device__ __forceinline__ void q_row_dot1(const uint8_t *__restrict__ ra, int in_dim,
+                                           const float4 *__restrict__ xs, int stride4, int nt,
+                                           float acc_a[NTOK]) {
+  if (FMT == DS_Q4_K) {
+    float acc[1][NTOK];
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) acc[0][t] = acc_a[t];
+    const uint8_t *rows[1] = {ra};
+    q4k_rows_dot<1, NTOK>(rows, in_dim, xs, stride4, nt, acc);
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) acc_a[t] = acc[0][t];
+  } else {
+    q2k_row_dot<NTOK>(ra, in_dim, xs, stride4, nt, acc_a);
+  }
 }
 
 // Same for a bf16 row (the shared expert); lane covers elements 8*lane + 256 i.
@@ -219,8 +257,8 @@ __global__ void __launch_bounds__(256) grouped_gemv_kernel(GemvArgs a) {
           bf16_row_dot<NT>(a.sh_a + (int64_t)r * a.D, in_dim, xs, stride4, nt, g);
           bf16_row_dot<NT>(a.sh_b + (int64_t)r * a.D, in_dim, xs, stride4, nt, u);
         } else {
-          q_row_dot<FMT, NT>(blob + a.off_a + r * row_bytes, in_dim, xs, stride4, nt, g);
-          q_row_dot<FMT, NT>(blob + a.off_b + r * row_bytes, in_dim, xs, stride4, nt, u);
+          q_rows_dot2<FMT, NT>(blob + a.off_a + r * row_bytes, blob + a.off_b + r * row_bytes, in_dim,
+                               xs, stride4, nt, g, u);
         }
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -234,7 +272,7 @@ __global__ void __launch_bounds__(256) grouped_gemv_kernel(GemvArgs a) {
       } else {
         float y[NT] = {};
         if (shared) bf16_row_dot<NT>(a.sh_a + (int64_t)r * a.Fs, in_dim, xs, stride4, nt, y);
-        else q_row_dot<FMT, NT>(blob + a.off_a + r * row_bytes, in_dim, xs, stride4, nt, y);
+        else q_row_dot1<FMT, NT>(blob + a.off_a + r * row_bytes, in_dim, xs, stride4, nt, y);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const float ys = warp_sum(y[t]);

@@ -76,6 +76,9 @@ PREFILL_ZIPF = replace(PREFILL, name="prefill T=4096 zipf(1.1) D=4096 E=256 k=6 
 STACK = Config("stack 43 layers T=8 D=4096 E=256 k=6 F=2048 Fs=2048", 8, 4096, 256, 6, 2048,
                2048, "bf16", "bf16", "normal", 0.02, 0.02, 0.02, 0.0, 4, layers=43)
 
+DECODE1_Q4K = replace(DECODE1, name="decode T=1 Q4_K experts D=4096 E=256 k=6 F=2048 Fs=2048",
+                      expert_fmt="q4k")
+
 ALL = [TINY, DECODE1, DECODE32_ZIPF, PREFILL, PREFILL_ZIPF, STACK]
 
 

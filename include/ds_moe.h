@@ -214,6 +214,18 @@ int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_
                  float *x, int64_t T, float eps, void *workspace, size_t workspace_bytes,
                  void *stream, char *err, size_t errlen);
 
+/* ds_moe_stack with a format per layer ("q2-q4" mixed stacks: most layers
+ * Q2_K, the last few Q4_K).  formats: host array of n_layers
+ * ds_expert_format values that replace shape->expert_format for each layer,
+ * or NULL (every layer as the shape says).  The workspace must hold
+ * ds_moe_workspace_bytes of the shape with expert_format = DS_Q2_K when any
+ * layer is Q2_K, else with DS_Q4_K.  A bad format entry returns
+ * DS_ERR_INVALID_ARG before any launch. */
+int ds_moe_stack_mixed(const ds_moe_shape *shape, const ds_moe_weights *layers,
+                       const int32_t *formats, int32_t n_layers, float *x, int64_t T, float eps,
+                       void *workspace, size_t workspace_bytes, void *stream, char *err,
+                       size_t errlen);
+
 /* ds_moe_layer for callers that cannot allocate device memory where they
  * call the layer -- for example code being captured into a CUDA graph, where
  * allocation calls are not allowed, or a plugin whose host program owns all

@@ -132,3 +132,17 @@ def test_layer_path_host_checks(L):
     q4 = ds.MoEShape(4096, 256, 2048, 2048, 6, expert_format=ds.DS_Q4_K)
     for T in (1, 4, 8, 4096):
         assert ds.layer_path(q4, T) == ds.PATH_GROUPED_GEMV
+
+
+def test_stack_mixed_rejects_bad_format_before_launch(L):
+    """The per-layer format list is checked on the host: nothing runs."""
+    sh = ds.MoEShape(4096, 256, 2048, 2048, 6).c()
+    W = (ds.Weights * 2)()
+    err = ctypes.create_string_buffer(256)
+    fm = (ctypes.c_int32 * 2)(0, 5)
+    rc = L.ds_moe_stack_mixed(ctypes.byref(sh), W, fm, 2, 256, 8, 1e-6, 256, 1 << 30, None, err, 256)
+    assert rc == ds.DS_ERR_INVALID_ARG and b"formats[1]" in err.value
+    shf = ds.MoEShape(4096, 256, 2048, 2048, 6, x_dtype=ds.DS_F32).c()
+    fm_ok = (ctypes.c_int32 * 2)(0, 1)
+    rc = L.ds_moe_stack_mixed(ctypes.byref(shf), W, fm_ok, 2, 256, 8, 1e-6, 256, 1 << 30, None, err, 256)
+    assert rc == ds.DS_ERR_INVALID_ARG

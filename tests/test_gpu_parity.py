@@ -554,3 +554,39 @@ def test_q4k_decode_b1_flash_shape():
     cfg = replace(dsgen.DECODE1, expert_fmt="q4k")
     assert ds.expert_bytes(cfg.D, cfg.F, ds.DS_Q4_K) == cfg.expert_bytes == 3 * 2048 * 16 * 144
     layer_parity(cfg, DECODE_TOL)
+
+
+def test_q4k_mixed_stack_by_layer():
+    """A mixed stack (Q2_K layers, then Q4_K layers, as in a "q2-q4" model)
+    at full width, T=8, through ds_moe_stack_mixed: each layer against the
+    oracle on the residual the GPU produced before it (as in the Q2_K stack
+    test), then the four-layer call bit-identical to one call per layer."""
+    from dataclasses import replace
+    fmts = ["q2k", "q2k", "q4k", "q4k"]
+    cfgs = [replace(dsgen.STACK, expert_fmt=f) for f in fmts]
+    codes = [ds.DS_Q4_K if f == "q4k" else ds.DS_Q2_K for f in fmts]
+    Ws = [synthetic.build_layer(c, l) for l, c in enumerate(cfgs)]
+    sh = synthetic.shape_of(cfgs[0])
+    ws = torch.empty(ds.workspace_bytes(sh, dsgen.STACK.T), dtype=torch.uint8, device="cuda")
+    x0 = torch.from_numpy(dsgen.host_x(replace(dsgen.STACK, x_dtype="f32"))).cuda()
+    x = x0.clone()
+    checked = 0
+    for l, c in enumerate(cfgs):
+        x_in = x.cpu().numpy()
+        ds.stack(sh, [Ws[l]], x, ws, formats=[codes[l]])
+        ds.sync_status()
+        got = x.cpu().numpy().astype(np.float64) - x_in
+        lo = oracle.LayerOracle(c, l)
+        r64 = oracle.as_f64(oracle.rmsnorm_bf16(x_in), "bf16")
+        res, _, _, L = lo.forward(r64)
+        keep = oracle.min_top_gap(L, c.k) >= oracle.GAP
+        ref = (x_in.astype(np.float64) + res).astype(np.float32).astype(np.float64) - x_in
+        sl = replace(sh, expert_format=codes[l])
+        tol = PREFILL_TOL if ds.layer_path(sl, c.T) == ds.PATH_TENSOR_CORE else DECODE_TOL
+        check_close(got[keep], ref[keep], tol, f"mixed stack layer {l} {fmts[l]}")
+        checked += int(keep.sum())
+    assert checked >= len(cfgs) * dsgen.STACK.T - 2
+    xa = x0.clone()
+    ds.stack(sh, Ws, xa, ws, formats=codes)
+    ds.sync_status()
+    assert torch.equal(xa, x)
