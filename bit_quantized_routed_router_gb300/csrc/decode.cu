@@ -184,8 +184,9 @@ __device__ __forceinline__ void bf16_row_dot(const uint16_t *__restrict__ row, i
                                              const float4 *__restrict__ xs, int stride4, int nt,
                                              float acc[NTOK]) {
   const int lane = threadIdx.x & 31;
+#pragma unroll 4
   for (int d = 8 * lane; d < in_dim; d += 256) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(row + d);
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row + d));
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
     float w[8];
 #pragma unroll
@@ -335,7 +336,8 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float *__restri
 
 template <int MODE, typename TX, int FMT>
 cudaError_t launch_gemv1(const GemvArgs &a, int out_rows_max, int in_dim_max, cudaStream_t s) {
-  const size_t smem = (size_t)NT * in_dim_max * sizeof(float);
+  // a block stages at most min(T, NT) tokens (no slot has more than T)
+  const size_t smem = (size_t)std::min<int64_t>(a.T, NT) * in_dim_max * sizeof(float);
   static bool attr_set = false;
   auto kern = grouped_gemv_kernel<MODE, TX, FMT>;
   if (!attr_set) {
