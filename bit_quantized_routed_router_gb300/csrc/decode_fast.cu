@@ -54,11 +54,12 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // holds in byte c the high (low) byte of X_{16 sb + 4c + i}: the byte order of
 // (codes >> 2i) & 0x03030303.  Within a plane the words are stored in the
 // order lanes read them, so every vector load is conflict-free.
-// Lane map of a row of nb blocks (nb = 2 SPL): LPB = 16 / SPL lanes per block;
-// lane l takes block l / LPB, sub-blocks SPL (l % LPB) + i, i < SPL.
-template <int SPL>
+// Lane map of a row of nb blocks of SPB sub-blocks (nb = 32 SPL / SPB):
+// LPB = SPB / SPL lanes per block; lane l takes block l / LPB, sub-blocks
+// SPL (l % LPB) + i, i < SPL.
+template <int SPL, int SPB = 16>
 struct LaneMap {
-  static constexpr int LPB = 16 / SPL;
+  static constexpr int LPB = SPB / SPL;
   static constexpr int Q = SPL < 4 ? SPL : 4;
   __device__ static __forceinline__ int off(int lane, int i) {
     return (i / Q) * (32 * Q) + lane * Q + (i % Q);
@@ -917,40 +918,247 @@ __device__ __forceinline__ float row_dot_reg(const RowPart<SPL> &r, const XReg<S
   return x.step * fmaf(d, (float)accq, -dmin * (float)accm);
 }
 
+// ------------------------------------------------------------- Q4_K rows --
+// "Understanding Dwarf Star", 2.3.2: a 144-byte block holds fp16 d and dmin,
+// twelve bytes of 6-bit sub-block scales and mins, and 128 bytes of 4-bit
+// codes; 8 sub-blocks of 32 weights.  Code word c of sub-block s (bytes
+// 16 + 16 s + 4 c) holds weights 8 c + 2 b (low nibble of byte b) and
+// 8 c + 2 b + 1 (high nibble), so (word >> 4 p) & 0x0F0F0F0F puts the codes
+// of parity p in the four bytes.  The fixed point planes of a vector follow
+// the Q2_K ones with seventeen planes per 32-weight sub-block: the high bytes
+// of X for the weights of code word c and parity p in plane 2 c + p, the low
+// bytes in plane 8 + 2 c + p, the sub-block sum of X in plane 16; then nb
+// steps.  Sums are exact integers as for Q2_K; a sub-block's scaled sum
+// (15 * 32767 * 32 * 63 at most) fits in 32 bits, a lane's total needs 64.
+
+// One block per half-warp: lane & 15 holds weights 16 (lane & 15) .. + 15 of
+// the block, i.e. half (lane & 1) of sub-block (lane & 15) / 2.
+template <int SPL>
+__device__ __forceinline__ void digitize_block4(const float v[16], int b, uint32_t *planes,
+                                               float *steps, int nsb) {
+  using M = LaneMap<SPL, 8>;
+  const int lane = threadIdx.x & 31, s = (lane & 15) >> 1, half = lane & 1;
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  int e = 0;
+  if (m > 0.f) frexpf(m, &e);  // m < 2^e
+  const float inv = m > 0.f ? ldexpf(1.0f, 15 - e) : 0.f;
+  uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};  // [2 * (local word) + parity]
+  int sx = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    int X = __float2int_rn(v[j] * inv);  // exact scaling by a power of two
+    X = max(-32767, min(32767, X));
+    sx += X;
+    const int idx = 2 * (j >> 3) + (j & 1), c = 8 * ((j & 7) >> 1);
+    hi[idx] |= ((uint32_t)(X >> 8) & 0xFFu) << c;
+    lo[idx] |= ((uint32_t)X & 0xFFu) << c;
+  }
+  sx += __shfl_xor_sync(0xffffffffu, sx, 1);  // the other half of the sub-block
+  const int lr = b * M::LPB + s / SPL;       // the lane that reads this sub-block
+  const int o = M::off(lr, s % SPL);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    planes[(4 * half + i) * nsb + o] = hi[i];
+    planes[(8 + 4 * half + i) * nsb + o] = lo[i];
+  }
+  if (half == 0) planes[16 * nsb + o] = (uint32_t)sx;
+  if ((lane & 15) == 0) steps[b] = m > 0.f ? ldexpf(1.0f, e - 15) : 0.f;
+}
+
+// This lane's parts of one Q4_K row in shared memory: the code words of its
+// SPL sub-blocks and the block header (d, dmin, the 6-bit fields).
+template <int SPL>
+struct RowPart4 {
+  uint4 codes[SPL];
+  uint4 hdr;
+};
+
+template <int SPL>
+__device__ __forceinline__ void load_row_s4(const uint8_t *row, RowPart4<SPL> &r) {
+  const int lane = threadIdx.x & 31;
+  constexpr int LPB = 8 / SPL;
+  const uint8_t *blk = row + (lane / LPB) * Q4B;
+  const int s0 = SPL * (lane % LPB);
+#pragma unroll
+  for (int i = 0; i < SPL; ++i) r.codes[i] = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * (s0 + i));
+  r.hdr = *reinterpret_cast<const uint4 *>(blk);
+}
+
+// 6-bit field i of a header: bits [6 i, 6 i + 6) of hdr.y | hdr.z << 32 | hdr.w << 64.
+__device__ __forceinline__ int q4_field(const uint4 &h, int i) {
+  const uint64_t lo = (uint64_t)h.y | ((uint64_t)h.z << 32);
+  const int p = 6 * i;
+  if (p + 6 <= 64) return (int)((lo >> p) & 63u);
+  if (p >= 64) return (int)((h.w >> (p - 64)) & 63u);
+  return (int)(((lo >> p) | ((uint64_t)h.w << (64 - p))) & 63u);
+}
+
+template <int SPL>
+struct XReg4 {
+  uint32_t hi[SPL][8], lo[SPL][8], sx[SPL];
+  float step;
+};
+
+template <int SPL>
+__device__ __forceinline__ void load_xreg4(const uint32_t *planes, const float *steps, int nsb,
+                                           XReg4<SPL> &x) {
+  using M = LaneMap<SPL, 8>;
+  constexpr int Q = M::Q;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int g = 0; g < SPL / Q; ++g) {
+    const int o = g * (32 * Q) + lane * Q;
+    uint32_t w[Q];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      lds_words<Q>(planes + i * nsb + o, w);
+#pragma unroll
+      for (int k = 0; k < Q; ++k) x.hi[g * Q + k][i] = w[k];
+      lds_words<Q>(planes + (8 + i) * nsb + o, w);
+#pragma unroll
+      for (int k = 0; k < Q; ++k) x.lo[g * Q + k][i] = w[k];
+    }
+    lds_words<Q>(planes + 16 * nsb + o, w);
+#pragma unroll
+    for (int k = 0; k < Q; ++k) x.sx[g * Q + k] = w[k];
+  }
+  x.step = steps[lane / M::LPB];
+}
+
+// sc_s * sum_j q_j X_j of one sub-block: 16 dp4a over the even and odd codes.
+__device__ __forceinline__ int q4_sub_dot(const uint4 &codes, const uint32_t hi[8], const uint32_t lo[8]) {
+  const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+  int sh = 0;
+  unsigned sl = 0u;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const uint32_t q = (cw[c] >> (4 * p)) & 0x0F0F0F0Fu;
+      sh = __dp4a((int)q, (int)hi[2 * c + p], sh);
+      sl = __dp4a(q, lo[2 * c + p], sl);
+    }
+  return sh * 256 + (int)sl;  // sum_j q_j X_j
+}
+
+// Q4_K row . activation with the activation words in registers.
+template <int SPL>
+__device__ __forceinline__ float row_dot_reg4(const RowPart4<SPL> &r, const XReg4<SPL> &x) {
+  const int lane = threadIdx.x & 31;
+  const int s0 = SPL * (lane % (8 / SPL));
+  long long accq = 0, accm = 0;
+#pragma unroll
+  for (int sub = 0; sub < SPL; ++sub) {
+    const int sc = q4_field(r.hdr, s0 + sub), mm = q4_field(r.hdr, 8 + s0 + sub);
+    accq += (long long)sc * q4_sub_dot(r.codes[sub], x.hi[sub], x.lo[sub]);
+    accm += (long long)mm * (int)x.sx[sub];
+  }
+  const float d = fp16_to_f32((uint16_t)(r.hdr.x & 0xFFFF)), dmin = fp16_to_f32((uint16_t)(r.hdr.x >> 16));
+  return x.step * fmaf(d, (float)accq, -dmin * (float)accm);
+}
+
+// The same with the activation planes read from shared memory.
+template <int SPL>
+__device__ __forceinline__ float row_dot4(const RowPart4<SPL> &r, const uint32_t *planes,
+                                          const float *steps, int nsb) {
+  XReg4<SPL> x;
+  load_xreg4<SPL>(planes, steps, nsb, x);
+  return row_dot_reg4<SPL>(r, x);
+}
+
+// Row formats of the one-token streaming kernel: bytes per block, weights
+// per sub-block, fixed point planes per sub-block, and the lane's row parts,
+// activation registers, loads and dots.
+template <int SPL>
+struct Q2Rows {
+  static constexpr int BB = QB, SUB = 16, NPL = 9;
+  using Row = RowPart<SPL>;
+  using XR = XReg<SPL>;
+  __device__ static __forceinline__ void digitize(const float v[16], int b, uint32_t *pl, float *st, int nsb) {
+    digitize_block<SPL>(v, b, pl, st, nsb);
+  }
+  __device__ static __forceinline__ void load_x(const uint32_t *pl, const float *st, int nsb, XR &x) {
+    load_xreg<SPL>(pl, st, nsb, x);
+  }
+  __device__ static __forceinline__ void load_s(const uint8_t *row, Row &r) { load_row_s<SPL>(row, r); }
+  __device__ static __forceinline__ float dot_reg(const Row &r, const XR &x) { return row_dot_reg<SPL>(r, x); }
+  __device__ static __forceinline__ float dot(const Row &r, const uint32_t *pl, const float *st, int nsb) {
+    return row_dot<SPL>(r, pl, st, nsb);
+  }
+};
+
+template <int SPL>
+struct Q4Rows {
+  static constexpr int BB = Q4B, SUB = 32, NPL = 17;
+  using Row = RowPart4<SPL>;
+  using XR = XReg4<SPL>;
+  __device__ static __forceinline__ void digitize(const float v[16], int b, uint32_t *pl, float *st, int nsb) {
+    digitize_block4<SPL>(v, b, pl, st, nsb);
+  }
+  __device__ static __forceinline__ void load_x(const uint32_t *pl, const float *st, int nsb, XR &x) {
+    load_xreg4<SPL>(pl, st, nsb, x);
+  }
+  __device__ static __forceinline__ void load_s(const uint8_t *row, Row &r) { load_row_s4<SPL>(row, r); }
+  __device__ static __forceinline__ float dot_reg(const Row &r, const XR &x) { return row_dot_reg4<SPL>(r, x); }
+  __device__ static __forceinline__ float dot(const Row &r, const uint32_t *pl, const float *st, int nsb) {
+    return row_dot4<SPL>(r, pl, st, nsb);
+  }
+};
+
 __host__ __device__ constexpr size_t s_align(size_t v) { return (v + 127) & ~(size_t)127; }
 
 __device__ __forceinline__ int tiles_of(int n, int bid, int G) { return bid < n ? (n - bid + G - 1) / G : 0; }
 
+// Row format of the streaming kernel for an expert format: block bytes,
+// weights per sub-block, planes per sub-block and the ring stage size (a
+// routed gate/up tile, S_GU rows of gate and of up, fills one stage).
+struct StreamFmt {
+  int bb, sub, npl;
+  uint32_t stage;
+};
+constexpr uint32_t S_STAGE_Q4 = 2 * S_GU * 16 * Q4B;  // 55,296 B: 12 gate + 12 up Q4_K rows of 4096
+__host__ __device__ constexpr StreamFmt stream_fmt(int fmt) {
+  return fmt == DS_Q4_K ? StreamFmt{Q4B, 32, 17, S_STAGE_Q4} : StreamFmt{QB, 16, 9, S_STAGE};
+}
+
 // Dynamic shared memory of the streaming kernel: stages, the small state,
 // then one region used as x (phase A) and as h, hs (phase B).
-size_t stream_smem(int D, int F, int Fs, int nslots) {
-  const size_t xa = 4 * (size_t)D + 4 * (9 * (size_t)(D / 16) + D / QK);
-  const size_t hb = 4 * (size_t)nslots * (9 * (F / 16) + F / QK) + 4 * (size_t)Fs;
-  return (size_t)S_NS * S_STAGE + s_align(sizeof(StreamShared)) + std::max(xa, hb);
+size_t stream_smem(int fmt, int D, int F, int Fs, int nslots) {
+  const StreamFmt f = stream_fmt(fmt);
+  const size_t xa = 4 * (size_t)D + 4 * (f.npl * (size_t)(D / f.sub) + D / QK);
+  const size_t hb = 4 * (size_t)nslots * (f.npl * (F / f.sub) + F / QK) + 4 * (size_t)Fs;
+  return (size_t)S_NS * f.stage + s_align(sizeof(StreamShared)) + std::max(xa, hb);
 }
 
 // Rows per phase-B tile: the largest of 4, 2, 1 whose shared and routed down
 // rows fit one stage.
-int stream_rows_b(int D, int F, int Fs, int nslots) {
-  const int64_t rowb_f = (int64_t)(F / QK) * QB;
+int stream_rows_b(int fmt, int D, int F, int Fs, int nslots) {
+  const StreamFmt f = stream_fmt(fmt);
+  const int64_t rowb_f = (int64_t)(F / QK) * f.bb;
   for (int rb = 4; rb >= 1; rb >>= 1)
     if (D % rb == 0 && (int64_t)rb * nslots <= S_MAXP &&
-        (int64_t)rb * (2 * (int64_t)Fs + nslots * rowb_f) <= S_STAGE)
+        (int64_t)rb * (2 * (int64_t)Fs + nslots * rowb_f) <= f.stage)
       return rb;
   return 0;
 }
 
-template <int SPL_D, int SPL_F>
+// RD, RF: the row formats (Q2Rows / Q4Rows) of n_embd-long and n_ff-long
+// rows; STG: the ring stage size.
+template <class RD, class RF, uint32_t STG>
 __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int rb) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *stages = smem;
-  StreamShared &S = *reinterpret_cast<StreamShared *>(smem + (size_t)S_NS * S_STAGE);
-  uint8_t *reg = smem + (size_t)S_NS * S_STAGE + s_align(sizeof(StreamShared));
+  StreamShared &S = *reinterpret_cast<StreamShared *>(smem + (size_t)S_NS * STG);
+  uint8_t *reg = smem + (size_t)S_NS * STG + s_align(sizeof(StreamShared));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, bid = blockIdx.x;
   const int D = a.D, F = a.F, Fs = a.Fs;
-  const int nb_d = D / QK, nsb_d = D / 16, nb_f = F / QK, nsb_f = F / 16;
-  const int rowb_d = nb_d * QB, rowb_f = nb_f * QB;
+  const int nb_d = D / QK, nsb_d = D / RD::SUB, nb_f = F / QK, nsb_f = F / RF::SUB;
+  const int rowb_d = nb_d * RD::BB, rowb_f = nb_f * RF::BB;
   const int nsa = Fs / 2;                       // shared gate/up tiles
   const int ngrp = (F + S_GU - 1) / S_GU;       // routed gate/up tiles per slot
   const int nslots = a.n_slots;
@@ -960,7 +1168,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
   const int rbid = G - 1 - bid;
   const int ns_b = tiles_of(nsa, bid, G), nr_b = tiles_of(nslots * ngrp, rbid, G);
   const int nb_b = tiles_of(nB, bid, G);                                          // and phase-B tiles
-  const int hw = 9 * nsb_f + nb_f;
+  const int hw = RF::NPL * nsb_f + nb_f;
   constexpr int NT = S_CONS * 32;               // consumer threads
   float *xraw = reinterpret_cast<float *>(reg);                    // phase A
   uint32_t *xpl = reinterpret_cast<uint32_t *>(reg + 4 * (size_t)D);
@@ -1018,7 +1226,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
     auto acquire = [&]() -> uint8_t * {
       const int st = kq % S_NS;
       if (kq >= S_NS && !s_wait(&S.empty[st], ((kq / S_NS) & 1) ^ 1, S, a.status)) return nullptr;
-      return stages + (size_t)st * S_STAGE;
+      return stages + (size_t)st * STG;
     };
     // phase A: shared tiles while the route is pending, then shared and
     // routed tiles interleaved in proportion; the order is published per
@@ -1098,19 +1306,19 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       v[j] = a.x_f32 ? __ldg((const float *)xin + e0 + j) : bf16_to_f32(__ldg((const uint16_t *)xin + e0 + j));
 #pragma unroll
     for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4 *>(xraw + e0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-    digitize_block<SPL_D>(v, blk, xpl, reinterpret_cast<float *>(xpl + 9 * nsb_d), nsb_d);
+    RD::digitize(v, blk, xpl, reinterpret_cast<float *>(xpl + RD::NPL * nsb_d), nsb_d);
   }
   named_bar(1, NT);
   int nu = 0;
   {
-    XReg<SPL_D> xr;
-    load_xreg<SPL_D>(xpl, reinterpret_cast<const float *>(xpl + 9 * nsb_d), nsb_d, xr);
+    typename RD::XR xr;
+    RD::load_x(xpl, reinterpret_cast<const float *>(xpl + RD::NPL * nsb_d), nsb_d, xr);
     bool have_route = false;
     int js = 0;
     for (int kq = 0; kq < ns_b + nr_b; ++kq) {
       const int st = kq % S_NS;
       const bool got = s_wait(&S.full[st], (kq / S_NS) & 1, S, a.status);
-      const uint8_t *src = stages + (size_t)st * S_STAGE;
+      const uint8_t *src = stages + (size_t)st * STG;
       const int td = got ? S.tile[st] : 0;
       if (td >= 0) {
         // rows in the stage: gate f, gate f+1, up f, up f+1; every consumer
@@ -1149,12 +1357,12 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       const int r = -1 - td, u = r / ngrp, g = r % ngrp;
       const int f = g * S_GU + warp;
       if (got && u < nu && f < F) {
-        RowPart<SPL_D> gp, up;
-        load_row_s<SPL_D>(src + (size_t)warp * rowb_d, gp);
-        load_row_s<SPL_D>(src + (size_t)(S_GU + warp) * rowb_d, up);
+        typename RD::Row gp, up;
+        RD::load_s(src + (size_t)warp * rowb_d, gp);
+        RD::load_s(src + (size_t)(S_GU + warp) * rowb_d, up);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[st]);
-        const float gu[2] = {row_dot_reg<SPL_D>(gp, xr), row_dot_reg<SPL_D>(up, xr)};
+        const float gu[2] = {RD::dot_reg(gp, xr), RD::dot_reg(up, xr)};
         const float tot = warp_sum_spread<2>(gu);  // lane 0: gate, lane 16: up
         const float upv = __shfl_sync(0xffffffffu, tot, 16);
         if (lane == 0) a.h[(int64_t)u * F + f] = silu(tot) * upv;
@@ -1223,7 +1431,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        digitize_block<SPL_F>(v[h], blk[h], hpl + q[h] * hw, reinterpret_cast<float *>(hpl + q[h] * hw + 9 * nsb_f), nsb_f);
+        RF::digitize(v[h], blk[h], hpl + q[h] * hw, reinterpret_cast<float *>(hpl + q[h] * hw + RF::NPL * nsb_f), nsb_f);
     }
     for (int i = threadIdx.x; i < Fs; i += NT) hsm[i] = __ldcg(a.hs + i);
   }
@@ -1239,7 +1447,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
   for (int m = 0; m < nb_b; ++m, ++kq) {
     const int st = kq % S_NS;
     const bool got = s_wait(&S.full[st], (kq / S_NS) & 1, S, a.status);
-    const uint8_t *src = stages + (size_t)st * S_STAGE;
+    const uint8_t *src = stages + (size_t)st * STG;
     float ys[4] = {0.f, 0.f, 0.f, 0.f};
     if (got) {
       for (int c = 8 * threadIdx.x; c < Fs; c += 8 * NT) {
@@ -1260,11 +1468,11 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
     const uint8_t *routed = src + (size_t)rb * 2 * Fs;
     float y[2] = {0.f, 0.f};
     if (two) {
-      RowPart<SPL_F> rp[2];
+      typename RF::Row rp[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int p = warp + h * S_CONS;
-        if (got && p < np) load_row_s<SPL_F>(routed + (size_t)p * rowb_f, rp[h]);
+        if (got && p < np) RF::load_s(routed + (size_t)p * rowb_f, rp[h]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[st]);
@@ -1273,7 +1481,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
         const int p = warp + h * S_CONS;
         if (got && p < np) {
           const uint32_t *pl = hpl + (p / rb) * hw;
-          y[h] = row_dot<SPL_F>(rp[h], pl, reinterpret_cast<const float *>(pl + 9 * nsb_f), nsb_f);
+          y[h] = RF::dot(rp[h], pl, reinterpret_cast<const float *>(pl + RF::NPL * nsb_f), nsb_f);
         }
       }
       const float v8[8] = {ys[0], ys[1], ys[2], ys[3], y[0], y[1], 0.f, 0.f};
@@ -1293,10 +1501,10 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       for (int p = warp; p < np; p += S_CONS) {
         float yy = 0.f;
         if (got) {
-          RowPart<SPL_F> rp;
-          load_row_s<SPL_F>(routed + (size_t)p * rowb_f, rp);
+          typename RF::Row rp;
+          RF::load_s(routed + (size_t)p * rowb_f, rp);
           const uint32_t *pl = hpl + (p / rb) * hw;
-          yy = row_dot<SPL_F>(rp, pl, reinterpret_cast<const float *>(pl + 9 * nsb_f), nsb_f);
+          yy = RF::dot(rp, pl, reinterpret_cast<const float *>(pl + RF::NPL * nsb_f), nsb_f);
         }
         yy = warp_sum(yy);
         if (lane == 0 && m < S_MAXT) S.yrb[m][p] = yy;
@@ -1370,7 +1578,7 @@ cudaError_t launch_all(const Args &a, const Shape &sh, cudaStream_t s) {
 
 // One token: router logits, then the streaming kernel (cooperative, so the
 // grid barrier is safe; PDL lets its prologue overlap the router grid).
-template <int SPL_D, int SPL_F>
+template <class RD, class RF, uint32_t STG>
 cudaError_t launch_stream(const Args &a, const Shape &sh, int rb, cudaStream_t s) {
   static int sms = 0;
   static bool attr = false;
@@ -1379,20 +1587,20 @@ cudaError_t launch_stream(const Args &a, const Shape &sh, int rb, cudaStream_t s
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   }
-  const size_t smem = stream_smem(a.D, a.F, a.Fs, a.n_slots);
+  const size_t smem = stream_smem(sh.fmt, a.D, a.F, a.Fs, a.n_slots);
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(stream_kernel<SPL_D, SPL_F>,
+    cudaError_t e = cudaFuncSetAttribute(stream_kernel<RD, RF, STG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
     if (e != cudaSuccess) return e;
     // the router grid runs with the streaming kernel's shared-memory split,
     // so that the SMs need no reconfiguration between the two
     for (const void *f : {(const void *)route_kernel<uint16_t, uint16_t>, (const void *)route_kernel<float, float>,
-                          (const void *)stream_kernel<SPL_D, SPL_F>})
+                          (const void *)stream_kernel<RD, RF, STG>})
       if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                     (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
         return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<SPL_D, SPL_F>, S_THREADS, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<RD, RF, STG>, S_THREADS, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     attr = true;
@@ -1415,11 +1623,11 @@ cudaError_t launch_stream(const Args &a, const Shape &sh, int rb, cudaStream_t s
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, stream_kernel<SPL_D, SPL_F>, a, rb);
+  e = cudaLaunchKernelEx(&cfg, stream_kernel<RD, RF, STG>, a, rb);
   if (e != cudaSuccess) {  // without the overlap: plain stream order
     (void)cudaGetLastError();
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, stream_kernel<SPL_D, SPL_F>, a, rb);
+    e = cudaLaunchKernelEx(&cfg, stream_kernel<RD, RF, STG>, a, rb);
   }
   return e;
 }
@@ -1431,28 +1639,36 @@ static bool fast_shape_ok(int nb_d, int nb_f) {
   return (nb_d == 16 && nb_f == 8) || (nb_d == 4 && nb_f == 4);
 }
 
-bool fused_decode_supported(const Shape &sh, int64_t T) {
-  if (sh.fmt != DS_Q2_K) return false;  // the kernels read Q2_K blocks
+// Shape conditions shared by the three-kernel chain and the streaming kernel.
+static bool fused_shape_ok(const Shape &sh, int64_t T) {
   if (T < 1 || T > 4 || (int64_t)T * sh.k > PMAXD) return false;
   if (sh.D % QK || sh.F % QK || !fast_shape_ok(sh.D / QK, sh.F / QK)) return false;
   if (sh.x_dtype != sh.router_dtype || sh.E > 1024) return false;
   // the shared partial sums [2][4][T][Fs] live in the routed-output region [T*k][D]
   if ((int64_t)8 * sh.Fs > (int64_t)sh.k * sh.D) return false;
+  return true;
+}
+
+bool fused_decode_supported(const Shape &sh, int64_t T) {
+  // Q4_K: the streaming kernel only (the three-kernel chain reads Q2_K rows)
+  if (sh.fmt == DS_Q4_K) return stream_decode_supported(sh, T);
+  if (sh.fmt != DS_Q2_K || !fused_shape_ok(sh, T)) return false;
   return k2_smem((int)T, sh.D) <= SMEM_LIMIT - 4096 && k3_smem((int)T, sh.k, sh.F, sh.Fs) <= SMEM_LIMIT - 4096;
 }
 
 bool stream_decode_supported(const Shape &sh, int64_t T) {
-  if (T != 1 || sh.k > S_MAXK || !fused_decode_supported(sh, T)) return false;
+  if (T != 1 || sh.k > S_MAXK || !fused_shape_ok(sh, T)) return false;
   const int nb_d = sh.D / QK, nb_f = sh.F / QK, nslots = std::min(sh.E, sh.k);
-  const int rb = stream_rows_b(sh.D, sh.F, sh.Fs, nslots);
+  const StreamFmt f = stream_fmt(sh.fmt);
+  const int rb = stream_rows_b(sh.fmt, sh.D, sh.F, sh.Fs, nslots);
   static int sms = 0;
   if (!sms) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   }
-  return rb > 0 && sms > 0 && stream_smem(sh.D, sh.F, sh.Fs, nslots) <= SMEM_LIMIT && nslots <= 32 &&
-         8 * (int64_t)sh.D <= S_STAGE && 2 * S_GU * (int64_t)nb_d * QB <= S_STAGE && nb_f % 4 == 0 &&
+  return rb > 0 && sms > 0 && stream_smem(sh.fmt, sh.D, sh.F, sh.Fs, nslots) <= SMEM_LIMIT && nslots <= 32 &&
+         8 * (int64_t)sh.D <= f.stage && 2 * S_GU * (int64_t)nb_d * f.bb <= f.stage && nb_f % 4 == 0 &&
          (sh.Fs / 2 + sms - 1) / sms <= S_MAXT && (sh.D / rb + sms - 1) / sms <= S_MAXT;
 }
 
@@ -1489,10 +1705,16 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
   a.n_slots = (int)std::min<int64_t>(sh.E, wk.T * sh.k);
   const int nb_d = sh.D / QK, nb_f = sh.F / QK;
   if (stream_decode_supported(sh, wk.T)) {
-    const int rb = stream_rows_b(a.D, a.F, a.Fs, a.n_slots);
-    if (nb_d == 16 && nb_f == 8) return launch_stream<8, 4>(a, sh, rb, s);
-    if (nb_d == 4 && nb_f == 4) return launch_stream<2, 2>(a, sh, rb, s);
+    const int rb = stream_rows_b(sh.fmt, a.D, a.F, a.Fs, a.n_slots);
+    if (sh.fmt == DS_Q4_K) {
+      if (nb_d == 16 && nb_f == 8) return launch_stream<Q4Rows<4>, Q4Rows<2>, S_STAGE_Q4>(a, sh, rb, s);
+      if (nb_d == 4 && nb_f == 4) return launch_stream<Q4Rows<1>, Q4Rows<1>, S_STAGE_Q4>(a, sh, rb, s);
+      return cudaErrorInvalidValue;
+    }
+    if (nb_d == 16 && nb_f == 8) return launch_stream<Q2Rows<8>, Q2Rows<4>, S_STAGE>(a, sh, rb, s);
+    if (nb_d == 4 && nb_f == 4) return launch_stream<Q2Rows<2>, Q2Rows<2>, S_STAGE>(a, sh, rb, s);
   }
+  if (sh.fmt != DS_Q2_K) return cudaErrorInvalidValue;
   if (nb_d == 16 && nb_f == 8) return launch_all<8, 4>(a, sh, s);
   if (nb_d == 4 && nb_f == 4) return launch_all<2, 2>(a, sh, s);
   return cudaErrorInvalidValue;

@@ -128,9 +128,11 @@ def test_layer_path_host_checks(L):
         ds.layer_path(ds.MoEShape(4000, 256, 2048, 2048, 6), 4)
     with pytest.raises(ds.DsMoeError):
         ds.layer_path(sh, -1)
-    # Q4_K experts: the grouped GEMV path at every batch size
+    # Q4_K experts: the streaming kernel for one token where a device can
+    # run it, the grouped GEMV path otherwise and at every other batch size
     q4 = ds.MoEShape(4096, 256, 2048, 2048, 6, expert_format=ds.DS_Q4_K)
-    for T in (1, 4, 8, 4096):
+    assert ds.layer_path(q4, 1) == (ds.PATH_STREAM if torch.cuda.is_available() else ds.PATH_GROUPED_GEMV)
+    for T in (2, 4, 8, 4096):
         assert ds.layer_path(q4, T) == ds.PATH_GROUPED_GEMV
 
 

@@ -534,12 +534,17 @@ def test_q4k_dequantize_bit_exact():
         assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("T,Fs,k,E,dtype", [(8, 0, 2, 16, "f32"), (1, 512, 6, 16, "bf16"),
-                                            (3, 256, 2, 16, "f32"), (33, 1024, 4, 40, "bf16")])
-def test_q4k_layer_parity(T, Fs, k, E, dtype):
+@pytest.mark.parametrize("T,Fs,k,E,dtype,D", [(8, 0, 2, 16, "f32", 1024), (1, 512, 6, 16, "bf16", 1024),
+                                              (1, 0, 8, 16, "f32", 1024), (1, 256, 2, 16, "f32", 512),
+                                              (3, 256, 2, 16, "f32", 1024), (33, 1024, 4, 40, "bf16", 1024)])
+def test_q4k_layer_parity(T, Fs, k, E, dtype, D):
+    """One token at the instantiated widths runs the streaming kernel with
+    Q4_K rows (integer dots on 4-bit codes); other widths and batches the
+    grouped GEMV path."""
     from dataclasses import replace
-    cfg = replace(_small(T, Fs, k, E, dtype), expert_fmt="q4k")
-    assert ds.layer_path(synthetic.shape_of(cfg), T) == ds.PATH_GROUPED_GEMV
+    cfg = replace(_small(T, Fs, k, E, dtype), expert_fmt="q4k", D=D, F=D)
+    path = ds.PATH_STREAM if (T == 1 and D == 1024) else ds.PATH_GROUPED_GEMV
+    assert ds.layer_path(synthetic.shape_of(cfg), T) == path
     layer_parity(cfg, DECODE_TOL)
 
 
@@ -549,11 +554,44 @@ def test_q4k_tiny_ragged_width():
     layer_parity(replace(dsgen.TINY, expert_fmt="q4k"), DECODE_TOL)
 
 
-def test_q4k_decode_b1_flash_shape():
+@pytest.fixture(scope="module")
+def decode1_q4k():
     from dataclasses import replace
     cfg = replace(dsgen.DECODE1, expert_fmt="q4k")
+    return cfg, synthetic.build_layer(cfg)
+
+
+def test_q4k_decode_b1_flash_shape(decode1_q4k):
+    cfg, W = decode1_q4k
     assert ds.expert_bytes(cfg.D, cfg.F, ds.DS_Q4_K) == cfg.expert_bytes == 3 * 2048 * 16 * 144
-    layer_parity(cfg, DECODE_TOL)
+    assert ds.layer_path(synthetic.shape_of(cfg), 1) == ds.PATH_STREAM
+    layer_parity(cfg, DECODE_TOL, W=W)
+
+
+def test_q4k_decode_b1_hostio_and_gemv_agree(decode1_q4k):
+    """The one-token Q4_K layer from pinned host buffers equals the device
+    call bit for bit; the grouped GEMV path (a two-token batch of the same
+    token twice) agrees within the decode tolerance."""
+    cfg, W = decode1_q4k
+    lo, att, x64 = oracle_case(cfg)
+    sh = synthetic.shape_of(cfg)
+    x = synthetic.build_x(cfg, att)
+    ws = torch.empty(ds.workspace_bytes(sh, 2), dtype=torch.uint8, device="cuda")
+    out = torch.empty((1, cfg.D), dtype=torch.float32, device="cuda")
+    ds.layer(sh, W, x, out, ws)
+    xh = x.cpu().pin_memory()
+    oh = torch.empty((1, cfg.D), dtype=torch.float32).pin_memory()
+    ds.layer_hostio(sh, W, xh, oh, ws)
+    ds.sync_status()
+    assert torch.equal(oh, out.cpu())
+    x2 = torch.cat([x, x])
+    out2 = torch.empty((2, cfg.D), dtype=torch.float32, device="cuda")
+    assert ds.layer_path(sh, 2) == ds.PATH_GROUPED_GEMV
+    ds.layer(sh, W, x2, out2, ws)
+    ds.sync_status()
+    assert torch.equal(out2[0], out2[1])
+    ref = out2[0].cpu().numpy().astype(np.float64)
+    check_close(out.cpu().numpy()[0], ref, DECODE_TOL, "stream vs GEMV")
 
 
 def test_q4k_mixed_stack_by_layer():
