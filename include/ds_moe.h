@@ -186,8 +186,9 @@ int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, 
  * (dequantised weights and activations rounded once to fp16; an |x| or
  * intermediate above 65504 is saturated and reported by ds_moe_sync_status
  * as DS_ERR_DEVICE_CHECK); every other case uses the grouped dequantising
- * GEMV path with fp32 arithmetic.  Q4_K experts use the grouped GEMV path
- * at every T. */
+ * GEMV path with fp32 arithmetic.  With Q4_K experts one token at the
+ * streaming kernel's widths (top_k <= 8) runs that kernel, every other batch
+ * the grouped GEMV path. */
 int ds_moe_layer(const ds_moe_shape *shape, const ds_moe_weights *weights, const void *x, int64_t T,
                  float *out, void *workspace, size_t workspace_bytes, const ds_moe_debug *dbg,
                  void *stream, char *err, size_t errlen);
