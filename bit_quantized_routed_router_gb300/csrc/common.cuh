@@ -44,6 +44,17 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
+// 6-bit field i of a Q4_K block header h (its first 16 bytes: fp16 d and
+// dmin, then the fields as one 96-bit little-endian integer, field i in bits
+// [6 i, 6 i + 6); fields 0..7 are the sub-block scales, 8..15 the mins).
+__device__ __forceinline__ int q4k_field(const uint4 &h, int i) {
+  const uint64_t lo = (uint64_t)h.y | ((uint64_t)h.z << 32);
+  const int p = 6 * i;
+  if (p + 6 <= 64) return (int)((lo >> p) & 63u);
+  if (p >= 64) return (int)((h.w >> (p - 64)) & 63u);
+  return (int)(((lo >> p) | ((uint64_t)h.w << (64 - p))) & 63u);
+}
+
 // fp32 -> unsigned key with the same order (for non-NaN values), and back.
 __device__ __forceinline__ uint32_t ord_key(float f) {
   const uint32_t b = __float_as_uint(f);

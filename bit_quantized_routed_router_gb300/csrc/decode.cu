@@ -109,13 +109,7 @@ __device__ __forceinline__ void q4k_rows_dot(const uint8_t *const *rows, int in_
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      // the 96-bit field integer = hdr.y | hdr.z << 32 | hdr.w << 64
-      const uint64_t f_lo = (uint64_t)hdr[r].y | ((uint64_t)hdr[r].z << 32);
-      const int sc = (int)((f_lo >> (6 * s)) & 63u);
-      const int pm = 48 + 6 * s;  // min field 8 + s
-      const int mm = pm + 6 <= 64 ? (int)((f_lo >> pm) & 63u)
-                     : pm >= 64   ? (int)((hdr[r].w >> (pm - 64)) & 63u)
-                                  : (int)(((f_lo >> pm) | ((uint64_t)hdr[r].w << (64 - pm))) & 63u);
+      const int sc = q4k_field(hdr[r], s), mm = q4k_field(hdr[r], 8 + s);
       const float dsc = fp16_to_f32((uint16_t)(hdr[r].x & 0xFFFF)) * (float)sc;
       const float dmm = fp16_to_f32((uint16_t)(hdr[r].x >> 16)) * (float)mm;
 #pragma unroll

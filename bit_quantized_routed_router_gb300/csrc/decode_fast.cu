@@ -988,15 +988,6 @@ __device__ __forceinline__ void load_row_s4(const uint8_t *row, RowPart4<SPL> &r
   r.hdr = *reinterpret_cast<const uint4 *>(blk);
 }
 
-// 6-bit field i of a header: bits [6 i, 6 i + 6) of hdr.y | hdr.z << 32 | hdr.w << 64.
-__device__ __forceinline__ int q4_field(const uint4 &h, int i) {
-  const uint64_t lo = (uint64_t)h.y | ((uint64_t)h.z << 32);
-  const int p = 6 * i;
-  if (p + 6 <= 64) return (int)((lo >> p) & 63u);
-  if (p >= 64) return (int)((h.w >> (p - 64)) & 63u);
-  return (int)(((lo >> p) | ((uint64_t)h.w << (64 - p))) & 63u);
-}
-
 template <int SPL>
 struct XReg4 {
   uint32_t hi[SPL][8], lo[SPL][8], sx[SPL];
@@ -1053,7 +1044,7 @@ __device__ __forceinline__ float row_dot_reg4(const RowPart4<SPL> &r, const XReg
   long long accq = 0, accm = 0;
 #pragma unroll
   for (int sub = 0; sub < SPL; ++sub) {
-    const int sc = q4_field(r.hdr, s0 + sub), mm = q4_field(r.hdr, 8 + s0 + sub);
+    const int sc = q4k_field(r.hdr, s0 + sub), mm = q4k_field(r.hdr, 8 + s0 + sub);
     accq += (long long)sc * q4_sub_dot(r.codes[sub], x.hi[sub], x.lo[sub]);
     accm += (long long)mm * (int)x.sx[sub];
   }

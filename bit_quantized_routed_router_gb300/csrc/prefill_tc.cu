@@ -46,7 +46,8 @@ constexpr int TC_NGU = 128;                // tokens per gate/up tile at most
 constexpr int TC_NDN = 128;                // tokens per down tile at most
 constexpr int TC_NRT = 256;                // tokens per router tile at most
 constexpr uint32_t TC_TILE_BYTES = TC_BM * 128;       // one 128 x 64 operand tile (16 KB)
-constexpr uint32_t TC_RAW_ROW = 96;        // bytes copied per weight row and 256-weight block
+constexpr uint32_t TC_RAW_ROW = 96;        // bytes copied per weight row and 256-weight block (Q2_K)
+constexpr uint32_t TC_RAW_ROW_Q4 = Q4B;    // Q4_K: the 144-byte block itself (16-byte aligned)
 constexpr int TC_MAX_STAGES = 5, TC_MAX_RAW = 3;
 constexpr int TC_TILE_CACHE = 128;         // a block's first tiles, copied to shared memory
 constexpr int TC_EPI = 4, TC_DQ = 8;       // epilogue and dequant warps
@@ -66,16 +67,19 @@ struct TcTile {
 enum { MODE_GU = 0, MODE_DN = 1, MODE_ROUTER = 2 };
 
 // Pipeline shape per contraction: a stage holds A_TILES weight tiles (gate
-// and up, or one) and a token tile of NMAX rows; RAW slots of raw Q2_K
-// blocks (one per 256-wide K block) feed the dequant warps.
-template <int MODE>
+// and up, or one) and a token tile of NMAX rows; RAW slots of raw blocks
+// (one per 256-wide K block) feed the dequant warps.  Q4_K blocks are 144
+// bytes: two raw slots (one block ahead) keep the pipeline within the
+// shared memory of a block.
+template <int MODE, int FMT = DS_Q2_K>
 struct TcCfg {
   static constexpr int A_TILES = MODE == MODE_ROUTER ? 1 : 2;  // gate + up, or two 128-row down blocks
   static constexpr int NMAX = MODE == MODE_GU ? TC_NGU : MODE == MODE_DN ? TC_NDN : TC_NRT;
   static constexpr int STAGES = MODE == MODE_ROUTER ? 4 : 3;
-  static constexpr int RAW = MODE == MODE_ROUTER ? 1 : 3;
+  static constexpr int RAW = MODE == MODE_ROUTER ? 1 : FMT == DS_Q4_K ? 2 : 3;
+  static constexpr uint32_t RAW_ROW = FMT == DS_Q4_K ? TC_RAW_ROW_Q4 : TC_RAW_ROW;
   static constexpr uint32_t STAGE_BYTES = (A_TILES + NMAX / 128) * TC_TILE_BYTES;
-  static constexpr uint32_t RAW_BYTES = A_TILES * TC_BM * TC_RAW_ROW;
+  static constexpr uint32_t RAW_BYTES = A_TILES * TC_BM * RAW_ROW;
 };
 
 struct TcArgs {
@@ -256,11 +260,45 @@ __device__ __forceinline__ void dequant_codes(uint32_t codes, uint32_t scm, floa
   c1 = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// One Q4_K sub-block (32 weights: code words cw[0..3], weight 8 c + 2 b in
+// the low nibble of byte b of word c, 8 c + 2 b + 1 in the high nibble) as
+// two 16-groups of fp16 in the permuted K order (position p of a group holds
+// index 4 (p mod 4) + p / 4): four 16-byte chunks.  Each weight is the exact
+// fp32 value q * (d sc) - dmin m (one rounding: both products are exact)
+// rounded to fp16; q becomes a float through the exponent of 2^23 (exact).
+// Sixteen levels do not fit the Q2_K byte permutation, which selects among
+// four fp16 values.
+__device__ __forceinline__ float q4_code_f(uint32_t cw, int shift) {
+  return __uint_as_float(((cw >> shift) & 0xFu) | 0x4B000000u) - 8388608.0f;
+}
+
+__device__ __forceinline__ void dequant_q4_sub(const uint4 codes, float dsc, float dmm, uint4 out[4]) {
+  const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // 16-group: weights 16 h .. 16 h + 15
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // positions 2 i, 2 i + 1
+      float v[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int pp = 2 * i + t, k = 4 * (pp & 3) + (pp >> 2);  // index within the group
+        const int w = 16 * h + k;                                   // weight within the sub-block
+        v[t] = fmaf(q4_code_f(cw[w >> 3], 8 * ((w & 7) >> 1) + 4 * (w & 1)), dsc, -dmm);
+      }
+      const __half2 hv = __floats2half2_rn(v[0], v[1]);
+      o[i] = *reinterpret_cast<const uint32_t *>(&hv);
+    }
+    out[2 * h] = make_uint4(o[0], o[1], o[2], o[3]);
+    out[2 * h + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // Operand tiles are 128 rows x 64 K-elements in the 128-byte swizzle of the
 // MMA descriptors: 16-byte chunk c (K elements 8c..8c+7) of row r sits at
 // byte r * 128 + ((c ^ (r mod 8)) * 16) of the 1024-byte aligned tile.
 
-template <int MODE>
+template <int MODE, int FMT = DS_Q2_K>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tm_raw,
                    const __grid_constant__ CUtensorMap tm_b_r32, const __grid_constant__ CUtensorMap tm_b_r64,
@@ -272,7 +310,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // derived from the array itself so that accesses stay shared-memory ones
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *stages = smem;
-  using C = TcCfg<MODE>;
+  using C = TcCfg<MODE, FMT>;
   constexpr int TC_STAGES = C::STAGES, TC_RAW_SLOTS = C::RAW;
   constexpr uint32_t TC_STAGE_BYTES = C::STAGE_BYTES, TC_RAW_BYTES = C::RAW_BYTES;
   uint8_t *raw = smem + TC_STAGES * TC_STAGE_BYTES;
@@ -320,9 +358,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (warp == TC_TMA_WARP) {
     // -------------------------------------------------- copies (one warp) --
-    // Raw Q2_K blocks (one 96-byte copy per weight row and 256-wide K block)
-    // of the routed tiles run ahead of the stages: when the stages of the
-    // routed block c begin, blocks up to c + 2 are issued.  (ri, rkb) walks
+    // Raw blocks (one copy per weight row and 256-wide K block: a 96-byte
+    // window holding the Q2_K block, or the 144-byte Q4_K block) of the
+    // routed tiles run ahead of the stages: when the stages of the routed
+    // block c begin, blocks up to c + RAW - 1 are issued.  (ri, rkb) walks
     // the routed blocks in the order the dequant warps consume them.
     if (lane == 0) {  // descriptors into the TMA unit's cache before the first copies
       const CUtensorMap *maps[8] = {&tm_raw, &tm_b_r32, &tm_b_r64, &tm_b_r96, &tm_b_routed, &tm_b_shared, &tm_a0, &tm_a1};
@@ -350,13 +389,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (lane == 0) {
         // words [x, x + 24) of 128 weight rows: the 96-byte window, 16-byte
         // aligned, that holds block rkb of each row
-        mbar_arrive_expect_tx(&S.raw_full[slot], rows * TC_RAW_ROW);
-        const int xw = (int)(((uint32_t)(QB * rkb) & ~15u) >> 2);
+        mbar_arrive_expect_tx(&S.raw_full[slot], rows * C::RAW_ROW);
+        const int xw = FMT == DS_Q4_K ? (int)((uint32_t)(Q4B * rkb) >> 2) : (int)(((uint32_t)(QB * rkb) & ~15u) >> 2);
         uint8_t *dst = raw + (size_t)slot * TC_RAW_BYTES;
         // gate/up: rows blk*128 of gate and of up; down: rows blk*256 and blk*256 + 128
         const int y0 = GU ? t.blk * TC_BM : 2 * t.blk * TC_BM;
         tma_load_3d(dst, &tm_raw, xw, y0, t.e, &S.raw_full[slot]);
-        tma_load_3d(dst + TC_BM * TC_RAW_ROW, &tm_raw, xw, GU ? a.F + y0 : y0 + TC_BM, t.e, &S.raw_full[slot]);
+        tma_load_3d(dst + TC_BM * C::RAW_ROW, &tm_raw, xw, GU ? a.F + y0 : y0 + TC_BM, t.e, &S.raw_full[slot]);
       }
       __syncwarp();
       ++rawq;
@@ -370,7 +409,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int kc = 0; ok && kc < nk; ++kc) {
         if (routed && (kc & 3) == 0) {
           ++rawpos;
-          while (rawq < rawpos + 2) {
+          while (rawq < rawpos + TC_RAW_SLOTS - 1) {
             const int r = issue_raw();
             if (r < 0) ok = false;
             if (r <= 0) break;
@@ -434,7 +473,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int dt = threadIdx.x - TC_DQ0 * 32;  // 0 .. 255
     const int r = dt;
     const int jb = 0;
-    const uint32_t raw_row = (uint32_t)r * TC_RAW_ROW;
+    const uint32_t raw_row = (uint32_t)r * C::RAW_ROW;
     const uint32_t dst_row = (uint32_t)((r / TC_BM) * TC_TILE_BYTES + (r % TC_BM) * 128);
     const int x7 = r & 7;
     int st_it = 0, raw_it = 0;
@@ -454,7 +493,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           ok = false;
           break;
         }
-        if (routed) {
+        if (routed && FMT == DS_Q4_K) {
+          // sub-blocks 2 q4 and 2 q4 + 1 of the block: eight chunks of the row
+          uint8_t *dst = stages + (size_t)s * TC_STAGE_BYTES + dst_row;
+          const uint8_t *blk = raw + (size_t)slot * TC_RAW_BYTES + raw_row;
+          const int q4 = kc & 3;
+          const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+          const float d = fp16_to_f32((uint16_t)(hdr.x & 0xFFFFu)), dmin = fp16_to_f32((uint16_t)(hdr.x >> 16));
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int sb = 2 * q4 + j;
+            const float dsc = d * (float)q4k_field(hdr, sb), dmm = dmin * (float)q4k_field(hdr, 8 + sb);  // exact
+            uint4 c4[4];
+            dequant_q4_sub(*reinterpret_cast<const uint4 *>(blk + 16 + 16 * sb), dsc, dmm, c4);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(dst + (((4 * j + c) ^ x7) << 4)) = c4[c];
+          }
+          fence_proxy_async();
+        } else if (routed) {
           uint8_t *dst = stages + (size_t)s * TC_STAGE_BYTES + dst_row;
           // the block's bytes start (84 kb) mod 16 into its 96-byte copy
           const uint8_t *blk = raw + (size_t)slot * TC_RAW_BYTES + raw_row + ((uint32_t)(QB * (kc >> 2)) & 15u);
@@ -751,25 +807,26 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int 
 // a row, y = row (gate rows then up rows, or down rows), z = expert; boxes
 // of 24 words x 128 rows.
 bool make_raw_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int64_t E,
-                  int64_t expert_bytes) {
+                  int64_t expert_bytes, uint32_t raw_row) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)rows, (cuuint64_t)E};
   const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_bytes};
-  const cuuint32_t box[3] = {TC_RAW_ROW / 4, (cuuint32_t)TC_BM, 1};
+  const cuuint32_t box[3] = {raw_row / 4, (cuuint32_t)TC_BM, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, int FMT = DS_Q2_K>
 constexpr size_t tc_smem() {
-  return 1024 + TcCfg<MODE>::STAGES * TcCfg<MODE>::STAGE_BYTES + TcCfg<MODE>::RAW * TcCfg<MODE>::RAW_BYTES +
-         sizeof(TcShared);
+  using C = TcCfg<MODE, FMT>;
+  return 1024 + C::STAGES * C::STAGE_BYTES + C::RAW * C::RAW_BYTES + sizeof(TcShared);
 }
 static_assert(tc_smem<MODE_GU>() <= 227 * 1024 && tc_smem<MODE_DN>() <= 227 * 1024 &&
-                  tc_smem<MODE_ROUTER>() <= 227 * 1024,
+                  tc_smem<MODE_ROUTER>() <= 227 * 1024 && tc_smem<MODE_GU, DS_Q4_K>() <= 227 * 1024 &&
+                  tc_smem<MODE_DN, DS_Q4_K>() <= 227 * 1024,
               "pipeline exceeds the shared memory of a block");
 static_assert(TcCfg<MODE_DN>::STAGES <= TC_MAX_STAGES && TcCfg<MODE_GU>::RAW <= TC_MAX_RAW, "barrier arrays");
 
@@ -806,7 +863,10 @@ cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const voi
 }
 
 bool prefill_tc_supported(const Shape &sh, int64_t T) {
-  if (sh.fmt != DS_Q2_K) return false;  // the dequantising warps read Q2_K blocks
+  // Q4_K tiles (tc_gemm_kernel<MODE, DS_Q4_K>) are compiled but have not
+  // yet been checked against the oracle on a GPU: Q4_K batches keep the
+  // grouped GEMV path until they are
+  if (sh.fmt != DS_Q2_K) return false;
   if (T < TC_MIN_T || T > (int64_t)1 << 24) return false;
   if (sh.x_dtype != DS_BF16 || sh.router_dtype != DS_BF16) return false;
   if (sh.D % 1024 || sh.F % 1024 || sh.Fs % TC_BM) return false;  // whole 4-block groups: raw copies stay inside rows
@@ -841,10 +901,19 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_DN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_DN>());
     if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_GU, DS_Q4_K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tc_smem<MODE_GU, DS_Q4_K>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_DN, DS_Q4_K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tc_smem<MODE_DN, DS_Q4_K>());
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_ROUTER>());
     if (e != cudaSuccess) return e;
     attr = true;
   }
+  const bool q4 = sh.fmt == DS_Q4_K;
+  const int64_t bb = sh.block_bytes();
+  const uint32_t raw_row = q4 ? TC_RAW_ROW_Q4 : TC_RAW_ROW;
   // workspace carve-up (see prefill_tc_workspace)
   const int64_t n_gu = ((T + TC_NGU - 1) / TC_NGU) * (sh.Fs / TC_BM) + (P / TC_NGU + sh.E) * (sh.F / TC_BM);
   const int64_t n_dn = ((T + TC_NDN - 1) / TC_NDN) * (sh.D / TC_BM) + (P / TC_NDN + sh.E) * (sh.D / TC_BM);
@@ -894,9 +963,9 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
       !make_map(&m_sd, sd16, sh.D, fs1, TC_BM, false))
     return cudaErrorInvalidValue;
   CUtensorMap m_rgu, m_rdn;
-  if (!make_raw_map(&m_rgu, W.experts, (int64_t)(sh.D / QK) * QB, 2 * (int64_t)sh.F, sh.E, sh.expert_bytes()) ||
-      !make_raw_map(&m_rdn, W.experts + 2 * sh.gate_bytes(), (int64_t)(sh.F / QK) * QB, sh.D, sh.E,
-                    sh.expert_bytes()))
+  if (!make_raw_map(&m_rgu, W.experts, (int64_t)(sh.D / QK) * bb, 2 * (int64_t)sh.F, sh.E, sh.expert_bytes(), raw_row) ||
+      !make_raw_map(&m_rdn, W.experts + 2 * sh.gate_bytes(), (int64_t)(sh.F / QK) * bb, sh.D, sh.E,
+                    sh.expert_bytes(), raw_row))
     return cudaErrorInvalidValue;
   a.tiles = tiles_gu;
   a.n_tiles = cnt;
@@ -905,8 +974,12 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
   if (!make_map(&m_xp32, xp, P, sh.D, 32, false) || !make_map(&m_xp64, xp, P, sh.D, 64, false) ||
       !make_map(&m_xp96, xp, P, sh.D, 96, false))
     return cudaErrorInvalidValue;
-  tc_gemm_kernel<MODE_GU><<<sms, TC_THREADS, tc_smem<MODE_GU>(), s>>>(a, m_rgu, m_xp32, m_xp64, m_xp96, m_xp, m_x, m_sg,
-                                                                      m_su);
+  if (q4)
+    tc_gemm_kernel<MODE_GU, DS_Q4_K><<<sms, TC_THREADS, tc_smem<MODE_GU, DS_Q4_K>(), s>>>(
+        a, m_rgu, m_xp32, m_xp64, m_xp96, m_xp, m_x, m_sg, m_su);
+  else
+    tc_gemm_kernel<MODE_GU><<<sms, TC_THREADS, tc_smem<MODE_GU>(), s>>>(a, m_rgu, m_xp32, m_xp64, m_xp96, m_xp, m_x, m_sg,
+                                                                        m_su);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the shared rows of h have n_ff_shared columns: their own map
   CUtensorMap m_hs;
@@ -917,8 +990,12 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
   if (!make_map(&m_h32, h16, P, sh.F, 32, false) || !make_map(&m_h64, h16, P, sh.F, 64, false) ||
       !make_map(&m_h96, h16, P, sh.F, 96, false))
     return cudaErrorInvalidValue;
-  tc_gemm_kernel<MODE_DN><<<sms, TC_THREADS, tc_smem<MODE_DN>(), s>>>(a, m_rdn, m_h32, m_h64, m_h96, m_h, m_hs, m_sd,
-                                                                      m_sd);
+  if (q4)
+    tc_gemm_kernel<MODE_DN, DS_Q4_K><<<sms, TC_THREADS, tc_smem<MODE_DN, DS_Q4_K>(), s>>>(
+        a, m_rdn, m_h32, m_h64, m_h96, m_h, m_hs, m_sd, m_sd);
+  else
+    tc_gemm_kernel<MODE_DN><<<sms, TC_THREADS, tc_smem<MODE_DN>(), s>>>(a, m_rdn, m_h32, m_h64, m_h96, m_h, m_hs, m_sd,
+                                                                        m_sd);
   return cudaGetLastError();
 }
 

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(256) quantize_q4k_kernel(const float *__restri
 }
 
 // Sub-block scale (s < 8) or min (s >= 8) of a Q4_K block.
-__device__ __forceinline__ int q4k_field(const uint8_t *blk, int i) {
+__device__ __forceinline__ int q4k_field_bytes(const uint8_t *blk, int i) {
   const int p = 6 * i;
   const uint32_t lo = blk[4 + (p >> 3)], hi = (p >> 3) + 5 < 16 ? blk[5 + (p >> 3)] : 0u;
   return (int)(((lo | (hi << 8)) >> (p & 7)) & 63u);
@@ -229,7 +229,7 @@ __global__ void dequantize_q4k_kernel(const uint8_t *__restrict__ q, int64_t row
     const int j = (int)(c % QK), s = j >> 5;
     const float d = fp16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
     const float dmin = fp16_to_f32((uint16_t)(blk[2] | (blk[3] << 8)));
-    const int sc = q4k_field(blk, s), m = q4k_field(blk, 8 + s);
+    const int sc = q4k_field_bytes(blk, s), m = q4k_field_bytes(blk, 8 + s);
     const int code = (blk[16 + (j >> 1)] >> (4 * (j & 1))) & 15;
     out[i] = __fmaf_rn(__fmul_rn(d, (float)sc), (float)code, -__fmul_rn(dmin, (float)m));
   }
