@@ -500,7 +500,9 @@ __device__ __forceinline__ RouteCache load_route(const Args &a) {
 
 // ===================================================================== K2 ==
 
-template <int SPL>
+// R: the row format of the n_embd-long rows (Q2Rows / Q4Rows, defined with
+// the streaming kernel below; a template, so resolved at instantiation).
+template <class R>
 __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
   pdl_trigger();  // every CTA of this grid is resident: the down kernel may queue
   extern __shared__ __align__(16) uint32_t xpl[];  // [T] planes + steps
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
   __shared__ float s_w[32];
   __shared__ volatile int s_ready;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = a.D / QK, nsb = a.D / 16, xw = 9 * nsb + nb;
+  const int nb = a.D / QK, nsb = a.D / R::SUB, xw = R::NPL * nsb + nb;
   if (threadIdx.x == 0) s_ready = 0;
   for (int u = warp; u < (a.T * nb + 1) / 2; u += NW2) {
     const int bi = min(2 * u + (lane >> 4), a.T * nb - 1);
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       v[j] = a.x_f32 ? __ldg((const float *)a.x + e0 + j) : bf16_to_f32(__ldg((const uint16_t *)a.x + e0 + j));
-    digitize_block<SPL>(v, b, xpl + t * xw, reinterpret_cast<float *>(xpl + t * xw + 9 * nsb), nsb);
+    R::digitize(v, b, xpl + t * xw, reinterpret_cast<float *>(xpl + t * xw + R::NPL * nsb), nsb);
   }
   __syncthreads();
   if (warp == 0) {
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
   const int n_sh = a.Fs > 0 ? 4 * a.Fs : 0;    // shared items: (row, quarter of n_embd)
   const int n_items = n_sh + a.n_slots * a.F;  // then one per routed (slot, row)
   const int gw = warp * gridDim.x + blockIdx.x, nwork = gridDim.x * NW2;
-  const int rb = nb * QB;
+  const int rb = nb * R::BB;
   bool have_route = false;
   RouteCache rc{0, 0, 0, 0, 0, 0.f, 0};
   // L2 prefetch (bulk-copy engine, lane 0) of item i's bytes; every lane calls
@@ -610,14 +612,14 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
     if (slot >= rc.nu) continue;
     const int e = shfl(rc.used, slot), base = shfl(rc.base, slot), n = shfl(rc.cnt, slot);
     const uint8_t *grow = a.experts + (int64_t)e * a.expert_bytes + (int64_t)f * rb;
-    RowPart<SPL> gp, up;
-    load_row<SPL>(grow, gp);
-    load_row<SPL>(grow + a.gate_bytes, up);
+    typename R::Row gp, up;
+    R::load_g(grow, gp);
+    R::load_g(grow + a.gate_bytes, up);
     for (int j = 0; j < n; ++j) {
       const int t = shfl(rc.perm, base + j) / a.k;
       const uint32_t *pl = xpl + t * xw;
-      const float *st = reinterpret_cast<const float *>(pl + 9 * nsb);
-      float gu[2] = {row_dot<SPL>(gp, pl, st, nsb), row_dot<SPL>(up, pl, st, nsb)};
+      const float *st = reinterpret_cast<const float *>(pl + R::NPL * nsb);
+      float gu[2] = {R::dot(gp, pl, st, nsb), R::dot(up, pl, st, nsb)};
       warp_sum_n<2>(gu);
       if (lane == 0) a.h[(int64_t)(base + j) * a.F + f] = silu(gu[0]) * gu[1];
     }
@@ -626,12 +628,13 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
 
 // ===================================================================== K3 ==
 
-template <int SPL>
+// R: the row format of the n_ff-long rows.
+template <class R>
 __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
   pdl_wait();  // gate/up (and through it the route) complete and visible
   extern __shared__ __align__(16) uint32_t hpl[];  // [P] planes + steps, then hs [T][Fs]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = a.F / QK, nsb = a.F / 16, hw = 9 * nsb + nb;
+  const int nb = a.F / QK, nsb = a.F / R::SUB, hw = R::NPL * nsb + nb;
   const int P = a.T * a.k;
   float *hs = reinterpret_cast<float *>(hpl + P * hw);
   const RouteCache rc = load_route(a);
@@ -646,7 +649,7 @@ __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
       const float4 f4 = __ldcg(src + j);
       v[4 * j] = f4.x; v[4 * j + 1] = f4.y; v[4 * j + 2] = f4.z; v[4 * j + 3] = f4.w;
     }
-    digitize_block<SPL>(v, b, hpl + q * hw, reinterpret_cast<float *>(hpl + q * hw + 9 * nsb), nsb);
+    R::digitize(v, b, hpl + q * hw, reinterpret_cast<float *>(hpl + q * hw + R::NPL * nsb), nsb);
   }
   {
     // shared activations: hs = SiLU(sum of gate quarters) * (sum of up quarters),
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
   __syncthreads();
 
   const int gw = warp * gridDim.x + blockIdx.x, nwork = gridDim.x * NW3;
-  const int er = nb * QB;
+  const int er = nb * R::BB;
   // L2 prefetch of output row d's bytes: shared down row and every used expert's row
   auto prefetch = [&](int d) {
     if (d >= a.D) return;
@@ -712,12 +715,12 @@ __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
     float yreg = 0.f;  // lane p: y of pair p at this row
     constexpr int BATCH = 6;
     for (int u0 = 0; u0 < rc.nu; u0 += BATCH) {
-      RowPart<SPL> rp[BATCH];
+      typename R::Row rp[BATCH];
 #pragma unroll
       for (int v = 0; v < BATCH; ++v) {
         const int e = shfl(rc.used, min(u0 + v, 31));
         if (u0 + v < rc.nu)
-          load_row<SPL>(a.experts + (int64_t)e * a.expert_bytes + 2 * a.gate_bytes + (int64_t)d * er, rp[v]);
+          R::load_g(a.experts + (int64_t)e * a.expert_bytes + 2 * a.gate_bytes + (int64_t)d * er, rp[v]);
       }
       for (int j = 0; j < a.T; ++j) {  // j-th pair of every expert of the batch
         float y[BATCH];
@@ -727,7 +730,7 @@ __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
           y[v] = 0.f;
           if (u0 + v < rc.nu && j < n) {
             const uint32_t *pl = hpl + (base + j) * hw;
-            y[v] = row_dot<SPL>(rp[v], pl, reinterpret_cast<const float *>(pl + 9 * nsb), nsb);
+            y[v] = R::dot(rp[v], pl, reinterpret_cast<const float *>(pl + R::NPL * nsb), nsb);
           }
         }
         warp_sum_n<BATCH>(y);
@@ -977,6 +980,18 @@ struct RowPart4 {
   uint4 hdr;
 };
 
+// The same from global memory (every byte read once: streaming loads).
+template <int SPL>
+__device__ __forceinline__ void load_row4(const uint8_t *row, RowPart4<SPL> &r) {
+  const int lane = threadIdx.x & 31;
+  constexpr int LPB = 8 / SPL;
+  const uint8_t *blk = row + (lane / LPB) * Q4B;
+  const int s0 = SPL * (lane % LPB);
+#pragma unroll
+  for (int i = 0; i < SPL; ++i) r.codes[i] = __ldcs(reinterpret_cast<const uint4 *>(blk + 16 + 16 * (s0 + i)));
+  r.hdr = __ldcs(reinterpret_cast<const uint4 *>(blk));
+}
+
 template <int SPL>
 __device__ __forceinline__ void load_row_s4(const uint8_t *row, RowPart4<SPL> &r) {
   const int lane = threadIdx.x & 31;
@@ -1076,6 +1091,7 @@ struct Q2Rows {
     load_xreg<SPL>(pl, st, nsb, x);
   }
   __device__ static __forceinline__ void load_s(const uint8_t *row, Row &r) { load_row_s<SPL>(row, r); }
+  __device__ static __forceinline__ void load_g(const uint8_t *row, Row &r) { load_row<SPL>(row, r); }
   __device__ static __forceinline__ float dot_reg(const Row &r, const XR &x) { return row_dot_reg<SPL>(r, x); }
   __device__ static __forceinline__ float dot(const Row &r, const uint32_t *pl, const float *st, int nsb) {
     return row_dot<SPL>(r, pl, st, nsb);
@@ -1094,6 +1110,7 @@ struct Q4Rows {
     load_xreg4<SPL>(pl, st, nsb, x);
   }
   __device__ static __forceinline__ void load_s(const uint8_t *row, Row &r) { load_row_s4<SPL>(row, r); }
+  __device__ static __forceinline__ void load_g(const uint8_t *row, Row &r) { load_row4<SPL>(row, r); }
   __device__ static __forceinline__ float dot_reg(const Row &r, const XR &x) { return row_dot_reg4<SPL>(r, x); }
   __device__ static __forceinline__ float dot(const Row &r, const uint32_t *pl, const float *st, int nsb) {
     return row_dot4<SPL>(r, pl, st, nsb);
@@ -1518,9 +1535,13 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
   }
 }
 
-size_t k2_smem(int T, int D) { return 4 * (size_t)T * (9 * (D / 16) + D / QK); }
-size_t k3_smem(int T, int k, int F, int Fs) {
-  return 4 * ((size_t)T * k * (9 * (F / 16) + F / QK) + (size_t)T * Fs);
+size_t k2_smem(int fmt, int T, int D) {
+  const StreamFmt f = stream_fmt(fmt);
+  return 4 * (size_t)T * (f.npl * (D / f.sub) + D / QK);
+}
+size_t k3_smem(int fmt, int T, int k, int F, int Fs) {
+  const StreamFmt f = stream_fmt(fmt);
+  return 4 * ((size_t)T * k * (f.npl * (F / f.sub) + F / QK) + (size_t)T * Fs);
 }
 
 template <typename K>
@@ -1538,7 +1559,7 @@ cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int SPL_D, int SPL_F>
+template <class RD, class RF>
 cudaError_t launch_all(const Args &a, const Shape &sh, cudaStream_t s) {
   static int sms = 0;
   static bool attr = false;
@@ -1548,10 +1569,10 @@ cudaError_t launch_all(const Args &a, const Shape &sh, cudaStream_t s) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   }
   if (!attr) {  // dynamic caps leave room for the kernels' static shared memory
-    cudaError_t e = cudaFuncSetAttribute(gateup_kernel<SPL_D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gateup_kernel<RD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(SMEM_LIMIT - 4096));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(down_kernel<SPL_F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(down_kernel<RF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)(SMEM_LIMIT - 4096));
     if (e != cudaSuccess) return e;
     attr = true;
@@ -1562,9 +1583,9 @@ cudaError_t launch_all(const Args &a, const Shape &sh, cudaStream_t s) {
   else if (sh.x_dtype == DS_F32 && sh.router_dtype == DS_F32) route_kernel<float, float><<<g1, 256, 0, s>>>(a);
   else return cudaErrorInvalidValue;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = launch_pdl(gateup_kernel<SPL_D>, dim3(sms), dim3(NW2 * 32), k2_smem(a.T, a.D), s, a)) != cudaSuccess)
+  if ((e = launch_pdl(gateup_kernel<RD>, dim3(sms), dim3(NW2 * 32), k2_smem(sh.fmt, a.T, a.D), s, a)) != cudaSuccess)
     return e;
-  return launch_pdl(down_kernel<SPL_F>, dim3(sms), dim3(NW3 * 32), k3_smem(a.T, a.k, a.F, a.Fs), s, a);
+  return launch_pdl(down_kernel<RF>, dim3(sms), dim3(NW3 * 32), k3_smem(sh.fmt, a.T, a.k, a.F, a.Fs), s, a);
 }
 
 // One token: router logits, then the streaming kernel (cooperative, so the
@@ -1641,10 +1662,14 @@ static bool fused_shape_ok(const Shape &sh, int64_t T) {
 }
 
 bool fused_decode_supported(const Shape &sh, int64_t T) {
-  // Q4_K: the streaming kernel only (the three-kernel chain reads Q2_K rows)
+  // Q4_K: the streaming kernel only.  The three-kernel chain has Q4_K
+  // instantiations (launch_all<Q4Rows...>) that have not yet been checked
+  // against the oracle on a GPU; until they are, other Q4_K batches take the
+  // grouped GEMV path
   if (sh.fmt == DS_Q4_K) return stream_decode_supported(sh, T);
   if (sh.fmt != DS_Q2_K || !fused_shape_ok(sh, T)) return false;
-  return k2_smem((int)T, sh.D) <= SMEM_LIMIT - 4096 && k3_smem((int)T, sh.k, sh.F, sh.Fs) <= SMEM_LIMIT - 4096;
+  return k2_smem(sh.fmt, (int)T, sh.D) <= SMEM_LIMIT - 4096 &&
+         k3_smem(sh.fmt, (int)T, sh.k, sh.F, sh.Fs) <= SMEM_LIMIT - 4096;
 }
 
 bool stream_decode_supported(const Shape &sh, int64_t T) {
@@ -1705,9 +1730,13 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
     if (nb_d == 16 && nb_f == 8) return launch_stream<Q2Rows<8>, Q2Rows<4>, S_STAGE>(a, sh, rb, s);
     if (nb_d == 4 && nb_f == 4) return launch_stream<Q2Rows<2>, Q2Rows<2>, S_STAGE>(a, sh, rb, s);
   }
-  if (sh.fmt != DS_Q2_K) return cudaErrorInvalidValue;
-  if (nb_d == 16 && nb_f == 8) return launch_all<8, 4>(a, sh, s);
-  if (nb_d == 4 && nb_f == 4) return launch_all<2, 2>(a, sh, s);
+  if (sh.fmt == DS_Q4_K) {
+    if (nb_d == 16 && nb_f == 8) return launch_all<Q4Rows<4>, Q4Rows<2>>(a, sh, s);
+    if (nb_d == 4 && nb_f == 4) return launch_all<Q4Rows<1>, Q4Rows<1>>(a, sh, s);
+    return cudaErrorInvalidValue;
+  }
+  if (nb_d == 16 && nb_f == 8) return launch_all<Q2Rows<8>, Q2Rows<4>>(a, sh, s);
+  if (nb_d == 4 && nb_f == 4) return launch_all<Q2Rows<2>, Q2Rows<2>>(a, sh, s);
   return cudaErrorInvalidValue;
 }
 
