@@ -53,6 +53,11 @@ def test_parameter_arithmetic_matches_pages():
     assert eb * s["n_expert"] == 2_113_929_216
     assert eb * s["n_expert"] * s["n_layer"] == 90_898_956_288
     assert dsgen.DECODE1.expert_bytes == eb
+    # the same expert in 144-byte Q4_K blocks (4.5 bits per weight)
+    eb4 = oracle.lib().oracle_expert_bytes_fmt(1, s["n_embd"], s["n_ff_exp"])
+    assert eb4 == per_expert // 256 * 144 == 14_155_776
+    assert oracle.lib().oracle_expert_bytes_fmt(0, s["n_embd"], s["n_ff_exp"]) == eb
+    assert dsgen.DECODE1_Q4K.expert_bytes == eb4
 
 
 # ------------------------------------------------------------------- fp16 --
