@@ -119,7 +119,7 @@ def test_quantize_rejects_bad_arguments_on_host(L):
 def test_layer_path_host_checks(L):
     sh = ds.MoEShape(4096, 256, 2048, 2048, 6)
     assert ds.layer_path(sh, 0) == ds.PATH_NONE
-    # 8 tokens: the tensor cores where the device has them (and the driver
+    # 8 tokens: the tensor cores where the device has them (and the CUDA driver
     # can build tensor maps), the grouped GEMV path on a host without a GPU
     import torch
     expect = ds.PATH_TENSOR_CORE if torch.cuda.is_available() else ds.PATH_GROUPED_GEMV
