@@ -27,6 +27,12 @@
 // converted once: w.x = step * (d * sum sc S - dmin * sum m X).  The only
 // rounding beyond fp32 is that fixed point (|err| <= 2^-16 of the block's
 // largest |v| per element).
+//
+// Q4_K rows ("Understanding Dwarf Star", 2.3.2: 144-byte blocks, 8
+// sub-blocks of 32 with 6-bit scales and mins, 4-bit codes) use the same
+// scheme with their own lane map and planes (the even and odd nibbles of each
+// code word); every kernel here is a template over the row format (Q2Rows /
+// Q4Rows, defined with the streaming kernel).
 #include <algorithm>
 
 #include "common.cuh"
