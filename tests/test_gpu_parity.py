@@ -548,6 +548,26 @@ def test_q4k_layer_parity(T, Fs, k, E, dtype, D):
     layer_parity(cfg, DECODE_TOL)
 
 
+@pytest.mark.parametrize("variant", ["one_expert", "k_eq_E", "zipf_select_only", "T1_zipf"])
+def test_q4k_tiny_variants(variant):
+    """Degenerate and biased routings with Q4_K experts: one expert (k = 1),
+    every expert selected (k = E), a Zipf router bias that steers the
+    selection only, and one token with a Zipf bias (the streaming kernel at
+    width 1024)."""
+    from dataclasses import replace
+    c = replace(dsgen.TINY, expert_fmt="q4k")
+    if variant == "one_expert":
+        layer_parity(replace(c, E=1, k=1), DECODE_TOL)
+    elif variant == "k_eq_E":
+        layer_parity(replace(c, k=16), DECODE_TOL)
+    elif variant == "zipf_select_only":
+        layer_parity(replace(c, zipf_s=1.1), DECODE_TOL, bias_select_only=1)
+    else:
+        cfg = replace(_small(1, 512, 6, 64, "bf16"), expert_fmt="q4k", zipf_s=1.1)
+        assert ds.layer_path(synthetic.shape_of(cfg), 1) == ds.PATH_STREAM
+        layer_parity(cfg, DECODE_TOL)
+
+
 def test_q4k_tiny_ragged_width():
     """n_ff = 128: half a Q4_K block per down row (zero-padded sub-blocks)."""
     from dataclasses import replace
