@@ -114,6 +114,16 @@ def test_quantize_rejects_bad_arguments_on_host(L):
     assert L.ds_moe_quantize_q2k(16, -1, 256, 16, None, err, 256) == ds.DS_ERR_INVALID_ARG
     assert L.ds_moe_quantize_q2k(18, 4, 256, 16, None, err, 256) == ds.DS_ERR_INVALID_ARG
     assert L.ds_moe_quantize_q2k(16, 0, 256, 16, None, err, 256) == ds.DS_OK
+    for q in (L.ds_moe_quantize_q4k, L.ds_moe_quantize_q2k):
+        assert q(None, 4, 256, 16, None, err, 256) == ds.DS_ERR_INVALID_ARG
+        assert q(16, 4, -2, 16, None, err, 256) == ds.DS_ERR_INVALID_ARG
+        assert q(16, 4, 256, 17, None, err, 256) == ds.DS_ERR_INVALID_ARG   # out not 4-byte aligned
+        assert q(16, 4, 0, 16, None, err, 256) == ds.DS_OK                  # nothing to do
+    for dq in (L.ds_moe_dequantize_q4k, L.ds_moe_dequantize_q2k):
+        assert dq(16, 4, 256, None, None, err, 256) == ds.DS_ERR_INVALID_ARG
+        assert dq(16, 4, 256, 18, None, err, 256) == ds.DS_ERR_INVALID_ARG
+        assert dq(16, -4, 256, 16, None, err, 256) == ds.DS_ERR_INVALID_ARG
+        assert dq(16, 0, 256, 16, None, err, 256) == ds.DS_OK
 
 
 def test_layer_path_host_checks(L):
