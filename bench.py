@@ -9,11 +9,14 @@ decode pass does, so no step finds the previous step's weights in L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--layers R] [--no-extra] [--no-cpu-baseline]
+                    [--workload prefill|prefill_zipf|decode32|stack|decode_q4k|prefill_small]
 
 Prints one JSON line (rank 0).  Its "extra" object times the metric's other
-workloads (prefill T=4096 uniform and Zipf against the bf16 tensor roofline,
-decode T=32 Zipf against HBM).  --impl reference times the fp64 CPU oracle on
-a bounded sample of the decode workload instead.
+workloads (prefill T=4096 uniform and Zipf against the bf16 tensor roofline;
+decode T=32 Zipf, decode T=1 with Q4_K experts and the 43-layer stack at T=8
+against HBM).  --impl reference times the fp64 CPU oracle on a bounded sample
+of the decode workload instead; --workload times one other workload alone
+(profiling runs).
 """
 from __future__ import annotations
 
