@@ -242,11 +242,12 @@ def gpu_arm(args, rank, world, local_rank):
 
 
 LAUNCHES_PER_DECODE_STEP = 2  # router logits; the one-token streaming kernel
-# DRAM bytes read + written by one decode step (route_kernel 2,117,888 read;
-# stream_kernel 99,979,008 read + 76,288 written), from one ncu capture of
-# these kernels as they stand (the command is in the decode profile summary);
-# to be set back to None whenever either kernel changes
-DECODE_STEP_DRAM_BYTES = 2_117_888 + 99_979_008 + 76_288
+# DRAM bytes read + written by one decode step, from one ncu capture of these
+# kernels as they stand, or None.  The last capture (route_kernel 2,117,888
+# read; stream_kernel 99,979,008 read + 76,288 written; the command is in the
+# decode profile summary) predates the streaming kernel's templating on the
+# row format, so it is not claimed until the kernel is captured again.
+DECODE_STEP_DRAM_BYTES = None
 
 PREFILL_FLOPS = 1.4517e12  # 4096 x (6*3*2*D*F + 3*2*D*F + 2*D*E) at the Flash shape
 
