@@ -31,7 +31,7 @@ SYMBOLS = ["ds_moe_q2k_bytes", "ds_moe_expert_bytes", "ds_moe_quantize_q2k",
            "ds_moe_stack_mixed"]
 
 # ds_moe_layer_path results
-PATH_NONE, PATH_STREAM, PATH_DECODE3, PATH_GROUPED_GEMV, PATH_TENSOR_CORE = 0, 1, 2, 3, 4
+PATH_NONE, PATH_STREAM, PATH_DECODE3, PATH_GROUPED_GEMV, PATH_TENSOR_CORE, PATH_BATCHED_DECODE = 0, 1, 2, 3, 4, 5
 
 
 class DsMoeError(RuntimeError):

@@ -114,7 +114,8 @@ size_t layout(const Shape &sh, int64_t T, char *base, Work *wk) {
   w.x_dev = take(xbytes);
   w.out_dev = (float *)take(sizeof(float) * T * sh.D);
   w.tc = prefill_tc_supported(sh, T) ? (void *)take(prefill_tc_workspace(sh, T)) : nullptr;
-  if (!base) w.tc = nullptr;
+  w.mt = decode_mt_supported(sh, T) ? (void *)take(decode_mt_workspace(sh, T)) : nullptr;
+  if (!base) w.tc = w.mt = nullptr;
   w.T = T;
   w.n_chunks = n_chunks;
   if (wk) *wk = w;
@@ -145,6 +146,10 @@ int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *ou
   if (fused_decode_supported(sh, wk.T)) {
     if ((e = launch_decode_fused(sh, W, x, wk, out, accumulate, s)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "fused decode layer");
+  } else if (wk.mt && aligned(x, 16) && decode_mt_supported(sh, wk.T)) {
+    if ((e = launch_router_logits(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "router");
+    if ((e = launch_decode_mt(sh, W, x, wk, out, accumulate, wk.mt, s)) != cudaSuccess)
+      return cuda_fail(err, errlen, e, "batched decode layer");
   } else {
     if ((e = cudaMemsetAsync(wk.ctrl, 0, 256, s)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "workspace control reset");
@@ -428,6 +433,7 @@ int ds_moe_layer_path(const ds_moe_shape *shape, int64_t T, const void *x) {
   if (check_shape(shape, nullptr, 0, &sh) != DS_OK || T < 0) return DS_ERR_INVALID_ARG;
   if (T == 0) return DS_PATH_NONE;
   if (fused_decode_supported(sh, T)) return stream_decode_supported(sh, T) ? DS_PATH_STREAM : DS_PATH_DECODE3;
+  if (aligned(x, 16) && decode_mt_supported(sh, T)) return DS_PATH_BATCHED_DECODE;
   if (aligned(x, 16) && prefill_tc_supported(sh, T)) return DS_PATH_TENSOR_CORE;
   return DS_PATH_GROUPED_GEMV;
 }

@@ -1,5 +1,6 @@
 // Internal launchers of the ds_moe library (not part of the C ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,9 +28,23 @@ struct Work {
   void *x_dev;       // [T][D] device copy of host x (hostio)
   float *out_dev;    // [T][D] device out (hostio)
   void *tc;          // tensor-core path scratch (prefill_tc_workspace bytes), or null
+  void *mt;          // batched decode scratch (decode_mt_workspace bytes), or null
   int64_t T;
   int64_t n_chunks;
 };
+
+// Tensor maps for the bulk-tensor (TMA) copies, encoded through the driver
+// entry point (null when the driver has none).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
+// Row-major 16-bit matrix [rows][cols] as a 2-D map with boxes of 64 columns
+// x box_rows rows in the 128-byte swizzle (zero fill beyond the edges).
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows, bool bf16);
+// Quantised expert rows as a 3-D map of 32-bit words {row words, rows, E}.
+bool make_words_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int64_t E,
+                    int64_t expert_bytes, uint32_t box_words, uint32_t box_rows);
 
 // fmt: DS_Q2_K or DS_Q4_K.
 cudaError_t launch_quantize(int fmt, const float *w, int64_t rows, int64_t in_dim, uint8_t *out,
@@ -71,6 +86,16 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
 // Router logits of the tensor-core path (bf16 x and router, tcgen05).
 cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
                              cudaStream_t s);
+// Batched decode (MT_MIN_T..MT_MAX_T tokens): the router logits alone, then
+// selection, route, expert FFNs and combine in the batched decode kernels.
+// (The kernels hold up to 32 tokens; above 16 the tensor-core path is faster.)
+constexpr int64_t MT_MIN_T = 5, MT_MAX_T = 16;
+cudaError_t launch_router_logits(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
+                                 cudaStream_t s);
+bool decode_mt_supported(const Shape &sh, int64_t T);
+size_t decode_mt_workspace(const Shape &sh, int64_t T);
+cudaError_t launch_decode_mt(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk, float *out,
+                             bool accumulate, void *mt_ws, cudaStream_t s);
 cudaError_t launch_combine(const Shape &sh, const Work &wk, float *out, bool accumulate,
                            cudaStream_t s);
 

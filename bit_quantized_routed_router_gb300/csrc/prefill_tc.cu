@@ -771,11 +771,20 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict
   }
 }
 
-// ---------------------------------------------------------------- host side --
+template <int MODE, int FMT = DS_Q2_K>
+constexpr size_t tc_smem() {
+  using C = TcCfg<MODE, FMT>;
+  return 1024 + C::STAGES * C::STAGE_BYTES + C::RAW * C::RAW_BYTES + sizeof(TcShared);
+}
+static_assert(tc_smem<MODE_GU>() <= 227 * 1024 && tc_smem<MODE_DN>() <= 227 * 1024 &&
+                  tc_smem<MODE_ROUTER>() <= 227 * 1024 && tc_smem<MODE_GU, DS_Q4_K>() <= 227 * 1024 &&
+                  tc_smem<MODE_DN, DS_Q4_K>() <= 227 * 1024,
+              "pipeline exceeds the shared memory of a block");
+static_assert(TcCfg<MODE_DN>::STAGES <= TC_MAX_STAGES && TcCfg<MODE_GU>::RAW <= TC_MAX_RAW, "barrier arrays");
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+}  // namespace
+
+// ---------------------------------------------------------------- host side --
 
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
@@ -803,34 +812,22 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The Q2_K rows of every expert as a 3-D map of 32-bit words: x = word in
-// a row, y = row (gate rows then up rows, or down rows), z = expert; boxes
-// of 24 words x 128 rows.
-bool make_raw_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int64_t E,
-                  int64_t expert_bytes, uint32_t raw_row) {
+
+// The quantised rows of every expert as a 3-D map of 32-bit words: x = word
+// in a row, y = row (gate rows then up rows, or down rows), z = expert; boxes
+// of box_words words x box_rows rows, no swizzle.
+bool make_words_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int64_t E,
+                    int64_t expert_bytes, uint32_t box_words, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)rows, (cuuint64_t)E};
   const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_bytes};
-  const cuuint32_t box[3] = {raw_row / 4, (cuuint32_t)TC_BM, 1};
+  const cuuint32_t box[3] = {box_words, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-template <int MODE, int FMT = DS_Q2_K>
-constexpr size_t tc_smem() {
-  using C = TcCfg<MODE, FMT>;
-  return 1024 + C::STAGES * C::STAGE_BYTES + C::RAW * C::RAW_BYTES + sizeof(TcShared);
-}
-static_assert(tc_smem<MODE_GU>() <= 227 * 1024 && tc_smem<MODE_DN>() <= 227 * 1024 &&
-                  tc_smem<MODE_ROUTER>() <= 227 * 1024 && tc_smem<MODE_GU, DS_Q4_K>() <= 227 * 1024 &&
-                  tc_smem<MODE_DN, DS_Q4_K>() <= 227 * 1024,
-              "pipeline exceeds the shared memory of a block");
-static_assert(TcCfg<MODE_DN>::STAGES <= TC_MAX_STAGES && TcCfg<MODE_GU>::RAW <= TC_MAX_RAW, "barrier arrays");
-
-}  // namespace
 
 cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
                              cudaStream_t s) {
@@ -963,9 +960,9 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
       !make_map(&m_sd, sd16, sh.D, fs1, TC_BM, false))
     return cudaErrorInvalidValue;
   CUtensorMap m_rgu, m_rdn;
-  if (!make_raw_map(&m_rgu, W.experts, (int64_t)(sh.D / QK) * bb, 2 * (int64_t)sh.F, sh.E, sh.expert_bytes(), raw_row) ||
-      !make_raw_map(&m_rdn, W.experts + 2 * sh.gate_bytes(), (int64_t)(sh.F / QK) * bb, sh.D, sh.E,
-                    sh.expert_bytes(), raw_row))
+  if (!make_words_map(&m_rgu, W.experts, (int64_t)(sh.D / QK) * bb, 2 * (int64_t)sh.F, sh.E, sh.expert_bytes(), raw_row / 4, TC_BM) ||
+      !make_words_map(&m_rdn, W.experts + 2 * sh.gate_bytes(), (int64_t)(sh.F / QK) * bb, sh.D, sh.E,
+                      sh.expert_bytes(), raw_row / 4, TC_BM))
     return cudaErrorInvalidValue;
   a.tiles = tiles_gu;
   a.n_tiles = cnt;

@@ -7,6 +7,7 @@
 // that groups each expert's tokens contiguously.
 #include "common.cuh"
 #include "internal.h"
+#include "select.cuh"
 
 namespace dsm {
 namespace {
@@ -75,6 +76,10 @@ __global__ void __launch_bounds__(256) router_small_kernel(const TX *__restrict_
                                                            const TW *__restrict__ wr,
                                                            const float *__restrict__ bias, int T,
                                                            int D, int E, float *__restrict__ logits) {
+  // a kernel launched after this one with programmatic dependent launch may
+  // start its independent work now (it waits for this grid before reading
+  // the logits)
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr int TB = 16 / NCH;  // tokens per batch
   __shared__ float part[8][64];  // [warp][token] partial logits
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -132,60 +137,6 @@ cudaError_t launch_router_small(const TX *x, const TW *wr, const float *bias, in
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
-}
-
-// Top-k of one token's logits in the calling warp: ids in descending logit
-// order, ties to the lower index; weights = routed_scale * softmax over
-// logit_scale * the selected logits, from which `unbias` (the router bias,
-// when it steers the selection only; else null) is taken back out.
-// E <= 1024, k <= 16.
-__device__ void select_token(const float *__restrict__ L, int E, int k, float routed_scale, float logit_scale,
-                             const float *__restrict__ unbias, int32_t *ids, float *w, unsigned *st) {
-  const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;  // bit i: element lane + 32 i already selected
-  int sel[16];
-  float selv[16];
-  // each lane's best remaining candidate; a pick is the warp's largest
-  // order-preserving key (two hardware reductions: the key, then the lowest
-  // index holding it), and only the lane that supplied it rescans
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  auto rescan = [&]() {
-    bv = -INFINITY;
-    bi = 0x7fffffff;
-    for (int i = 0, e = lane; e < E; ++i, e += 32) {
-      if (taken & (1u << i)) continue;
-      const float v = L[e];
-      if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
-    }
-  };
-  rescan();
-  for (int j = 0; j < k; ++j) {
-    const uint32_t key = ord_key(bv + 0.f);  // -0 as +0: equal logits tie
-    const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
-    int wi = (int)__reduce_min_sync(0xffffffffu, key == mk ? (uint32_t)bi : 0x7fffffffu);
-    if (wi < 0 || wi >= E) {  // only possible with NaN logits
-      if (lane == 0) flag(st, ST_BAD_ID);
-      wi = 0;
-    }
-    if ((wi & 31) == lane && wi == bi) {
-      taken |= 1u << (wi >> 5);
-      rescan();
-    }
-    sel[j] = wi;
-    selv[j] = ord_val(mk);
-  }
-  if (lane == 0) {
-    if (unbias)
-      for (int j = 0; j < k; ++j) selv[j] -= unbias[sel[j]];
-    const float m = selv[0];
-    float den = 0.0f;
-    for (int j = 0; j < k; ++j) den += __expf(logit_scale * (selv[j] - m));
-    for (int j = 0; j < k; ++j) {
-      ids[j] = sel[j];
-      w[j] = routed_scale * (__expf(logit_scale * (selv[j] - m)) / den);
-    }
-  }
 }
 
 __global__ void __launch_bounds__(256) select_kernel(const float *__restrict__ logits, int64_t T,
@@ -371,6 +322,13 @@ __global__ void __launch_bounds__(ROUTE_CHUNK) route_scatter_kernel(
 
 cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
                          cudaStream_t s) {
+  cudaError_t err = launch_router_logits(sh, W, x, wk, s);
+  if (err != cudaSuccess) return err;
+  return launch_select_route(sh, wk, W.router_bias, s);
+}
+
+cudaError_t launch_router_logits(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
+                                 cudaStream_t s) {
   const int64_t T = wk.T;
   const int E = sh.E, D = sh.D;
   unsigned *st = status_word();
@@ -399,9 +357,7 @@ cudaError_t launch_route(const Shape &sh, const ds_moe_weights &W, const void *x
       router_logits_kernel<float, float><<<g, 256, 0, s>>>(
           (const float *)x, (const float *)W.router_w, W.router_bias, T, D, E, tb, wk.logits);
   }
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  return launch_select_route(sh, wk, W.router_bias, s);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_select_route(const Shape &sh, const Work &wk, const float *bias, cudaStream_t s) {

@@ -257,7 +257,9 @@ enum {
   DS_PATH_STREAM = 1,        /* one token: router kernel + one cooperative streaming kernel */
   DS_PATH_DECODE3 = 2,       /* T <= 4: router, gate/up and down kernels chained */
   DS_PATH_GROUPED_GEMV = 3,  /* route kernels + grouped dequantising GEMVs + combine */
-  DS_PATH_TENSOR_CORE = 4    /* route kernels + grouped tcgen05 GEMMs + combine */
+  DS_PATH_TENSOR_CORE = 4,   /* route kernels + grouped tcgen05 GEMMs + combine */
+  DS_PATH_BATCHED_DECODE = 5 /* 5..16 tokens: router kernel + batched decode kernels (integer
+                                routed dots, shared expert on the tensor cores) */
 };
 int ds_moe_layer_path(const ds_moe_shape *shape, int64_t T, const void *x);
 
