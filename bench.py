@@ -394,7 +394,10 @@ def extra_workloads(args, dev):
     pk, pk_kind = peaks()
     res = {}
     for cfg, iters in ((dsgen.PREFILL, 10), (dsgen.PREFILL_ZIPF, 10), (dsgen.DECODE32_ZIPF, 200)):
-        ms, used, path = time_layer(cfg, iters, dev)
+        if cfg.T < 64:  # decode-sized: rotate four layers (inputs larger than L2), graph-timed
+            ms, used, path = time_decode_rotating(cfg, 4, iters, dev)
+        else:
+            ms, used, path = time_layer(cfg, iters, dev)
         entry = {"tokens_per_s": cfg.T / (ms / 1e3), "ms_per_layer": ms, "T": cfg.T,
                  "used_experts": used, "path": path}
         if cfg.T >= 64:
@@ -409,6 +412,7 @@ def extra_workloads(args, dev):
             hbm = float(pk.get("hbm_gbs", HBM_FALLBACK_GBS))
             entry["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                                  "frac": gbs / hbm, "peak_source": pk_kind, "algorithmic_bytes": b}
+            entry["timing"] = "CUDA graph of 40 calls rotating over 4 layers"
         res[cfg.name] = entry
     cfg = dsgen.DECODE1_Q4K
     ms, used, path = time_decode_rotating(cfg, 2, 400, dev)
@@ -449,12 +453,35 @@ WORKLOADS = {
 
 # ------------------------------------------------------------ oracle (CPU) --
 
+def host_info():
+    """The host's logical core count and CPU model (for the CPU-baseline rows)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k = k.strip().lower()
+                if k in ("model name", "cpu model", "hardware") and v.strip():
+                    model = v.strip()
+                    break
+                if k == "cpu part" and model is None:
+                    model = f"cpu part {v.strip()}"
+    except OSError:
+        pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"host_cores": os.cpu_count() or 1, "cpu_model": model}
+
+
 def oracle_sample(n_tokens: int = 2, budget_s: float = 12.0):
     """Time the fp64 oracle on decode-B=1 steps (one token each) of the same
     layer shape.  The experts the sampled tokens select are regenerated and
     packed once (input preparation, untimed); then whole layer evaluations
     (router, selection, routed and shared experts, combine) of those tokens
-    are timed in turn until about budget_s seconds of compute."""
+    are timed in turn until about budget_s seconds of compute.  `cores` is
+    the number of threads the oracle's work split used (one per selected
+    expert plus the shared expert, at most the host's cores)."""
     sys.path.insert(0, os.path.join(ROOT, "oracle"))
     import oracle
 
@@ -478,10 +505,34 @@ def oracle_sample(n_tokens: int = 2, budget_s: float = 12.0):
         used_threads = max(used_threads, min(oracle.NTHREADS, len(set(ids.ravel())) + 1))
     tot = sum(times)
     return {"value": len(times) / tot, "unit": "tokens/s", "cores": used_threads,
-            "kind": "oracle",
+            "kind": "oracle", **host_info(),
             "sample": f"{len(times)} decode-B=1 layer evaluations cycling over {n_tokens} seeded "
                       f"tokens of the same layer (fp64 C oracle, {tot:.1f} s of layer compute; "
                       f"expert regeneration untimed)"}
+
+
+def oracle_batch_sample(cfg, n_tokens: int, what: str):
+    """The fp64 oracle on one layer evaluation of the first n_tokens tokens of
+    a batched workload (decode T=32, prefill, a stack layer): tokens/s of
+    that evaluation; the selected experts are regenerated first (untimed)."""
+    sys.path.insert(0, os.path.join(ROOT, "oracle"))
+    import oracle
+    from dataclasses import replace
+
+    c = replace(cfg, T=n_tokens)
+    lo = oracle.LayerOracle(c)
+    x = oracle.as_f64(dsgen.host_x(c), c.x_dtype)
+    ids0, _ = oracle.select(lo.logits(x), c.k)
+    exps = lo.experts(ids0)
+    t0 = time.perf_counter()
+    L = lo.logits(x)
+    ids, w = oracle.select(L, c.k)
+    oracle.moe_layer(x, exps, lo.shared, ids, w, c.D, c.E, c.F, c.Fs, fmt=c.expert_fmt)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": min(oracle.NTHREADS, len(exps) + 1),
+            "kind": "oracle", **host_info(),
+            "sample": f"one layer evaluation of {n_tokens} tokens of the {what} workload "
+                      f"({len(exps)} experts, fp64 C oracle, {dt:.1f} s; expert regeneration untimed)"}
 
 
 def reference_arm(args, rank):
@@ -556,6 +607,12 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = oracle_sample()
+            if "extra" in line:
+                for cfg, n, what in ((dsgen.DECODE32_ZIPF, 32, "decode T=32 Zipf"),
+                                     (dsgen.PREFILL, 8, "prefill T=4096 (a sample of its tokens)"),
+                                     (dsgen.STACK, 8, "43-layer stack (its first layer)")):
+                    if cfg.name in line["extra"]:
+                        line["extra"][cfg.name]["cpu_baseline"] = oracle_batch_sample(cfg, n, what)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch

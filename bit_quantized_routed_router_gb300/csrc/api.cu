@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -15,6 +16,12 @@
 namespace dsm {
 
 __device__ unsigned g_status_word;
+
+// Slots for the values ds_moe_sync_status takes out of the status word.
+constexpr unsigned STATUS_SLOTS = 64;
+__device__ unsigned g_status_taken[STATUS_SLOTS];
+
+__global__ void status_take_kernel(unsigned slot) { g_status_taken[slot] = atomicExch(&g_status_word, 0u); }
 
 unsigned *status_word() {
   static std::mutex mu;
@@ -28,6 +35,16 @@ unsigned *status_word() {
     addr[dev] = (unsigned *)p;
   }
   return addr[dev];
+}
+
+int device_sms() {
+  static std::mutex mu;
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!sms[dev] && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms[dev] = 0;
+  return sms[dev];
 }
 
 namespace {
@@ -407,16 +424,20 @@ int ds_moe_stack(const ds_moe_shape *shape, const ds_moe_weights *layers, int32_
 }
 
 int ds_moe_sync_status(void *stream, char *err, size_t errlen) {
-  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(err, errlen, e, "stream");
+  // read and clear in one atomic exchange on the device, so that bits another
+  // stream's kernel sets meanwhile are kept for the next call; each call
+  // takes its own slot for the value read
+  static std::atomic<unsigned> next_slot{0};
+  const unsigned slot = next_slot.fetch_add(1u) % STATUS_SLOTS;
+  status_take_kernel<<<1, 1, 0, s>>>(slot);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, errlen, e, "status exchange");
   unsigned v = 0;
-  e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof v);
+  e = cudaMemcpyFromSymbolAsync(&v, g_status_taken, sizeof v, sizeof(unsigned) * slot, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(err, errlen, e, "read status word");
-  if (v) {
-    unsigned z = 0;
-    e = cudaMemcpyToSymbol(g_status_word, &z, sizeof z);
-    if (e != cudaSuccess) return cuda_fail(err, errlen, e, "clear status word");
-  }
   if (v & ST_TIMEOUT) return fail(err, errlen, DS_ERR_TIMEOUT, "a device wait timed out (status 0x%x)", v);
   if (v & ST_QUANT_INPUT)
     return fail(err, errlen, DS_ERR_DEVICE_CHECK, "quantiser input not finite or |w| > 65504 (status 0x%x)", v);

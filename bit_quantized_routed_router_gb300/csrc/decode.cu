@@ -332,14 +332,12 @@ template <int MODE, typename TX, int FMT>
 cudaError_t launch_gemv1(const GemvArgs &a, int out_rows_max, int in_dim_max, cudaStream_t s) {
   // a block stages at most min(T, NT) tokens (no slot has more than T)
   const size_t smem = (size_t)std::min<int64_t>(a.T, NT) * in_dim_max * sizeof(float);
-  static bool attr_set = false;
+  static OncePerDevice once;
   auto kern = grouped_gemv_kernel<MODE, TX, FMT>;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = once_per_device(once, [&]() {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  if (e != cudaSuccess) return e;
   dim3 g((out_rows_max + RPB - 1) / RPB, a.n_slots + (a.Fs > 0 ? 1 : 0));
   kern<<<g, 256, smem, s>>>(a);
   return cudaGetLastError();

@@ -1101,23 +1101,17 @@ cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t 
 
 template <class RD, class RF>
 cudaError_t launch_all(const Args &a, const Shape &sh, cudaStream_t s) {
-  static int sms = 0;
-  static bool attr = false;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  }
-  if (!attr) {  // dynamic caps leave room for the kernels' static shared memory
-    cudaError_t e = cudaFuncSetAttribute(gateup_kernel<RD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static OncePerDevice once;
+  const int sms = device_sms();
+  if (!sms) return cudaErrorNoDevice;
+  cudaError_t e = once_per_device(once, []() {  // dynamic caps leave room for the kernels' static shared memory
+    cudaError_t r = cudaFuncSetAttribute(gateup_kernel<RD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(SMEM_LIMIT - 4096));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(down_kernel<RF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)(SMEM_LIMIT - 4096));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  cudaError_t e;
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(down_kernel<RF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SMEM_LIMIT - 4096));
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   const dim3 g1((sh.E + 1) / 2);
   if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16) route_kernel<uint16_t, uint16_t><<<g1, 256, 0, s>>>(a);
   else if (sh.x_dtype == DS_F32 && sh.router_dtype == DS_F32) route_kernel<float, float><<<g1, 256, 0, s>>>(a);
@@ -1132,15 +1126,11 @@ cudaError_t launch_all(const Args &a, const Shape &sh, cudaStream_t s) {
 // grid barrier is safe; PDL lets its prologue overlap the router grid).
 template <class RD, class RF, uint32_t STG>
 cudaError_t launch_stream(const Args &a, const Shape &sh, int rb, cudaStream_t s) {
-  static int sms = 0;
-  static bool attr = false;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  }
+  static OncePerDevice once;
+  const int sms = device_sms();
+  if (!sms) return cudaErrorNoDevice;
   const size_t smem = stream_smem(sh.fmt, a.D, a.F, a.Fs, a.n_slots);
-  if (!attr) {
+  cudaError_t e0 = once_per_device(once, []() {
     cudaError_t e = cudaFuncSetAttribute(stream_kernel<RD, RF, STG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
     if (e != cudaSuccess) return e;
@@ -1151,11 +1141,27 @@ cudaError_t launch_stream(const Args &a, const Shape &sh, int rb, cudaStream_t s
       if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                     (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
         return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<RD, RF, STG>, S_THREADS, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-    attr = true;
+    return cudaSuccess;
+  });
+  if (e0 != cudaSuccess) return e0;
+  // the grid barrier needs every block resident: one block per SM at this
+  // call's shared-memory size (checked per device and size)
+  {
+    static std::mutex mu;
+    static int dev_seen[64] = {};
+    static size_t smem_seen[64] = {};
+    int dev = 0;
+    if ((e0 = cudaGetDevice(&dev)) != cudaSuccess) return e0;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!dev_seen[dev] || smem_seen[dev] != smem) {
+      int per_sm = 0;
+      e0 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<RD, RF, STG>, S_THREADS, smem);
+      if (e0 != cudaSuccess) return e0;
+      if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+      dev_seen[dev] = 1;
+      smem_seen[dev] = smem;
+    }
   }
   const dim3 g1((sh.E + 1) / 2);
   if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16) route_kernel<uint16_t, uint16_t><<<g1, 256, 0, s>>>(a);
@@ -1217,12 +1223,7 @@ bool stream_decode_supported(const Shape &sh, int64_t T) {
   const int nb_d = sh.D / QK, nb_f = sh.F / QK, nslots = std::min(sh.E, sh.k);
   const StreamFmt f = stream_fmt(sh.fmt);
   const int rb = stream_rows_b(sh.fmt, sh.D, sh.F, sh.Fs, nslots);
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  }
+  const int sms = device_sms();
   return rb > 0 && sms > 0 && stream_smem(sh.fmt, sh.D, sh.F, sh.Fs, nslots) <= SMEM_LIMIT && nslots <= 32 &&
          8 * (int64_t)sh.D <= f.stage && 2 * S_GU * (int64_t)nb_d * f.bb <= f.stage && nb_f % 4 == 0 &&
          (sh.Fs / 2 + sms - 1) / sms <= S_MAXT && (sh.D / rb + sms - 1) / sms <= S_MAXT;

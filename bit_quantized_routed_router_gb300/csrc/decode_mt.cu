@@ -920,30 +920,15 @@ cudaError_t launch_pdl_maps(K kern, dim3 grid, size_t smem, cudaStream_t s, cons
   return cudaLaunchKernelEx(&cfg, kern, a, maps...);
 }
 
-struct DevInfo {
-  int sms = 0;
-  bool attrs = false;
-};
-
-// Per-device launch facts, set up once per device under a lock.
-DevInfo *dev_info(cudaError_t *err) {
-  static std::mutex mu;
-  static DevInfo info[64];
-  int dev = 0;
-  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= 64) { *err = cudaErrorInvalidDevice; return nullptr; }
-  std::lock_guard<std::mutex> lock(mu);
-  DevInfo &d = info[dev];
-  if (!d.attrs) {
-    if ((*err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return nullptr;
+// Kernel attributes, set once per device.
+cudaError_t mt_setup() {
+  static OncePerDevice once;
+  return once_per_device(once, []() {
     const int lim = (int)MT_SMEM_LIMIT;
-    if ((*err = cudaFuncSetAttribute(mt_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) != cudaSuccess ||
-        (*err = cudaFuncSetAttribute(mt_dn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) != cudaSuccess)
-      return nullptr;
-    d.attrs = true;
-  }
-  *err = cudaSuccess;
-  return &d;
+    cudaError_t e = cudaFuncSetAttribute(mt_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(mt_dn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    return e;
+  });
 }
 
 size_t gu_smem(const Shape &sh, int64_t T) {
@@ -983,9 +968,10 @@ size_t decode_mt_workspace(const Shape &sh, int64_t T) {
 
 cudaError_t launch_decode_mt(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk, float *out,
                              bool accumulate, void *mt_ws, cudaStream_t s) {
-  cudaError_t e;
-  DevInfo *di = dev_info(&e);
-  if (!di) return e;
+  cudaError_t e = mt_setup();
+  if (e != cudaSuccess) return e;
+  const int G = device_sms();
+  if (!G) return cudaErrorNoDevice;
   const int T = (int)wk.T, P = T * sh.k;
   const int KS = slices_for(sh.D / MT_CHUNK, T), KSd = slices_for(sh.F / MT_CHUNK, T);
   if (KS == 0 || KSd == 0) return cudaErrorInvalidValue;
@@ -1039,7 +1025,6 @@ cudaError_t launch_decode_mt(const Shape &sh, const ds_moe_weights &W, const voi
       !make_map(&m_hl, a.hs_lo, T, sh.Fs > 0 ? sh.Fs : MT_BOX_K, a.T8, true))
     return cudaErrorInvalidValue;
 
-  const int G = di->sms;
   if ((e = launch_pdl_maps(mt_gu_kernel, dim3(G), gu_smem(sh, T), s, a, m_rgu, m_sg, m_su, m_x)) != cudaSuccess)
     return e;
   if ((e = launch_pdl_mt(mt_h_kernel, dim3(G), dim3(256), 0, s, true, a)) != cudaSuccess) return e;

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace dsm {
@@ -45,6 +47,32 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int 
 // Quantised expert rows as a 3-D map of 32-bit words {row words, rows, E}.
 bool make_words_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int64_t E,
                     int64_t expert_bytes, uint32_t box_words, uint32_t box_rows);
+
+// The current device's SM count (looked up once per device); 0 without a
+// usable device.
+int device_sms();
+
+// Per-device one-time set-up of a launch site (kernel attributes): init()
+// runs once per device, under a lock, with that device current; later calls
+// on the same device return its result.
+struct OncePerDevice {
+  std::mutex mu;
+  signed char state[64] = {};  // 0: not run, 1: done
+  cudaError_t err[64] = {};
+};
+template <class F>
+cudaError_t once_per_device(OncePerDevice &o, F &&init) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(o.mu);
+  if (!o.state[dev]) {
+    o.err[dev] = init();
+    o.state[dev] = 1;
+  }
+  return o.err[dev];
+}
 
 // fmt: DS_Q2_K or DS_Q4_K.
 cudaError_t launch_quantize(int fmt, const float *w, int64_t rows, int64_t in_dim, uint8_t *out,

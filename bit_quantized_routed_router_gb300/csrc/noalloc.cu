@@ -1,12 +1,11 @@
 // ds_moe_layer_noalloc: the layer with its scratch in a static device array.
 //
 // Some callers cannot allocate device memory at the point where they run the
-// layer: code being recorded into a CUDA graph (allocation calls are not
-// allowed while a stream is capturing), plugins inside a host program whose
-// own allocator owns all device memory, and latency-critical loops where the
-// implicit synchronisation of cudaMalloc is not acceptable.  For them this
-// entry point needs no workspace argument: it uses a fixed array that lives
-// in this file's device module, sized NOALLOC_SCRATCH_BYTES.
+// layer: plugins inside a host program whose own allocator owns all device
+// memory, and latency-critical loops where the implicit device-wide
+// synchronisation of cudaMalloc is not acceptable.  For them this entry point
+// needs no workspace argument: it uses a fixed array that lives in this
+// file's device module, sized NOALLOC_SCRATCH_BYTES.
 //
 // The array is allocated once per GPU when the library's module is loaded
 // there and is held until the process exits.  All calls share it, and it
@@ -71,7 +70,8 @@ extern "C" int ds_moe_layer_noalloc(const ds_moe_shape *shape, const ds_moe_weig
                (long long)T, need, NOALLOC_SCRATCH_BYTES);
     return DS_ERR_INVALID_ARG;
   }
-  if (T == 0) return DS_OK;
+  // ds_moe_layer validates the weights and the other arguments in its own
+  // order (T == 0 included); the scratch only has to be addressable
   void *scratch = scratch_address(err, errlen, &rc);
   if (!scratch) return rc;
   return ds_moe_layer(shape, weights, x, T, out, scratch, NOALLOC_SCRATCH_BYTES, nullptr, stream,

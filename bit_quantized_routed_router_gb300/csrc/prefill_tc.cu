@@ -831,19 +831,14 @@ bool make_words_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t
 
 cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
                              cudaStream_t s) {
-  static int sms = 0;
-  static bool attr = false;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  }
-  if (!attr) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_ROUTER>());
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static OncePerDevice once;
+  const int sms = device_sms();
+  if (!sms) return cudaErrorNoDevice;
+  const cudaError_t e0 = once_per_device(once, []() {
+    return cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)tc_smem<MODE_ROUTER>());
+  });
+  if (e0 != cudaSuccess) return e0;
   const int64_t T = wk.T;
   TcArgs a{};
   a.D = sh.D; a.F = sh.F; a.Fs = sh.Fs; a.T = (int)T; a.E = sh.E;
@@ -886,14 +881,10 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
                               void *tc_ws, cudaStream_t s) {
   const int64_t T = wk.T, P = T * sh.k;
   unsigned *st = status_word();
-  static int sms = 0;
-  static bool attr = false;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  }
-  if (!attr) {
+  static OncePerDevice once;
+  const int sms = device_sms();
+  if (!sms) return cudaErrorNoDevice;
+  const cudaError_t e0 = once_per_device(once, []() {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_GU>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_DN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_DN>());
@@ -905,9 +896,9 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
                                (int)tc_smem<MODE_DN, DS_Q4_K>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc_gemm_kernel<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<MODE_ROUTER>());
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+    return e;
+  });
+  if (e0 != cudaSuccess) return e0;
   const bool q4 = sh.fmt == DS_Q4_K;
   const int64_t bb = sh.block_bytes();
   const uint32_t raw_row = q4 ? TC_RAW_ROW_Q4 : TC_RAW_ROW;

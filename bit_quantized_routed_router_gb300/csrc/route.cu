@@ -367,16 +367,15 @@ cudaError_t launch_select_route(const Shape &sh, const Work &wk, const float *bi
   unsigned *st = status_word();
   const int64_t P = T * k;
   cudaError_t err;
-  static bool attrs = false;
-  if (!attrs) {  // up to 33E+1 ints (E <= 1024: 132 KB) of dynamic shared memory
-    err = cudaFuncSetAttribute(select_route_small_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, 140 * 1024);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 140 * 1024);
-    if (err != cudaSuccess) return err;
-    attrs = true;
-  }
+  static OncePerDevice once;
+  err = once_per_device(once, []() {  // up to 33E+1 ints (E <= 1024: 132 KB) of dynamic shared memory
+    cudaError_t e = cudaFuncSetAttribute(select_route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         140 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 140 * 1024);
+    return e;
+  });
+  if (err != cudaSuccess) return err;
   if (P <= ROUTE_CHUNK) {
     size_t smem = sizeof(int) * (size_t)(E + E + 1 + 32 * E);
     select_route_small_kernel<<<1, ROUTE_CHUNK, smem, s>>>(wk.logits, T, E, k, sh.routed_scale, sh.logit_scale, unbias,

@@ -228,19 +228,20 @@ int ds_moe_stack_mixed(const ds_moe_shape *shape, const ds_moe_weights *layers,
                        size_t errlen);
 
 /* ds_moe_layer for callers that cannot allocate device memory where they
- * call the layer -- for example code being captured into a CUDA graph, where
- * allocation calls are not allowed, or a plugin whose host program owns all
- * device memory through its own allocator.  It takes no workspace: its
- * scratch is a static 64 MiB device array inside this library, allocated on
- * each GPU when the library is loaded there and held until the process
+ * call the layer: a plugin or extension inside a host program whose own
+ * allocator owns all device memory, or a real-time loop that must not take
+ * cudaMalloc's implicit device-wide synchronisation.  It takes no workspace:
+ * its scratch is a static 64 MiB device array inside this library, allocated
+ * on each GPU when the library is loaded there and held until the process
  * exits.  The pages have no counterpart to this entry point.
- *   x, T, out, stream, err: as for ds_moe_layer (no debug outputs).
+ *   x, T, out, stream, err: as for ds_moe_layer (no debug outputs); the
+ *   arguments are validated in the same order, so T == 0 with bad weights
+ *   is rejected as ds_moe_layer rejects it.
  *   Rejects, with DS_ERR_INVALID_ARG and a message, any T whose
- *   ds_moe_workspace_bytes exceeds 64 MiB (at the 4096/256/6/2048 shape a
- *   batch of about 5 or more tokens takes the tensor-core path, whose scratch
- *   includes a 16.8 MB fp16 copy of the shared down matrix; the limit is then
- *   reached at about 200 tokens).  Allocates nothing: no cudaMalloc, no
- *   cudaFree.
+ *   ds_moe_workspace_bytes exceeds 64 MiB (at the 4096/256/6/2048 shape the
+ *   limit is reached at about 200 tokens; from 17 tokens the tensor-core
+ *   path's scratch includes a 16.8 MB fp16 copy of the shared down matrix).
+ *   Allocates nothing: no cudaMalloc, no cudaFree.
  *   The first call on a device looks up the array's device address with
  *   that device current; make that first call before any stream capture.
  *   Every call reuses the same array and leaves its contents behind; the
@@ -264,7 +265,9 @@ enum {
 int ds_moe_layer_path(const ds_moe_shape *shape, int64_t T, const void *x);
 
 /* Synchronise `stream`, then read and clear this device's sticky status
- * word.  Returns DS_OK, DS_ERR_TIMEOUT or DS_ERR_DEVICE_CHECK (with a message
+ * word (one atomic exchange on the device, so bits that kernels on other
+ * streams set meanwhile are not lost: they are reported by the next call).
+ * Returns DS_OK, DS_ERR_TIMEOUT or DS_ERR_DEVICE_CHECK (with a message
  * naming the check), or DS_ERR_CUDA if the stream itself failed. */
 int ds_moe_sync_status(void *stream, char *err, size_t errlen);
 
