@@ -71,43 +71,48 @@ def lib():
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() "
                                "(or python bit_quantized_routed_router_gb300/build.py)")
-        L = ctypes.CDLL(LIB_PATH)
-        vp, i64, sz, cp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_char_p
-        L.ds_moe_q2k_bytes.restype = sz
-        L.ds_moe_q2k_bytes.argtypes = [i64, i64]
-        L.ds_moe_q4k_bytes.restype = sz
-        L.ds_moe_q4k_bytes.argtypes = [i64, i64]
-        L.ds_moe_expert_bytes.restype = sz
-        L.ds_moe_expert_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
-        L.ds_moe_expert_bytes_fmt.restype = sz
-        L.ds_moe_expert_bytes_fmt.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
-        for f in (L.ds_moe_quantize_q2k, L.ds_moe_dequantize_q2k, L.ds_moe_quantize_q4k,
-                  L.ds_moe_dequantize_q4k):
-            f.restype = ctypes.c_int
-            f.argtypes = [vp, i64, i64, vp, vp, cp, sz]
-        L.ds_moe_workspace_bytes.restype = ctypes.c_int
-        L.ds_moe_workspace_bytes.argtypes = [ctypes.POINTER(Shape), i64, ctypes.POINTER(sz), cp, sz]
-        L.ds_moe_layer.restype = ctypes.c_int
-        L.ds_moe_layer.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64, vp, vp,
-                                   sz, ctypes.POINTER(Debug), vp, cp, sz]
-        L.ds_moe_layer_hostio.restype = ctypes.c_int
-        L.ds_moe_layer_hostio.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64,
-                                          vp, vp, sz, vp, cp, sz]
-        L.ds_moe_stack.restype = ctypes.c_int
-        L.ds_moe_stack.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), ctypes.c_int32,
-                                   vp, i64, ctypes.c_float, vp, sz, vp, cp, sz]
-        L.ds_moe_stack_mixed.restype = ctypes.c_int
-        L.ds_moe_stack_mixed.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp,
-                                         ctypes.c_int32, vp, i64, ctypes.c_float, vp, sz, vp, cp, sz]
-        L.ds_moe_layer_noalloc.restype = ctypes.c_int
-        L.ds_moe_layer_noalloc.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64,
-                                           vp, vp, cp, sz]
-        L.ds_moe_sync_status.restype = ctypes.c_int
-        L.ds_moe_sync_status.argtypes = [vp, cp, sz]
-        L.ds_moe_version.restype = ctypes.c_char_p
-        L.ds_moe_version.argtypes = []
-        _lib = L
+        _lib = load(LIB_PATH)
     return _lib
+
+
+def load(path: str):
+    """A build of the library at `path` (ctypes handle with its signatures)."""
+    L = ctypes.CDLL(path)
+    vp, i64, sz, cp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_char_p
+    L.ds_moe_q2k_bytes.restype = sz
+    L.ds_moe_q2k_bytes.argtypes = [i64, i64]
+    L.ds_moe_q4k_bytes.restype = sz
+    L.ds_moe_q4k_bytes.argtypes = [i64, i64]
+    L.ds_moe_expert_bytes.restype = sz
+    L.ds_moe_expert_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    L.ds_moe_expert_bytes_fmt.restype = sz
+    L.ds_moe_expert_bytes_fmt.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+    for f in (L.ds_moe_quantize_q2k, L.ds_moe_dequantize_q2k, L.ds_moe_quantize_q4k,
+              L.ds_moe_dequantize_q4k):
+        f.restype = ctypes.c_int
+        f.argtypes = [vp, i64, i64, vp, vp, cp, sz]
+    L.ds_moe_workspace_bytes.restype = ctypes.c_int
+    L.ds_moe_workspace_bytes.argtypes = [ctypes.POINTER(Shape), i64, ctypes.POINTER(sz), cp, sz]
+    L.ds_moe_layer.restype = ctypes.c_int
+    L.ds_moe_layer.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64, vp, vp,
+                               sz, ctypes.POINTER(Debug), vp, cp, sz]
+    L.ds_moe_layer_hostio.restype = ctypes.c_int
+    L.ds_moe_layer_hostio.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64,
+                                      vp, vp, sz, vp, cp, sz]
+    L.ds_moe_stack.restype = ctypes.c_int
+    L.ds_moe_stack.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), ctypes.c_int32,
+                               vp, i64, ctypes.c_float, vp, sz, vp, cp, sz]
+    L.ds_moe_stack_mixed.restype = ctypes.c_int
+    L.ds_moe_stack_mixed.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp,
+                                     ctypes.c_int32, vp, i64, ctypes.c_float, vp, sz, vp, cp, sz]
+    L.ds_moe_layer_noalloc.restype = ctypes.c_int
+    L.ds_moe_layer_noalloc.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights), vp, i64,
+                                       vp, vp, cp, sz]
+    L.ds_moe_sync_status.restype = ctypes.c_int
+    L.ds_moe_sync_status.argtypes = [vp, cp, sz]
+    L.ds_moe_version.restype = ctypes.c_char_p
+    L.ds_moe_version.argtypes = []
+    return L
 
 
 def _call(fn, *args):

@@ -33,8 +33,8 @@ def _newest(paths):
     return max(os.path.getmtime(p) for p in paths)
 
 
-def _compile(src, extra):
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src, extra, suffix=""):
+    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + suffix + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= _newest([src] + headers()):
         return obj
     cmd = ["nvcc"] + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
@@ -56,6 +56,27 @@ def build(verbose_ptxas: bool = False) -> str:
         cmd = ["nvcc"] + ARCH + ["-shared", "-o", LIB] + objs
         subprocess.check_call(cmd)
     return LIB
+
+
+HOOKS_LIB = os.path.join(BUILD, "libds_moe_test_hooks.so")
+
+
+def build_test_hooks() -> str:
+    """A second library for the tests only: the same objects, except that the
+    decode kernels are compiled with DS_MOE_TEST_HOOKS (a hook that holds the
+    route so that the device waits for it run out, and ds_moe_test_hooks to
+    set it).  The product library never contains the hook."""
+    build()
+    srcs = sources()
+    objs = []
+    for s in srcs:
+        if os.path.basename(s) == "decode_fast.cu":
+            objs.append(_compile(s, ["-DDS_MOE_TEST_HOOKS"], suffix="_hooks"))
+        else:
+            objs.append(os.path.join(BUILD, os.path.basename(s)[:-3] + ".o"))
+    if not os.path.exists(HOOKS_LIB) or os.path.getmtime(HOOKS_LIB) < _newest(objs):
+        subprocess.check_call(["nvcc"] + ARCH + ["-shared", "-o", HOOKS_LIB] + objs)
+    return HOOKS_LIB
 
 
 if __name__ == "__main__":

@@ -43,6 +43,25 @@
 namespace dsm {
 namespace {
 
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bound of every wait
+
+#ifdef DS_MOE_TEST_HOOKS
+// Test build only (never in the library the product loads): bit 0 of
+// g_test_hook_flags keeps the route from being published to the block, so
+// that every wait for it runs out, and a nonzero g_test_hook_limit_ns
+// replaces the bound of the waits for the route, the ring stages and the grid
+// barrier (the final wait for a block's own copies keeps the full bound).
+__device__ unsigned g_test_hook_flags;
+__device__ unsigned long long g_test_hook_limit_ns;
+__device__ __forceinline__ uint64_t wait_limit() {
+  return g_test_hook_limit_ns ? (uint64_t)g_test_hook_limit_ns : WAIT_LIMIT_NS;
+}
+__device__ __forceinline__ bool hold_route() { return (g_test_hook_flags & 1u) != 0; }
+#else
+__device__ __forceinline__ uint64_t wait_limit() { return WAIT_LIMIT_NS; }
+__device__ __forceinline__ bool hold_route() { return false; }
+#endif
+
 constexpr int PMAXD = 32;          // token-expert pairs this path serves (one per lane)
 constexpr int NW2 = 12, NW3 = 12;  // warps per CTA of K2 and K3
 constexpr size_t SMEM_LIMIT = 227 * 1024;
@@ -349,7 +368,7 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
     s_w[lane] = r.w;
     __threadfence_block();
     __syncwarp();
-    if (lane == 0) s_ready = 1;
+    if (lane == 0 && !hold_route()) s_ready = 1;
   }
 
   const int n_sh = a.Fs > 0 ? 4 * a.Fs : 0;    // shared items: (row, quarter of n_embd)
@@ -386,7 +405,7 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
       if (lane == 0) {  // bounded wait for this CTA's route
         const uint64_t t0 = globaltimer_ns();
         while (!s_ready) {
-          if (globaltimer_ns() - t0 > 2000000000ull) { flag(a.status, ST_TIMEOUT); ok = 0; break; }
+          if (globaltimer_ns() - t0 > wait_limit()) { flag(a.status, ST_TIMEOUT); ok = 0; break; }
           __nanosleep(64);
         }
       }
@@ -605,7 +624,7 @@ constexpr int S_GU = S_CONS;                     // routed gate/up rows per tile
 constexpr int S_MAXP = 64;                       // slots x rows of a phase-B tile
 constexpr int S_MAXK = 8;                        // top-k at most
 constexpr int S_MAXT = 16;                       // shared or phase-B tiles of one block
-constexpr uint64_t S_LIMIT_NS = 2000000000ull;   // bound of every wait
+constexpr uint64_t S_LIMIT_NS = WAIT_LIMIT_NS;    // bound of every wait
 
 struct StreamShared {
   uint64_t full[S_NS], empty[S_NS];
@@ -632,7 +651,7 @@ __device__ bool s_wait(uint64_t *bar, uint32_t par, StreamShared &S, unsigned *s
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait_sleep(bar, par, 20000u)) {  // sleeps until the phase completes (20 us at most)
     if (vload(&S.abort_)) return false;
-    if (globaltimer_ns() - t0 > S_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > wait_limit()) {
       flag(status, ST_TIMEOUT);
       *(volatile int *)&S.abort_ = 1;
       return false;
@@ -646,7 +665,7 @@ __device__ bool s_wait_ready(StreamShared &S, unsigned *status) {
   const uint64_t t0 = globaltimer_ns();
   while (!vload(&S.ready)) {
     if (vload(&S.abort_)) return false;
-    if (globaltimer_ns() - t0 > S_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > wait_limit()) {
       flag(status, ST_TIMEOUT);
       *(volatile int *)&S.abort_ = 1;
       return false;
@@ -747,7 +766,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
     if (lane == 0) S.rt_nu = r.nu;
     __threadfence_block();
     __syncwarp();
-    if (lane == 0) *(volatile int *)&S.ready = 1;
+    if (lane == 0 && !hold_route()) *(volatile int *)&S.ready = 1;
     return;
   }
 
@@ -761,7 +780,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
     {
       const uint64_t t0 = globaltimer_ns();
       while (!vload(&S.lg_loaded) && !vload(&S.abort_)) {
-        if (globaltimer_ns() - t0 > S_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > wait_limit()) {
           flag(a.status, ST_TIMEOUT);
           *(volatile int *)&S.abort_ = 1;
           ok = false;
@@ -943,7 +962,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       atom_add_release(a.ctrl + C_BAR, 1u);
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire(a.ctrl + C_BAR) < (unsigned)G) {
-        if (globaltimer_ns() - t0 > S_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > wait_limit()) {
           flag(a.status, ST_TIMEOUT);
           fine = false;
           break;
@@ -1282,3 +1301,13 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
 }
 
 }  // namespace dsm
+
+#ifdef DS_MOE_TEST_HOOKS
+// Test build only: sets the hooks above on the current device (flags bit 0:
+// hold the route; limit_ns: the shortened bound, 0 = the normal one).
+extern "C" int ds_moe_test_hooks(unsigned flags, unsigned long long limit_ns) {
+  cudaError_t e = cudaMemcpyToSymbol(dsm::g_test_hook_flags, &flags, sizeof flags);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(dsm::g_test_hook_limit_ns, &limit_ns, sizeof limit_ns);
+  return e == cudaSuccess ? 0 : -3;
+}
+#endif
