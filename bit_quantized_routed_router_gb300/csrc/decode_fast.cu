@@ -1227,12 +1227,7 @@ static bool fused_shape_ok(const Shape &sh, int64_t T) {
 }
 
 bool fused_decode_supported(const Shape &sh, int64_t T) {
-  // Q4_K: the streaming kernel only.  The three-kernel chain has Q4_K
-  // instantiations (launch_all<Q4Rows...>) that have not yet been checked
-  // against the oracle on a GPU; until they are, other Q4_K batches take the
-  // grouped GEMV path
-  if (sh.fmt == DS_Q4_K) return stream_decode_supported(sh, T);
-  if (sh.fmt != DS_Q2_K || !fused_shape_ok(sh, T)) return false;
+  if ((sh.fmt != DS_Q2_K && sh.fmt != DS_Q4_K) || !fused_shape_ok(sh, T)) return false;
   return k2_smem(sh.fmt, (int)T, sh.D) <= SMEM_LIMIT - 4096 &&
          k3_smem(sh.fmt, (int)T, sh.k, sh.F, sh.Fs) <= SMEM_LIMIT - 4096;
 }

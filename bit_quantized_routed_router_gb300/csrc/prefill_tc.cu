@@ -855,10 +855,7 @@ cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const voi
 }
 
 bool prefill_tc_supported(const Shape &sh, int64_t T) {
-  // Q4_K tiles (tc_gemm_kernel<MODE, DS_Q4_K>) are compiled but have not
-  // yet been checked against the oracle on a GPU: Q4_K batches keep the
-  // grouped GEMV path until they are
-  if (sh.fmt != DS_Q2_K) return false;
+  if (sh.fmt != DS_Q2_K && sh.fmt != DS_Q4_K) return false;
   if (T < TC_MIN_T || T > (int64_t)1 << 24) return false;
   if (sh.x_dtype != DS_BF16 || sh.router_dtype != DS_BF16) return false;
   if (sh.D % 1024 || sh.F % 1024 || sh.Fs % TC_BM) return false;  // whole 4-block groups: raw copies stay inside rows

@@ -180,15 +180,18 @@ int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, 
  * T == 0 is a no-op.  The kernels that run depend on T and the shape (see
  * ds_moe_layer_path): one token at the instantiated widths with top_k <= 8
  * streams the whole layer through one cooperative kernel; up to four tokens
- * (and one token otherwise) use a three-kernel
- * decode chain; T >= 5 with bf16 x and router and n_embd, n_ff multiples of
- * 1024 runs the expert FFNs as grouped tcgen05 GEMMs with fp16 operands
- * (dequantised weights and activations rounded once to fp16; an |x| or
- * intermediate above 65504 is saturated and reported by ds_moe_sync_status
- * as DS_ERR_DEVICE_CHECK); every other case uses the grouped dequantising
- * GEMV path with fp32 arithmetic.  With Q4_K experts one token at the
- * streaming kernel's widths (top_k <= 8) runs that kernel, every other batch
- * the grouped GEMV path. */
+ * (and one token otherwise) use a three-kernel decode chain; both compute
+ * the routed rows as exact integer dots on 16-bit fixed-point activations.
+ * 5..16 tokens with Q2_K experts, bf16 x and router and n_embd, n_ff,
+ * n_ff_shared multiples of 1024 run the batched decode kernels (the same
+ * integer dots; the shared expert on the tensor cores with exact bf16
+ * products).  Larger batches with bf16 x and router and n_embd, n_ff
+ * multiples of 1024 (Q4_K experts: from five tokens) run the expert FFNs as
+ * grouped tcgen05 GEMMs with fp16 operands (dequantised weights and
+ * activations rounded once to fp16; an |x| or intermediate above 65504 is
+ * saturated and reported by ds_moe_sync_status as DS_ERR_DEVICE_CHECK);
+ * every other case uses the grouped dequantising GEMV path with fp32
+ * arithmetic. */
 int ds_moe_layer(const ds_moe_shape *shape, const ds_moe_weights *weights, const void *x, int64_t T,
                  float *out, void *workspace, size_t workspace_bytes, const ds_moe_debug *dbg,
                  void *stream, char *err, size_t errlen);

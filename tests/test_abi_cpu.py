@@ -129,21 +129,26 @@ def test_quantize_rejects_bad_arguments_on_host(L):
 def test_layer_path_host_checks(L):
     sh = ds.MoEShape(4096, 256, 2048, 2048, 6)
     assert ds.layer_path(sh, 0) == ds.PATH_NONE
-    # 8 tokens: the tensor cores where the device has them (and the CUDA driver
-    # can build tensor maps), the grouped GEMV path on a host without a GPU
+    # 8 tokens: the batched decode kernels where the device has them (and the
+    # CUDA driver can build tensor maps), the grouped GEMV path on a host
+    # without a GPU
     import torch
-    expect = ds.PATH_TENSOR_CORE if torch.cuda.is_available() else ds.PATH_GROUPED_GEMV
-    assert ds.layer_path(sh, 8) == expect
+    gpu = torch.cuda.is_available()
+    assert ds.layer_path(sh, 8) == (ds.PATH_BATCHED_DECODE if gpu else ds.PATH_GROUPED_GEMV)
+    assert ds.layer_path(sh, 3) == ds.PATH_DECODE3
     with pytest.raises(ds.DsMoeError):
         ds.layer_path(ds.MoEShape(4000, 256, 2048, 2048, 6), 4)
     with pytest.raises(ds.DsMoeError):
         ds.layer_path(sh, -1)
-    # Q4_K experts: the streaming kernel for one token where a device can
-    # run it, the grouped GEMV path otherwise and at every other batch size
+    # Q4_K experts: the streaming kernel for one token where a device can run
+    # it (else the three-kernel chain), the chain up to four tokens, the
+    # tensor cores beyond (the grouped GEMV path without a device)
     q4 = ds.MoEShape(4096, 256, 2048, 2048, 6, expert_format=ds.DS_Q4_K)
-    assert ds.layer_path(q4, 1) == (ds.PATH_STREAM if torch.cuda.is_available() else ds.PATH_GROUPED_GEMV)
-    for T in (2, 4, 8, 4096):
-        assert ds.layer_path(q4, T) == ds.PATH_GROUPED_GEMV
+    assert ds.layer_path(q4, 1) == (ds.PATH_STREAM if gpu else ds.PATH_DECODE3)
+    for T in (2, 4):
+        assert ds.layer_path(q4, T) == ds.PATH_DECODE3
+    for T in (8, 4096):
+        assert ds.layer_path(q4, T) == (ds.PATH_TENSOR_CORE if gpu else ds.PATH_GROUPED_GEMV)
 
 
 def test_stack_mixed_rejects_bad_format_before_launch(L):

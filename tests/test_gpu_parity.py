@@ -548,15 +548,48 @@ def test_q4k_dequantize_bit_exact():
 
 @pytest.mark.parametrize("T,Fs,k,E,dtype,D", [(8, 0, 2, 16, "f32", 1024), (1, 512, 6, 16, "bf16", 1024),
                                               (1, 0, 8, 16, "f32", 1024), (1, 256, 2, 16, "f32", 512),
-                                              (3, 256, 2, 16, "f32", 1024), (33, 1024, 4, 40, "bf16", 1024)])
+                                              (3, 256, 2, 16, "f32", 1024), (2, 512, 6, 16, "bf16", 1024),
+                                              (4, 256, 4, 40, "f32", 1024), (33, 1024, 4, 40, "bf16", 1024)])
 def test_q4k_layer_parity(T, Fs, k, E, dtype, D):
-    """One token at the instantiated widths runs the streaming kernel with
-    Q4_K rows (integer dots on 4-bit codes); other widths and batches the
-    grouped GEMV path."""
+    """Q4_K experts on every decode-sized path: one token at the instantiated
+    widths runs the streaming kernel, two to four tokens the three-kernel
+    chain (integer dots on 4-bit codes), fp32 inputs beyond that the grouped
+    GEMV path and bf16 inputs of five tokens or more the tensor cores."""
     from dataclasses import replace
     cfg = replace(_small(T, Fs, k, E, dtype), expert_fmt="q4k", D=D, F=D)
-    path = ds.PATH_STREAM if (T == 1 and D == 1024) else ds.PATH_GROUPED_GEMV
-    assert ds.layer_path(synthetic.shape_of(cfg), T) == path
+    sh = synthetic.shape_of(cfg)
+    if D == 1024 and T == 1:
+        path = ds.PATH_STREAM
+    elif D == 1024 and T <= 4:
+        path = ds.PATH_DECODE3
+    elif dtype == "bf16" and T >= 5:
+        path = ds.PATH_TENSOR_CORE
+    else:
+        path = ds.PATH_GROUPED_GEMV
+    assert ds.layer_path(sh, T) == path
+    layer_parity(cfg, DECODE_TOL)
+
+
+@pytest.mark.parametrize("T,Fs,k,E,zipf", [(64, 1024, 2, 8, 0.0), (300, 1024, 4, 16, 0.0),
+                                            (520, 1024, 6, 32, 1.1), (200, 0, 6, 40, 0.0)])
+def test_q4k_tensor_core_path(T, Fs, k, E, zipf):
+    """Q4_K experts on the tensor cores (the 144-byte blocks copied whole,
+    dequantised to fp16 by the dequant warps): the whole output against the
+    oracle at the prefill tolerance, including several 128-token chunks per
+    expert, a Zipf route and no shared expert."""
+    from dataclasses import replace
+    cfg = replace(_tc(T, Fs, k, E, zipf, seed=9), expert_fmt="q4k")
+    assert ds.layer_path(synthetic.shape_of(cfg), T) == ds.PATH_TENSOR_CORE
+    layer_parity(cfg, PREFILL_TOL)
+
+
+def test_q4k_decode_sized_tensor_core_batch():
+    """A decode-sized Q4_K batch beyond the three-kernel chain with bf16
+    inputs (17 tokens at the Flash widths) on the tensor cores, at the decode
+    tolerance."""
+    from dataclasses import replace
+    cfg = replace(dsgen.DECODE1, T=17, expert_fmt="q4k")
+    assert ds.layer_path(synthetic.shape_of(cfg), cfg.T) == ds.PATH_TENSOR_CORE
     layer_parity(cfg, DECODE_TOL)
 
 
@@ -602,7 +635,7 @@ def test_q4k_decode_b1_flash_shape(decode1_q4k):
 
 def test_q4k_decode_b1_hostio_and_gemv_agree(decode1_q4k):
     """The one-token Q4_K layer from pinned host buffers equals the device
-    call bit for bit; the grouped GEMV path (a two-token batch of the same
+    call bit for bit; the three-kernel chain (a two-token batch of the same
     token twice) agrees within the decode tolerance."""
     cfg, W = decode1_q4k
     lo, att, x64 = oracle_case(cfg)
@@ -618,12 +651,12 @@ def test_q4k_decode_b1_hostio_and_gemv_agree(decode1_q4k):
     assert torch.equal(oh, out.cpu())
     x2 = torch.cat([x, x])
     out2 = torch.empty((2, cfg.D), dtype=torch.float32, device="cuda")
-    assert ds.layer_path(sh, 2) == ds.PATH_GROUPED_GEMV
+    assert ds.layer_path(sh, 2) == ds.PATH_DECODE3
     ds.layer(sh, W, x2, out2, ws)
     ds.sync_status()
     assert torch.equal(out2[0], out2[1])
     ref = out2[0].cpu().numpy().astype(np.float64)
-    check_close(out.cpu().numpy()[0], ref, DECODE_TOL, "stream vs GEMV")
+    check_close(out.cpu().numpy()[0], ref, DECODE_TOL, "stream vs three-kernel chain")
 
 
 def test_q4k_mixed_stack_by_layer():
