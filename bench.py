@@ -27,6 +27,7 @@ import statistics
 import subprocess
 import sys
 import time
+from dataclasses import replace
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 for _p in (ROOT, os.path.join(ROOT, "gen")):
@@ -381,6 +382,64 @@ def time_stack(cfg, iters, dev, warmup=3):
     return e0.elapsed_time(e1) / iters, b, used, path
 
 
+def time_resident(cfg, R, budgets, n_tokens, dev):
+    """One-token decode with the routed experts of R layers in pinned host
+    memory and a device cache (ds_moe_cache_layer) holding a fraction of
+    them: per budget, ms per layer call (wall clock: every call reads back
+    its route to update the cache), the hit rate and the bytes the calls
+    read from host memory.  One warm-up pass of n_tokens tokens through the
+    R layers, then one timed pass of other tokens."""
+    import torch
+    import bit_quantized_routed_router_gb300 as ds
+    from bit_quantized_routed_router_gb300 import synthetic
+    from dataclasses import replace
+
+    sh = synthetic.shape_of(cfg)
+    eb = cfg.expert_bytes
+    Ws, hosts = [], []
+    for r in range(R):
+        W = synthetic.build_layer(cfg, layer=r, device=dev)
+        h = torch.empty(W.experts.shape, dtype=W.experts.dtype, pin_memory=True)
+        h.copy_(W.experts)
+        hosts.append(h)
+        Ws.append(replace(W, experts=None))  # the device copy is dropped
+        del W
+    torch.cuda.empty_cache()
+    ws = torch.empty(ds.workspace_bytes(sh, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty((1, cfg.D), dtype=torch.float32, device=dev)
+    res = {}
+    for frac in budgets:
+        n_slots = int(round(frac * R * cfg.E))
+        slots = torch.empty((max(n_slots, 1), eb), dtype=torch.uint8, device=dev)
+        tables = torch.empty((R, cfg.E), dtype=torch.int32, device=dev)
+        c = ds.ExpertCache(sh, hosts, slots, n_slots, tables)
+        for t in range(n_tokens):
+            x = synthetic.build_x(cfg, layer=1000 + t, device=dev)
+            for r in range(R):
+                c.layer(r, Ws[r], x, out, ws)
+        xs = [synthetic.build_x(cfg, layer=2000 + t, device=dev) for t in range(n_tokens)]
+        ds.sync_status()
+        st0 = c.stats()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for t in range(n_tokens):
+            for r in range(R):
+                c.layer(r, Ws[r], xs[t], out, ws)
+        torch.cuda.synchronize(dev)
+        ms = (time.perf_counter() - t0) * 1e3 / (n_tokens * R)
+        ds.sync_status()
+        st1 = c.stats()
+        hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
+        res[f"{frac:g}"] = {"slots": n_slots, "cache_gb": n_slots * eb / 1e9, "ms_per_layer": ms,
+                            "tokens_per_s_per_layer": 1e3 / ms, "hit_rate": hits / max(1, hits + misses),
+                            "host_expert_bytes_per_call": misses * eb / (n_tokens * R)}
+        c.close()
+        del slots, tables
+        torch.cuda.empty_cache()
+    del Ws, hosts, ws, out
+    return res
+
+
 def extra_workloads(args, dev):
     """The other timed workloads of the metric (not the headline line):
     prefill T=4096 (uniform and Zipf router) against the bf16 tensor roofline,
@@ -393,7 +452,8 @@ def extra_workloads(args, dev):
 
     pk, pk_kind = peaks()
     res = {}
-    for cfg, iters in ((dsgen.PREFILL, 10), (dsgen.PREFILL_ZIPF, 10), (dsgen.DECODE32_ZIPF, 200)):
+    for cfg, iters in ((dsgen.PREFILL, 10), (dsgen.PREFILL_ZIPF, 10), (PREFILL_Q4K, 10),
+                       (dsgen.DECODE32_ZIPF, 200)):
         if cfg.T < 64:  # decode-sized: rotate four layers (inputs larger than L2), graph-timed
             ms, used, path = time_decode_rotating(cfg, 4, iters, dev)
         else:
@@ -424,6 +484,11 @@ def extra_workloads(args, dev):
                      "timing": "CUDA graph of 20 calls rotating over 2 layers",
                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                                   "frac": gbs / hbm, "peak_source": pk_kind, "algorithmic_bytes": b}}
+    cfg = RESIDENT
+    res[cfg.name] = {"T": 1, "layers": 2, "budgets": time_resident(cfg, 2, (0.0, 0.25, 1.0), 24, dev),
+                     "timing": "wall clock per ds_moe_cache_layer call (each reads back its route); "
+                               "budget = fraction of the layers' experts that fit in device slots",
+                     "experts": "routed experts in pinned host memory, read in place when not cached"}
     cfg = dsgen.STACK
     ms, b, used, path = time_stack(cfg, 20, dev)
     gbs = b / (ms / 1e3) / 1e9
@@ -438,6 +503,11 @@ def extra_workloads(args, dev):
     return res
 
 
+PREFILL_Q4K = replace(dsgen.PREFILL, name="prefill T=4096 Q4_K experts D=4096 E=256 k=6 F=2048 Fs=2048",
+                      expert_fmt="q4k")
+RESIDENT = replace(dsgen.DECODE1, name="decode T=1 experts in host memory, device cache, zipf(1.1) "
+                                       "D=4096 E=256 k=6 F=2048 Fs=2048", zipf_s=1.1)
+
 # single workloads for profiling runs (not the benchmark line)
 WORKLOADS = {
     "prefill": dsgen.PREFILL,
@@ -445,6 +515,8 @@ WORKLOADS = {
     "decode32": dsgen.DECODE32_ZIPF,
     "stack": dsgen.STACK,
     "decode_q4k": dsgen.DECODE1_Q4K,
+    "prefill_q4k": PREFILL_Q4K,
+    "resident": RESIDENT,
     # same shapes at 1/4 of the experts and tokens (about 96 tokens per
     # expert as at full size): a case small enough for full profiler captures
     "prefill_small": None,
@@ -579,6 +651,10 @@ def main():
                                                   warmup=args.warmup)
             print(json.dumps({"workload": cfg.name, "ms_per_layer": ms, "tokens_per_s": cfg.T / (ms / 1e3),
                               "used_experts": used, "path": path, "steps": args.steps}), flush=True)
+            return
+        if args.workload == "resident":
+            r = time_resident(cfg, 2, (0.0, 0.25, 1.0), max(2, args.steps), torch.device("cuda", 0))
+            print(json.dumps({"workload": cfg.name, "budgets": r}), flush=True)
             return
         if args.workload == "stack":
             ms, b, used, path = time_stack(cfg, args.steps, torch.device("cuda", 0), warmup=args.warmup)

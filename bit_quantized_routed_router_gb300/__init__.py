@@ -28,7 +28,9 @@ SYMBOLS = ["ds_moe_q2k_bytes", "ds_moe_expert_bytes", "ds_moe_quantize_q2k",
            "ds_moe_layer_hostio", "ds_moe_stack", "ds_moe_sync_status", "ds_moe_version",
            "ds_moe_layer_noalloc", "ds_moe_layer_path", "ds_moe_q4k_bytes",
            "ds_moe_expert_bytes_fmt", "ds_moe_quantize_q4k", "ds_moe_dequantize_q4k",
-           "ds_moe_stack_mixed"]
+           "ds_moe_stack_mixed", "ds_moe_layer_resident", "ds_moe_layer_path_resident",
+           "ds_moe_cache_create", "ds_moe_cache_destroy", "ds_moe_cache_layer", "ds_moe_cache_record",
+           "ds_moe_cache_slot", "ds_moe_cache_stats"]
 
 # ds_moe_layer_path results
 PATH_NONE, PATH_STREAM, PATH_DECODE3, PATH_GROUPED_GEMV, PATH_TENSOR_CORE, PATH_BATCHED_DECODE = 0, 1, 2, 3, 4, 5
@@ -53,6 +55,10 @@ class Weights(ctypes.Structure):
     _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("shared_gate", ctypes.c_void_p), ("shared_up", ctypes.c_void_p),
                 ("shared_down", ctypes.c_void_p), ("experts", ctypes.c_void_p)]
+
+
+class Residency(ctypes.Structure):
+    _fields_ = [("slot", ctypes.c_void_p), ("cache", ctypes.c_void_p), ("experts_host", ctypes.c_void_p)]
 
 
 class Debug(ctypes.Structure):
@@ -112,6 +118,26 @@ def load(path: str):
     L.ds_moe_sync_status.argtypes = [vp, cp, sz]
     L.ds_moe_version.restype = ctypes.c_char_p
     L.ds_moe_version.argtypes = []
+    L.ds_moe_layer_resident.restype = ctypes.c_int
+    L.ds_moe_layer_resident.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Weights),
+                                        ctypes.POINTER(Residency), vp, i64, vp, vp, sz,
+                                        ctypes.POINTER(Debug), vp, cp, sz]
+    L.ds_moe_layer_path_resident.restype = ctypes.c_int
+    L.ds_moe_layer_path_resident.argtypes = [ctypes.POINTER(Shape), i64]
+    L.ds_moe_cache_create.restype = ctypes.c_int
+    L.ds_moe_cache_create.argtypes = [ctypes.POINTER(Shape), ctypes.c_int32, ctypes.POINTER(vp), vp, i64,
+                                      vp, ctypes.POINTER(vp), cp, sz]
+    L.ds_moe_cache_destroy.restype = None
+    L.ds_moe_cache_destroy.argtypes = [vp]
+    L.ds_moe_cache_layer.restype = ctypes.c_int
+    L.ds_moe_cache_layer.argtypes = [vp, ctypes.c_int32, ctypes.POINTER(Weights), vp, i64, vp, vp, sz, vp,
+                                     cp, sz]
+    L.ds_moe_cache_record.restype = ctypes.c_int
+    L.ds_moe_cache_record.argtypes = [vp, ctypes.c_int32, vp, vp, ctypes.POINTER(ctypes.c_int32)]
+    L.ds_moe_cache_slot.restype = ctypes.c_int
+    L.ds_moe_cache_slot.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+    L.ds_moe_cache_stats.restype = ctypes.c_int
+    L.ds_moe_cache_stats.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64)]
     return L
 
 
@@ -248,6 +274,91 @@ def layer_noalloc(shape: MoEShape, weights: MoEWeights, x, out, stream=None, T: 
     T = x.shape[0] if T is None else T
     _call(lib().ds_moe_layer_noalloc, ctypes.byref(shape.c()), ctypes.byref(weights.c()),
           x.data_ptr(), T, out.data_ptr(), _stream(stream))
+
+
+def layer_resident(shape: MoEShape, weights: MoEWeights, slot, cache, experts_host, x, out, workspace,
+                   debug: dict | None = None, stream=None, T: int | None = None):
+    """layer() with the routed experts read through a residency view: slot [E]
+    int32 (device, -1 = host), cache (device slots or None), experts_host (a
+    pinned host tensor of the E packed experts)."""
+    T = x.shape[0] if T is None else T
+    dbg = None
+    if debug is not None:
+        dbg = ctypes.byref(Debug(*[_ptr(debug.get(n)) for n in
+                                   ("logits", "ids", "w", "counts", "offsets", "perm")]))
+    res = Residency(_ptr(slot), _ptr(cache), _ptr(experts_host))
+    _call(lib().ds_moe_layer_resident, ctypes.byref(shape.c()), ctypes.byref(weights.c()), ctypes.byref(res),
+          x.data_ptr(), T, out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+          dbg, _stream(stream))
+
+
+def layer_path_resident(shape: MoEShape, T: int) -> int:
+    rc = lib().ds_moe_layer_path_resident(ctypes.byref(shape.c()), T)
+    if rc < 0:
+        raise DsMoeError(rc, "invalid shape or T")
+    return rc
+
+
+class ExpertCache:
+    """A cache of routed experts in device slots for n_layers layers (the C
+    object ds_moe_cache).  experts_host: per layer a pinned host tensor of the
+    E packed experts; slots: device tensor of n_slots experts (or None for a
+    planning-only cache); tables: device int32 tensor [n_layers][E] (or None)."""
+
+    def __init__(self, shape: MoEShape, experts_host, slots, n_slots: int, tables):
+        self._keep = list(experts_host)
+        arr = (ctypes.c_void_p * len(self._keep))(*[_host_ptr(h) for h in self._keep])
+        out = ctypes.c_void_p()
+        _call(lib().ds_moe_cache_create, ctypes.byref(shape.c()), len(self._keep), arr, _ptr(slots), n_slots,
+              _ptr(tables), ctypes.byref(out))
+        self.handle = out
+
+    def close(self):
+        if self.handle:
+            lib().ds_moe_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def layer(self, layer: int, weights: MoEWeights, x, out, workspace, stream=None, T: int | None = None):
+        T = x.shape[0] if T is None else T
+        _call(lib().ds_moe_cache_layer, self.handle, layer, ctypes.byref(weights.c()), x.data_ptr(), T,
+              out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+
+    def record(self, layer: int, counts):
+        """Host policy step: counts a host int32 array [E]; returns the (slot,
+        expert) fills it planned."""
+        import numpy as np
+        c = np.ascontiguousarray(counts, np.int32)
+        fills = np.empty(2 * c.size, np.int32)
+        n = ctypes.c_int32()
+        rc = lib().ds_moe_cache_record(self.handle, layer, c.ctypes.data, fills.ctypes.data, ctypes.byref(n))
+        if rc:
+            raise DsMoeError(rc, "cache record")
+        return [(int(fills[2 * j]), int(fills[2 * j + 1])) for j in range(n.value)]
+
+    def slot(self, layer: int, expert: int) -> int:
+        s = ctypes.c_int32()
+        rc = lib().ds_moe_cache_slot(self.handle, layer, expert, ctypes.byref(s))
+        if rc:
+            raise DsMoeError(rc, "cache slot")
+        return s.value
+
+    def stats(self):
+        h, m, r = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        lib().ds_moe_cache_stats(self.handle, ctypes.byref(h), ctypes.byref(m), ctypes.byref(r))
+        return {"hits": h.value, "misses": m.value, "resident": r.value}
+
+
+def _host_ptr(t):
+    """Address of a host buffer: a torch tensor or a numpy array."""
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    return t.ctypes.data
 
 
 def stack(shape: MoEShape, layers, x, workspace, eps: float = 1e-6, stream=None, formats=None):

@@ -139,11 +139,11 @@ size_t layout(const Shape &sh, int64_t T, char *base, Work *wk) {
   return off;
 }
 
-int check_weights(const Shape &sh, const ds_moe_weights *W, char *err, size_t errlen) {
+int check_weights(const Shape &sh, const ds_moe_weights *W, char *err, size_t errlen, bool need_experts = true) {
   if (!W) return fail(err, errlen, DS_ERR_INVALID_ARG, "weights is NULL");
-  if (!W->router_w || !W->experts)
+  if (!W->router_w || (need_experts && !W->experts))
     return fail(err, errlen, DS_ERR_INVALID_ARG, "router_w and experts are required");
-  if (!aligned(W->router_w, 16) || !aligned(W->experts, 16))
+  if (!aligned(W->router_w, 16) || (W->experts && !aligned(W->experts, 16)))
     return fail(err, errlen, DS_ERR_INVALID_ARG, "router_w / experts must be 16-byte aligned");
   if (W->router_bias && !aligned(W->router_bias, 4))
     return fail(err, errlen, DS_ERR_INVALID_ARG, "router_bias must be 4-byte aligned");
@@ -158,11 +158,18 @@ int check_weights(const Shape &sh, const ds_moe_weights *W, char *err, size_t er
 
 // One layer on device buffers: route, expert FFNs, combine into out.
 int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *out, bool accumulate,
-              const Work &wk, const ds_moe_debug *dbg, cudaStream_t s, char *err, size_t errlen) {
+              const Work &wk, const ds_moe_debug *dbg, cudaStream_t s, char *err, size_t errlen,
+              const Residency *res = nullptr) {
   cudaError_t e;
   if (fused_decode_supported(sh, wk.T)) {
-    if ((e = launch_decode_fused(sh, W, x, wk, out, accumulate, s)) != cudaSuccess)
+    if ((e = launch_decode_fused(sh, W, x, wk, out, accumulate, s, nullptr, res)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "fused decode layer");
+  } else if (res) {  // residency: the kernels that address each expert by pointer
+    if ((e = cudaMemsetAsync(wk.ctrl, 0, 256, s)) != cudaSuccess)
+      return cuda_fail(err, errlen, e, "workspace control reset");
+    if ((e = launch_route(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
+    if ((e = launch_decode_ffn(sh, W, x, wk, s, res)) != cudaSuccess) return cuda_fail(err, errlen, e, "expert FFN");
+    if ((e = launch_combine(sh, wk, out, accumulate, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "combine");
   } else if (wk.mt && aligned(x, 16) && decode_mt_supported(sh, wk.T)) {
     if ((e = launch_router_logits(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "router");
     if ((e = launch_decode_mt(sh, W, x, wk, out, accumulate, wk.mt, s)) != cudaSuccess)
@@ -210,6 +217,13 @@ int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *ou
 }
 
 }  // namespace
+
+int32_t *workspace_counts(const Shape &sh, int64_t T, void *workspace) {
+  Work wk;
+  layout(sh, T, (char *)workspace, &wk);
+  return wk.counts;
+}
+
 }  // namespace dsm
 
 using namespace dsm;
@@ -366,6 +380,49 @@ int ds_moe_layer_hostio(const ds_moe_shape *shape, const ds_moe_weights *weights
   return e == cudaSuccess ? DS_OK : cuda_fail(err, errlen, e, "copy out to host");
 }
 
+// Checks a residency view and turns it into the kernels' form (device view of
+// the host copy).
+static int residency_of(const Shape &sh, const ds_moe_residency *r, Residency *out, char *err, size_t errlen) {
+  if (!r) return fail(err, errlen, DS_ERR_INVALID_ARG, "residency is NULL");
+  if (!r->slot || !r->experts_host)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "residency needs a slot table and the host copy of the experts");
+  if (!aligned(r->slot, 4) || (r->cache && !aligned(r->cache, 16)))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "slot table must be 4-byte and cache 16-byte aligned");
+  const void *hv = device_view(r->experts_host);
+  if (!hv || !aligned(hv, 16))
+    return fail(err, errlen, DS_ERR_INVALID_ARG,
+                "experts_host must be 16-byte aligned host memory the device can address (pinned or registered)");
+  (void)sh;
+  *out = Residency{r->slot, r->cache, (const uint8_t *)hv};
+  return DS_OK;
+}
+
+int ds_moe_layer_resident(const ds_moe_shape *shape, const ds_moe_weights *weights,
+                          const ds_moe_residency *residency, const void *x, int64_t T, float *out,
+                          void *workspace, size_t workspace_bytes, const ds_moe_debug *dbg, void *stream,
+                          char *err, size_t errlen) {
+  Shape sh{};
+  int rc = check_shape(shape, err, errlen, &sh);
+  if (rc) return rc;
+  if ((rc = check_weights(sh, weights, err, errlen, false))) return rc;
+  Residency res{};
+  if ((rc = residency_of(sh, residency, &res, err, errlen))) return rc;
+  if (T < 0 || T > (1 << 24)) return fail(err, errlen, DS_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
+  if (T == 0) return DS_OK;
+  if (!x || !out || !workspace) return fail(err, errlen, DS_ERR_INVALID_ARG, "x, out and workspace are required");
+  if (!aligned(x, 16) || !aligned(out, 16))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  if (!aligned(workspace, ALIGN))
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = layout(sh, T, nullptr, nullptr);
+  if (workspace_bytes < need)
+    return fail(err, errlen, DS_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+  if (!status_word()) return fail(err, errlen, DS_ERR_CUDA, "no CUDA device");
+  Work wk;
+  layout(sh, T, (char *)workspace, &wk);
+  return run_layer(sh, *weights, x, out, false, wk, dbg, (cudaStream_t)stream, err, errlen, &res);
+}
+
 int ds_moe_stack_mixed(const ds_moe_shape *shape, const ds_moe_weights *layers,
                        const int32_t *formats, int32_t n_layers, float *x, int64_t T, float eps,
                        void *workspace, size_t workspace_bytes, void *stream, char *err,
@@ -459,6 +516,14 @@ int ds_moe_layer_path(const ds_moe_shape *shape, int64_t T, const void *x) {
   return DS_PATH_GROUPED_GEMV;
 }
 
-const char *ds_moe_version(void) { return "ds_moe 0.1 (sm_103a)"; }
+int ds_moe_layer_path_resident(const ds_moe_shape *shape, int64_t T) {
+  Shape sh;
+  if (check_shape(shape, nullptr, 0, &sh) != DS_OK || T < 0) return DS_ERR_INVALID_ARG;
+  if (T == 0) return DS_PATH_NONE;
+  if (fused_decode_supported(sh, T)) return stream_decode_supported(sh, T) ? DS_PATH_STREAM : DS_PATH_DECODE3;
+  return DS_PATH_GROUPED_GEMV;
+}
+
+const char *ds_moe_version(void) { return "ds_moe 0.2 (sm_103a)"; }
 
 }  // extern "C"

@@ -20,6 +20,8 @@ enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 struct GemvArgs {
   const uint8_t *experts;
   int64_t expert_bytes, off_a, off_b;  // gate|up (GU) or down (DN) offsets in a blob
+  const int32_t *slot;                 // residency: [E] cache slot or -1 (host copy); null: experts
+  const uint8_t *cache, *host;
   const uint16_t *sh_a, *sh_b;         // shared expert rows (bf16): gate, up | down
   const void *in;                      // GU: x [T][D] (x_dtype); DN: h [T*k][F] fp32
   const float *in_shared;              // DN: hs [T][Fs]
@@ -225,7 +227,12 @@ __global__ void __launch_bounds__(256) grouped_gemv_kernel(GemvArgs a) {
   if (r0 >= out_rows) return;
   const int stride4 = in_dim >> 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint8_t *blob = a.experts + (int64_t)e * a.expert_bytes;
+  // the expert's bytes: its cache slot, the host copy (ordinary loads) or
+  // the experts array; the same bytes either way
+  const int es = a.slot ? __ldg(a.slot + e) : 0;
+  const uint8_t *blob = !a.slot ? a.experts + (int64_t)e * a.expert_bytes
+                        : es >= 0 ? a.cache + (int64_t)es * a.expert_bytes
+                                  : a.host + (int64_t)e * a.expert_bytes;
   const int64_t row_bytes = (int64_t)((in_dim + QK - 1) / QK) * (FMT == DS_Q4_K ? Q4B : QB);
 
   for (int g0 = 0; g0 < n_tok; g0 += NT) {
@@ -352,10 +359,15 @@ cudaError_t launch_gemv(int fmt, const GemvArgs &a, int out_rows_max, int in_dim
 }  // namespace
 
 cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const void *x,
-                              const Work &wk, cudaStream_t s) {
+                              const Work &wk, cudaStream_t s, const Residency *res) {
   GemvArgs a{};
   a.experts = W.experts;
   a.expert_bytes = sh.expert_bytes();
+  if (res) {
+    a.slot = res->slot;
+    a.cache = res->cache;
+    a.host = res->host;
+  }
   a.offsets = wk.offsets;
   a.perm = wk.perm;
   a.used = wk.used;

@@ -82,6 +82,10 @@ struct Args {
   const uint16_t *sg, *su, *sd;
   const uint8_t *experts;
   int64_t expert_bytes, gate_bytes;
+  // expert residency (null slot: every expert at experts + e * expert_bytes)
+  const int32_t *slot;   // [E]: cache slot of expert e, or -1: read it from host
+  const uint8_t *cache;  // device slots of expert_bytes each
+  const uint8_t *host;   // device view of the host copy of all E experts
   const void *x;
   int x_f32;
   void *x_stage;  // non-null: x is host memory; the router grid copies it here for the streaming kernel
@@ -98,6 +102,19 @@ struct Args {
   unsigned *status;
   int n_slots;
 };
+
+// Packed bytes of expert e: its cache slot when it has one, else the host
+// copy (far = true: read with ordinary loads, never with bulk copies); without
+// a slot table the experts array.  The same bytes either way.
+__device__ __forceinline__ const uint8_t *expert_at(const Args &a, int e, bool &far) {
+  if (!a.slot) {
+    far = false;
+    return a.experts + (int64_t)e * a.expert_bytes;
+  }
+  const int s = __ldg(a.slot + e);
+  far = s < 0;
+  return far ? a.host + (int64_t)e * a.expert_bytes : a.cache + (int64_t)s * a.expert_bytes;
+}
 
 template <typename T>
 __device__ __forceinline__ void ld8(const T *p, float v[8]);
@@ -391,9 +408,12 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
       const int r = i - n_sh, slot = r / a.F, f = r % a.F;
       const int e = shfl(rc.used, min(slot, 31));
       if (slot < rc.nu && lane == 0) {
-        const uint8_t *g = a.experts + (int64_t)e * a.expert_bytes + (int64_t)f * rb;
-        bulk_prefetch_l2(g, (uint32_t)rb);
-        bulk_prefetch_l2(g + a.gate_bytes, (uint32_t)rb);
+        bool far;
+        const uint8_t *g = expert_at(a, e, far) + (int64_t)f * rb;
+        if (!far) {
+          bulk_prefetch_l2(g, (uint32_t)rb);
+          bulk_prefetch_l2(g + a.gate_bytes, (uint32_t)rb);
+        }
       }
     }
   };
@@ -446,7 +466,8 @@ __global__ void __launch_bounds__(NW2 * 32, 1) gateup_kernel(const Args a) {
     const int r = it - n_sh, slot = r / a.F, f = r % a.F;
     if (slot >= rc.nu) continue;
     const int e = shfl(rc.used, slot), base = shfl(rc.base, slot), n = shfl(rc.cnt, slot);
-    const uint8_t *grow = a.experts + (int64_t)e * a.expert_bytes + (int64_t)f * rb;
+    bool far;
+    const uint8_t *grow = expert_at(a, e, far) + (int64_t)f * rb;
     typename R::Row gp, up;
     R::load_g(grow, gp);
     R::load_g(grow + a.gate_bytes, up);
@@ -518,8 +539,11 @@ __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
   auto prefetch = [&](int d) {
     if (d >= a.D) return;
     const int e = shfl(rc.used, lane);
-    if (lane < rc.nu)
-      bulk_prefetch_l2(a.experts + (int64_t)e * a.expert_bytes + 2 * a.gate_bytes + (int64_t)d * er, (uint32_t)er);
+    if (lane < rc.nu) {
+      bool far;
+      const uint8_t *p = expert_at(a, e, far);
+      if (!far) bulk_prefetch_l2(p + 2 * a.gate_bytes + (int64_t)d * er, (uint32_t)er);
+    }
     if (lane == 31 && a.Fs > 0) bulk_prefetch_l2(a.sd + (int64_t)d * a.Fs, (uint32_t)a.Fs * 2u);
   };
   prefetch(gw);
@@ -554,8 +578,10 @@ __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
 #pragma unroll
       for (int v = 0; v < BATCH; ++v) {
         const int e = shfl(rc.used, min(u0 + v, 31));
-        if (u0 + v < rc.nu)
-          R::load_g(a.experts + (int64_t)e * a.expert_bytes + 2 * a.gate_bytes + (int64_t)d * er, rp[v]);
+        if (u0 + v < rc.nu) {
+          bool far;
+          R::load_g(expert_at(a, e, far) + 2 * a.gate_bytes + (int64_t)d * er, rp[v]);
+        }
       }
       for (int j = 0; j < a.T; ++j) {  // j-th pair of every expert of the batch
         float y[BATCH];
@@ -818,14 +844,15 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
         const int r = rbid + G * jr++, u = r / ngrp, g = r % ngrp;
         S.tile[st] = -1 - r;
         const int rows = min(S_GU, F - g * S_GU);
-        if (u < S.rt_nu) {
-          const uint8_t *gr = a.experts + (int64_t)S.rt_used[u] * a.expert_bytes + (int64_t)g * S_GU * rowb_d;
+        bool far = false;
+        const uint8_t *gr = u < S.rt_nu ? expert_at(a, S.rt_used[u], far) + (int64_t)g * S_GU * rowb_d : nullptr;
+        if (u < S.rt_nu && !far) {
           const uint32_t bytes = (uint32_t)(rows * rowb_d);
           mbar_arrive_expect_tx(full, 2 * bytes);
           bulk_g2s(dst, gr, bytes, full);
           bulk_g2s(dst + S_GU * rowb_d, gr + a.gate_bytes, bytes, full);
         } else {
-          mbar_arrive(full);
+          mbar_arrive(full);  // nothing to copy (an expert in host memory: the consumers load its rows)
         }
       }
       ++kq;
@@ -838,12 +865,19 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       uint64_t *full = &S.full[kq % S_NS];
       const int d0 = (bid + G * m) * rb, nu = S.rt_nu;
       const uint32_t sb = (uint32_t)(rb * 2 * Fs), ub = (uint32_t)(rb * rowb_f);
-      mbar_arrive_expect_tx(full, sb + (uint32_t)nu * ub);
+      uint32_t near_bytes = 0;
+      for (int u = 0; u < nu; ++u) {
+        bool far;
+        (void)expert_at(a, S.rt_used[u], far);
+        if (!far) near_bytes += ub;
+      }
+      mbar_arrive_expect_tx(full, sb + near_bytes);
       if (Fs > 0) bulk_g2s(dst, a.sd + (size_t)d0 * Fs, sb, full);
-      for (int u = 0; u < nu; ++u)
-        bulk_g2s(dst + sb + (size_t)u * ub,
-                 a.experts + (int64_t)S.rt_used[u] * a.expert_bytes + 2 * a.gate_bytes + (int64_t)d0 * rowb_f,
-                 ub, full);
+      for (int u = 0; u < nu; ++u) {
+        bool far;
+        const uint8_t *p = expert_at(a, S.rt_used[u], far);
+        if (!far) bulk_g2s(dst + sb + (size_t)u * ub, p + 2 * a.gate_bytes + (int64_t)d0 * rowb_f, ub, full);
+      }
       ++kq;
     }
     // keep the block resident until every copy issued has landed
@@ -925,8 +959,15 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       const int f = g * S_GU + warp;
       if (got && u < nu && f < F) {
         typename RD::Row gp, up;
-        RD::load_s(src + (size_t)warp * rowb_d, gp);
-        RD::load_s(src + (size_t)(S_GU + warp) * rowb_d, up);
+        bool far;
+        const uint8_t *hrow = expert_at(a, S.rt_used[u], far) + (int64_t)f * rowb_d;
+        if (far) {  // the expert's rows are read from host memory
+          RD::load_g(hrow, gp);
+          RD::load_g(hrow + a.gate_bytes, up);
+        } else {
+          RD::load_s(src + (size_t)warp * rowb_d, gp);
+          RD::load_s(src + (size_t)(S_GU + warp) * rowb_d, up);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[st]);
         const float gu[2] = {RD::dot_reg(gp, xr), RD::dot_reg(up, xr)};
@@ -1033,13 +1074,21 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       }
     }
     const uint8_t *routed = src + (size_t)rb * 2 * Fs;
+    // pair p = (slot p / rb, row p % rb) of this tile: from the stage, or from
+    // host memory for an expert that has no cache slot
+    auto load_down_row = [&](int p, typename RF::Row &row) {
+      bool far;
+      const uint8_t *hp = expert_at(a, S.rt_used[p / rb], far);
+      if (far) RF::load_g(hp + 2 * a.gate_bytes + (int64_t)((bid + G * m) * rb + p % rb) * rowb_f, row);
+      else RF::load_s(routed + (size_t)p * rowb_f, row);
+    };
     float y[2] = {0.f, 0.f};
     if (two) {
       typename RF::Row rp[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int p = warp + h * S_CONS;
-        if (got && p < np) RF::load_s(routed + (size_t)p * rowb_f, rp[h]);
+        if (got && p < np) load_down_row(p, rp[h]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[st]);
@@ -1069,7 +1118,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
         float yy = 0.f;
         if (got) {
           typename RF::Row rp;
-          RF::load_s(routed + (size_t)p * rowb_f, rp);
+          load_down_row(p, rp);
           const uint32_t *pl = hpl + (p / rb) * hw;
           yy = RF::dot(rp, pl, reinterpret_cast<const float *>(pl + RF::NPL * nsb_f), nsb_f);
         }
@@ -1244,7 +1293,8 @@ bool stream_decode_supported(const Shape &sh, int64_t T) {
 }
 
 cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const void *x,
-                                const Work &wk, float *out, bool accumulate, cudaStream_t s, void *x_stage) {
+                                const Work &wk, float *out, bool accumulate, cudaStream_t s, void *x_stage,
+                                const Residency *res) {
   Args a{};
   a.D = sh.D; a.E = sh.E; a.F = sh.F; a.Fs = sh.Fs; a.k = sh.k; a.T = (int)wk.T;
   a.routed_scale = sh.routed_scale;
@@ -1257,6 +1307,11 @@ cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const 
   a.experts = W.experts;
   a.expert_bytes = sh.expert_bytes();
   a.gate_bytes = sh.gate_bytes();
+  if (res) {
+    a.slot = res->slot;
+    a.cache = res->cache;
+    a.host = res->host;
+  }
   a.x = x;
   a.x_f32 = sh.x_dtype == DS_F32;
   a.x_stage = nullptr;

@@ -74,6 +74,17 @@ cudaError_t once_per_device(OncePerDevice &o, F &&init) {
   return o.err[dev];
 }
 
+// Expert residency of one layer call: slot[e] >= 0 puts expert e in cache
+// slot slot[e], -1 in the device view `host` of the host copy of all experts.
+struct Residency {
+  const int32_t *slot;
+  const uint8_t *cache;
+  const uint8_t *host;
+};
+
+// The per-expert token counts region of a workspace laid out for T tokens.
+int32_t *workspace_counts(const Shape &sh, int64_t T, void *workspace);
+
 // fmt: DS_Q2_K or DS_Q4_K.
 cudaError_t launch_quantize(int fmt, const float *w, int64_t rows, int64_t in_dim, uint8_t *out,
                             cudaStream_t s);
@@ -92,7 +103,7 @@ cudaError_t launch_select_route(const Shape &sh, const Work &wk, const float *bi
 
 // Decode path: grouped dequantising GEMVs and the combine.
 cudaError_t launch_decode_ffn(const Shape &sh, const ds_moe_weights &W, const void *x,
-                              const Work &wk, cudaStream_t s);
+                              const Work &wk, cudaStream_t s, const Residency *res = nullptr);
 // Decode path for T <= 8: the whole layer in one persistent kernel (writes or
 // accumulates into out, and fills the route arrays of the workspace).
 bool fused_decode_supported(const Shape &sh, int64_t T);
@@ -103,7 +114,7 @@ bool stream_decode_supported(const Shape &sh, int64_t T);
 // the copy.
 cudaError_t launch_decode_fused(const Shape &sh, const ds_moe_weights &W, const void *x,
                                 const Work &wk, float *out, bool accumulate, cudaStream_t s,
-                                void *x_stage = nullptr);
+                                void *x_stage = nullptr, const Residency *res = nullptr);
 // Large batches: the expert FFNs as grouped tcgen05 GEMMs (after
 // launch_route; the combine follows).  tc_ws holds prefill_tc_workspace bytes.
 constexpr int64_t TC_MIN_T = 5;

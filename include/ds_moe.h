@@ -253,6 +253,84 @@ int ds_moe_stack_mixed(const ds_moe_shape *shape, const ds_moe_weights *layers,
 int ds_moe_layer_noalloc(const ds_moe_shape *shape, const ds_moe_weights *weights, const void *x,
                          int64_t T, float *out, void *stream, char *err, size_t errlen);
 
+/* Expert residency beyond device memory ("The sparsity that pays for
+ * everything else in DwarfStar", "Page the experts off the SSD" and "The
+ * cache is never allowed to become a correctness structure": routed experts
+ * are paged in through a cache, and the output does not depend on what the
+ * cache holds).  Here every routed expert of a layer has a copy in host
+ * memory the device can address (pinned and mapped by cudaHostAlloc,
+ * registered by cudaHostRegister, or the memory of a coherent host such as
+ * Grace, read over NVLink-C2C), and a caller-owned pool of device slots holds
+ * some of them.
+ *   slot          [E] int32 (device): the cache slot of expert e, or -1
+ *   cache         device: slots of ds_moe_expert_bytes_fmt() bytes each,
+ *                 16-byte aligned (may be NULL when no slot is in use)
+ *   experts_host  HOST pointer to the layer's E packed experts (the layout of
+ *                 ds_moe_weights.experts), 16-byte aligned */
+typedef struct {
+  const int32_t *slot;
+  const uint8_t *cache;
+  const uint8_t *experts_host;
+} ds_moe_residency;
+
+/* ds_moe_layer with the routed experts read through a residency view: each
+ * expert from its cache slot, or from the host copy (ordinary loads) when it
+ * has none; weights->experts is ignored and may be NULL.  The same kernels
+ * run on the same bytes wherever an expert lives, so the output is
+ * bit-identical for every slot table.  Kernels: as ds_moe_layer for up to
+ * four tokens at the instantiated widths (the streaming kernel, the
+ * three-kernel chain), the grouped dequantising GEMV path otherwise
+ * (ds_moe_layer_path_resident).  Errors as ds_moe_layer, and
+ * DS_ERR_INVALID_ARG for a missing slot table or a host copy the device
+ * cannot address. */
+int ds_moe_layer_resident(const ds_moe_shape *shape, const ds_moe_weights *weights,
+                          const ds_moe_residency *residency, const void *x, int64_t T, float *out,
+                          void *workspace, size_t workspace_bytes, const ds_moe_debug *dbg, void *stream,
+                          char *err, size_t errlen);
+
+/* A cache of routed experts for n_layers layers of one shape (opaque host
+ * object).  experts_host: host array of n_layers host pointers, each a
+ * layer's E packed experts in device-addressable host memory (as for
+ * ds_moe_residency).  slots: caller-owned device buffer of n_slots experts
+ * (ds_moe_expert_bytes_fmt() bytes each, 16-byte aligned; the byte budget of
+ * the cache); tables: caller-owned device buffer of n_layers * E int32 slot
+ * tables, set here (synchronously) to "every expert in host memory".  With
+ * tables == NULL the object only plans (ds_moe_cache_record; no device
+ * memory is touched).  The library allocates no device memory; the object
+ * itself is host memory, freed by ds_moe_cache_destroy. */
+typedef struct ds_moe_cache ds_moe_cache;
+int ds_moe_cache_create(const ds_moe_shape *shape, int32_t n_layers, const void *const *experts_host,
+                        void *slots, int64_t n_slots, int32_t *tables, ds_moe_cache **cache, char *err,
+                        size_t errlen);
+void ds_moe_cache_destroy(ds_moe_cache *cache);
+
+/* One layer through the cache: ds_moe_layer_resident with this layer's slot
+ * table, then (after synchronising the stream to read which experts the call
+ * used) the experts it missed are copied on `stream` into free slots or the
+ * least recently used slots that this call did not use, and the slot tables
+ * are updated on `stream` for the calls that follow.  The output does not
+ * depend on the cache's contents.  Not for use inside stream capture (it
+ * synchronises the stream). */
+int ds_moe_cache_layer(ds_moe_cache *cache, int32_t layer, const ds_moe_weights *weights, const void *x, int64_t T,
+                       float *out, void *workspace, size_t workspace_bytes, void *stream, char *err,
+                       size_t errlen);
+
+/* The cache policy alone, on the host: record that a call of `layer` used
+ * the experts with counts[e] > 0 (host array [E]).  Hits refresh their
+ * slots; each miss takes a free slot, else the least recently used slot not
+ * used by this call (none: the expert stays in host memory).  fills (host,
+ * optional, 2 * E int32) receives (slot, expert) pairs of the copies to make,
+ * n_fills their number.  ds_moe_cache_layer does this after every call. */
+int ds_moe_cache_record(ds_moe_cache *cache, int32_t layer, const int32_t *counts, int32_t *fills,
+                        int32_t *n_fills);
+/* *slot = the slot of expert `expert` of `layer` (host mirror of the
+ * tables), or -1 when it is in host memory.  DS_ERR_INVALID_ARG for a bad
+ * cache, layer, expert or NULL slot. */
+int ds_moe_cache_slot(const ds_moe_cache *cache, int32_t layer, int32_t expert, int32_t *slot);
+/* Counters since creation: experts found in a slot, experts read from host
+ * memory, and slots in use. */
+int ds_moe_cache_stats(const ds_moe_cache *cache, int64_t *hits, int64_t *misses, int64_t *resident);
+
 /* Which kernels ds_moe_layer runs for T tokens of this shape with this x
  * pointer (host call; nothing is launched).  Returns one of the DS_PATH_*
  * values, or DS_ERR_INVALID_ARG for a shape ds_moe_layer would reject. */
@@ -266,6 +344,8 @@ enum {
                                 routed dots, shared expert on the tensor cores) */
 };
 int ds_moe_layer_path(const ds_moe_shape *shape, int64_t T, const void *x);
+/* The same for ds_moe_layer_resident. */
+int ds_moe_layer_path_resident(const ds_moe_shape *shape, int64_t T);
 
 /* Synchronise `stream`, then read and clear this device's sticky status
  * word (one atomic exchange on the device, so bits that kernels on other
