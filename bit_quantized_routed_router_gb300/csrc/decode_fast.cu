@@ -39,6 +39,7 @@
 #include "internal.h"
 #include "ptx.cuh"
 #include "qrows.cuh"
+#include "select.cuh"
 
 namespace dsm {
 namespace {
@@ -130,9 +131,10 @@ __device__ __forceinline__ void ld8<uint16_t>(const uint16_t *p, float v[8]) {
 
 // ===================================================================== K1 ==
 
-// Router logits: two expert rows per CTA, a quarter of n_embd per warp.
+// Router logits: two expert rows per CTA, a quarter of n_embd per warp (at
+// most 32 registers per thread, so that the CTA fits beside a streaming CTA).
 template <typename TX, typename TW>
-__global__ void __launch_bounds__(256) route_kernel(const Args a) {
+__global__ void __launch_bounds__(256, 8) route_kernel(const Args a) {
   pdl_trigger();  // the gate/up kernel may start its route-free work now
   // The dependent kernel touches this word only after its griddepcontrol.wait,
   // i.e. after this grid has completed.
@@ -187,7 +189,7 @@ struct RouteCache {
 // expert and a smaller p).  Returns the calling lane's RouteCache entries; with
 // publish, also writes ids, w, counts, offsets, perm, pos and used.
 template <int PMAX>
-__device__ RouteCache select_route_warp(const Args &a, bool publish, volatile int *loaded = nullptr) {
+__device__ RouteCache select_route_warp(const Args &a, bool publish) {
   const int lane = threadIdx.x & 31, P = a.T * a.k;
   int my_id = 0;     // lane p: expert of pair p
   float my_lg = 0.f; // lane p: its logit
@@ -197,15 +199,9 @@ __device__ RouteCache select_route_warp(const Args &a, bool publish, volatile in
     float lv[32];
 #pragma unroll
     for (int ii = 0; ii < 32; ++ii) lv[ii] = ii < nv && lane + 32 * ii < a.E ? __ldcg(L + lane + 32 * ii) : -INFINITY;
-    if (loaded && t == a.T - 1) {
-      // every lane's logits have arrived (the flag's value depends on them)
-      float mx = lv[0];
-#pragma unroll
-      for (int ii = 1; ii < 32; ++ii) mx = fmaxf(mx, lv[ii]);
-      int one;  // 1, computed from mx so that it waits for the loads
-      asm volatile("{\n\t.reg .pred p;\n\tsetp.num.f32 p, %1, %1;\n\tselp.s32 %0, 1, 1, p;\n\t}" : "=r"(one) : "f"(mx));
-      const int got = __all_sync(0xffffffffu, one);
-      if (lane == 0) *loaded = got;
+    if (a.E <= 256) {  // eight candidates per lane, sorted once
+      topk_sorted8(lv, a.E, a.k, my_id, my_lg, a.status, t * a.k);
+      continue;
     }
     // each lane's best remaining candidate (largest logit, then lowest
     // index); per pick the warp takes the best of those, and only the lane
@@ -644,6 +640,12 @@ __global__ void __launch_bounds__(NW3 * 32, 1) down_kernel(const Args a) {
 // without writing the output.
 constexpr int S_CONS = 12;                       // consumer warps
 constexpr int S_THREADS = (S_CONS + 2) * 32;     // + producer warp + router warp
+// Registers per thread: four streaming warps of an SM sub-partition take
+// 4 * 32 * 112 = 14,336 of its 16,384 registers, which leaves room for two
+// warps of a router CTA at 32 registers (route_kernel's bounds), so the
+// streaming grid's dependent launch starts while the router grid still runs.
+// (Q2_K rows; the Q4_K kernels keep 128, which their rows need.)
+constexpr int S_REGS = 112;
 constexpr uint32_t S_STAGE = 32768;              // bytes per ring stage
 constexpr int S_NS = 3;                          // ring stages
 constexpr int S_GU = S_CONS;                     // routed gate/up rows per tile (one per warp)
@@ -659,7 +661,6 @@ struct StreamShared {
   float rt_w[32];      // pair j -> routing weight
   int rt_nu;           // slots in use
   int ready;           // the route above is published
-  int lg_loaded;       // the router warp holds the logits
   int abort_;          // a wait expired
   int go;              // consumers continue past the grid barrier
   int tile[S_NS];                  // phase-A tile in each stage: shared i >= 0, routed -1 - r
@@ -742,7 +743,7 @@ int stream_rows_b(int fmt, int D, int F, int Fs, int nslots) {
 // RD, RF: the row formats (Q2Rows / Q4Rows) of n_embd-long and n_ff-long
 // rows; STG: the ring stage size.
 template <class RD, class RF, uint32_t STG>
-__global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int rb) {
+__global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Args a, int rb) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *stages = smem;
   StreamShared &S = *reinterpret_cast<StreamShared *>(smem + (size_t)S_NS * STG);
@@ -774,7 +775,6 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       mbar_init(&S.empty[i], S_CONS);
     }
     S.ready = 0;
-    S.lg_loaded = 0;
     S.abort_ = 0;
     S.go = 0;
     S.rt_nu = 0;
@@ -785,7 +785,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
   // ---------------------------------------------------------------- router --
   if (warp == S_CONS + 1) {
     pdl_wait();  // router logits complete and visible
-    const RouteCache r = select_route_warp<S_MAXK>(a, bid == 0, &S.lg_loaded);  // one token: k pairs
+    const RouteCache r = select_route_warp<S_MAXK>(a, bid == 0);  // one token: k pairs
     S.rt_used[lane] = r.used;
     S.rt_pos[lane] = r.pos;
     S.rt_w[lane] = r.w;
@@ -801,20 +801,6 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
     if (lane != 0) return;
     int kq = 0;
     bool ok = true;
-    // the router warp's logit loads go first: behind a full copy ring they
-    // would wait several microseconds, and the routed tiles with them
-    {
-      const uint64_t t0 = globaltimer_ns();
-      while (!vload(&S.lg_loaded) && !vload(&S.abort_)) {
-        if (globaltimer_ns() - t0 > wait_limit()) {
-          flag(a.status, ST_TIMEOUT);
-          *(volatile int *)&S.abort_ = 1;
-          ok = false;
-          break;
-        }
-        __nanosleep(32);
-      }
-    }
     // a free stage for the next tile (its previous tile consumed)
     auto acquire = [&]() -> uint8_t * {
       const int st = kq % S_NS;
@@ -999,7 +985,8 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
     bool fine = !vload(&S.abort_) && s_wait_ready(S, a.status);
     if (fine) {
       pdl_wait();  // the router grid (which reset the barrier word) has completed
-      __threadfence();
+      // the release add publishes every h and hs store of the block: they
+      // precede this thread's add through the named barrier above
       atom_add_release(a.ctrl + C_BAR, 1u);
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire(a.ctrl + C_BAR) < (unsigned)G) {
@@ -1008,7 +995,6 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
           fine = false;
           break;
         }
-        __nanosleep(32);
       }
     }
     if (!fine) *(volatile int *)&S.abort_ = 1;
@@ -1019,8 +1005,16 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
   nu = S.rt_nu;
 
   // h of every slot in fixed point, and hs: one half-warp per 256-element
-  // block, two blocks per half-warp and pass with all loads issued first
+  // block, two blocks per half-warp and pass, with the hs loads and every h
+  // load of the pass issued before the first use
   {
+    constexpr int HSR = 8;  // hs values per thread kept in flight
+    float hv[HSR];
+#pragma unroll
+    for (int j = 0; j < HSR; ++j) {
+      const int i = threadIdx.x + j * NT;
+      hv[j] = i < Fs ? __ldcg(a.hs + i) : 0.f;
+    }
     const int nblk = nu * nb_f, nun = (nblk + 1) / 2;
     for (int un = warp; un < nun; un += 2 * S_CONS) {
       float v[2][16];
@@ -1041,7 +1035,12 @@ __global__ void __launch_bounds__(S_THREADS, 1) stream_kernel(const Args a, int 
       for (int h = 0; h < 2; ++h)
         RF::digitize(v[h], blk[h], hpl + q[h] * hw, reinterpret_cast<float *>(hpl + q[h] * hw + RF::NPL * nsb_f), nsb_f);
     }
-    for (int i = threadIdx.x; i < Fs; i += NT) hsm[i] = __ldcg(a.hs + i);
+#pragma unroll
+    for (int j = 0; j < HSR; ++j) {
+      const int i = threadIdx.x + j * NT;
+      if (i < Fs) hsm[i] = hv[j];
+    }
+    for (int i = threadIdx.x + HSR * NT; i < Fs; i += NT) hsm[i] = __ldcg(a.hs + i);
   }
   named_bar(1, NT);
 
