@@ -505,6 +505,7 @@ def extra_workloads(args, dev):
 
 PREFILL_Q4K = replace(dsgen.PREFILL, name="prefill T=4096 Q4_K experts D=4096 E=256 k=6 F=2048 Fs=2048",
                       expert_fmt="q4k")
+DECODE8 = replace(dsgen.DECODE1, name="decode T=8 D=4096 E=256 k=6 F=2048 Fs=2048 (one layer)", T=8)
 RESIDENT = replace(dsgen.DECODE1, name="decode T=1 experts in host memory, device cache, zipf(1.1) "
                                        "D=4096 E=256 k=6 F=2048 Fs=2048", zipf_s=1.1)
 
@@ -513,6 +514,7 @@ WORKLOADS = {
     "prefill": dsgen.PREFILL,
     "prefill_zipf": dsgen.PREFILL_ZIPF,
     "decode32": dsgen.DECODE32_ZIPF,
+    "decode8": DECODE8,
     "stack": dsgen.STACK,
     "decode_q4k": dsgen.DECODE1_Q4K,
     "prefill_q4k": PREFILL_Q4K,
