@@ -244,11 +244,11 @@ def gpu_arm(args, rank, world, local_rank):
 
 LAUNCHES_PER_DECODE_STEP = 2  # router logits; the one-token streaming kernel
 # DRAM bytes read + written by one decode step, from one ncu capture of these
-# kernels as they stand, or None.  The last capture (route_kernel 2,117,888
-# read; stream_kernel 99,979,008 read + 76,288 written; the command is in the
-# decode profile summary) predates the streaming kernel's templating on the
-# row format, so it is not claimed until the kernel is captured again.
-DECODE_STEP_DRAM_BYTES = None
+# kernels as they stand (route_kernel 2,118,144 read; stream_kernel
+# 99,994,880 read + 2,781,184 written; the commands are in the decode profile
+# summary).  Set to None whenever either kernel changes until it is captured
+# again.
+DECODE_STEP_DRAM_BYTES = 104_894_208
 
 PREFILL_FLOPS = 1.4517e12  # 4096 x (6*3*2*D*F + 3*2*D*F + 2*D*E) at the Flash shape
 
