@@ -1046,8 +1046,9 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
 
   // phase B: every consumer thread takes eight-element chunks of all rb
   // shared rows (hs read once); warp w takes the routed (slot, row) pairs
-  // w and w + S_CONS when they are the only two (else it loops over its
-  // pairs one at a time)
+  // 2w and 2w + 1 when there are at most two per warp — with rb even both
+  // rows belong to one slot, whose h planes the warp then loads into
+  // registers once — else it loops over its pairs one at a time
   const int np = nu * rb;
   const bool two = np <= 2 * S_CONS;
   int kq = ns_b + nr_b;
@@ -1086,17 +1087,27 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
       typename RF::Row rp[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int p = warp + h * S_CONS;
+        const int p = 2 * warp + h;
         if (got && p < np) load_down_row(p, rp[h]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[st]);
+      if (got && 2 * warp < np) {
+        if ((rb & 1) == 0) {  // one slot: its planes in registers, two dots
+          const uint32_t *pl = hpl + (2 * warp / rb) * hw;
+          typename RF::XR hr;
+          RF::load_x(pl, reinterpret_cast<const float *>(pl + RF::NPL * nsb_f), nsb_f, hr);
+          y[0] = RF::dot_reg(rp[0], hr);
+          y[1] = RF::dot_reg(rp[1], hr);
+        } else {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int p = warp + h * S_CONS;
-        if (got && p < np) {
-          const uint32_t *pl = hpl + (p / rb) * hw;
-          y[h] = RF::dot(rp[h], pl, reinterpret_cast<const float *>(pl + RF::NPL * nsb_f), nsb_f);
+          for (int h = 0; h < 2; ++h) {
+            const int p = 2 * warp + h;
+            if (p < np) {
+              const uint32_t *pl = hpl + (p / rb) * hw;
+              y[h] = RF::dot(rp[h], pl, reinterpret_cast<const float *>(pl + RF::NPL * nsb_f), nsb_f);
+            }
+          }
         }
       }
       const float v8[8] = {ys[0], ys[1], ys[2], ys[3], y[0], y[1], 0.f, 0.f};
@@ -1104,7 +1115,7 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
       const int vi = lane >> 2;
       if ((lane & 3) == 0 && m < S_MAXT) {
         if (vi < 4) S.redb[m][warp][vi] = tot;
-        else if (vi < 6 && warp + (vi - 4) * S_CONS < np) S.yrb[m][warp + (vi - 4) * S_CONS] = tot;
+        else if (vi < 6 && 2 * warp + (vi - 4) < np) S.yrb[m][2 * warp + (vi - 4)] = tot;
       }
     } else {
       // one pair at a time, the stage released after the last
