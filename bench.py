@@ -244,11 +244,11 @@ def gpu_arm(args, rank, world, local_rank):
 
 LAUNCHES_PER_DECODE_STEP = 2  # router logits; the one-token streaming kernel
 # DRAM bytes read + written by one decode step, from one ncu capture of these
-# kernels as they stand (route_kernel 2,118,144 read; stream_kernel
-# 99,994,880 read + 2,781,184 written; the commands are in the decode profile
+# kernels as they stand (route_kernel 2,117,888 read; stream_kernel
+# 100,033,024 read + 2,804,736 written; the commands are in the decode profile
 # summary).  Set to None whenever either kernel changes until it is captured
 # again.
-DECODE_STEP_DRAM_BYTES = None
+DECODE_STEP_DRAM_BYTES = 104_955_648
 
 PREFILL_FLOPS = 1.4517e12  # 4096 x (6*3*2*D*F + 3*2*D*F + 2*D*E) at the Flash shape
 
@@ -530,6 +530,7 @@ WORKLOADS = {
 def host_info():
     """The host's logical core count and CPU model (for the CPU-baseline rows)."""
     model = None
+    impl_arm = False
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
@@ -538,8 +539,14 @@ def host_info():
                 if k in ("model name", "cpu model", "hardware") and v.strip():
                     model = v.strip()
                     break
+                if k == "cpu implementer" and v.strip() == "0x41":
+                    impl_arm = True
                 if k == "cpu part" and model is None:
-                    model = f"cpu part {v.strip()}"
+                    # Arm's published part numbers for the cores these hosts use
+                    part = v.strip().lower()
+                    names = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+                             "0xd49": "Arm Neoverse N2", "0xd84": "Arm Neoverse V3"}
+                    model = names.get(part, f"Arm cpu part {part}") if impl_arm else f"cpu part {part}"
     except OSError:
         pass
     if model is None:
