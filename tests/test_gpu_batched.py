@@ -1,5 +1,6 @@
-"""Parity of the batched decode path (5..16 tokens) and of every selection
-implementation on exact ties, through the C ABI, against the fp64 oracle.
+"""Parity of the batched decode path (5..16 tokens), of every selection
+implementation on exact ties and of every path with more than 256 experts,
+through the C ABI, against the fp64 oracle.
 
 Batched decode: routed experts as exact integer dots on 16-bit fixed-point
 activations, the shared expert on the tensor cores with exact bf16 products;
@@ -67,7 +68,7 @@ def close(got, ref, tol, what="out"):
     assert err <= tol * rms, f"{what}: max|err| {err:.3e} > {tol} * rms {rms:.3e}"
 
 
-def parity(cfg, bias_select_only=0, W=None, path=ds.PATH_BATCHED_DECODE):
+def parity(cfg, bias_select_only=0, W=None, path=ds.PATH_BATCHED_DECODE, tol=DECODE_TOL):
     lo = oracle.LayerOracle(cfg)
     att = oracle.resample_attempts(cfg, lo)
     x64 = oracle.as_f64(dsgen.host_x(cfg, att), cfg.x_dtype)
@@ -84,7 +85,7 @@ def parity(cfg, bias_select_only=0, W=None, path=ds.PATH_BATCHED_DECODE):
     assert np.max(np.abs(dbg["w"] - w)) <= 1e-5
     res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs,
                            fmt=cfg.expert_fmt)
-    close(out, res, DECODE_TOL, cfg.name)
+    close(out, res, tol, cfg.name)
     return out
 
 
@@ -211,3 +212,19 @@ def test_exact_tie_goes_to_lower_index(T, dtype, Fs, path):
     res = oracle.moe_layer(x64, lo.experts(ids), lo.shared, ids, w, cfg.D, cfg.E, cfg.F, cfg.Fs)
     tol = DECODE_TOL if path != ds.PATH_TENSOR_CORE else 5e-3
     close(out, res, tol, f"tie T={T}")
+
+
+# ------------------------------------------------------- many experts --
+
+@pytest.mark.parametrize("E", [300, 1024])
+@pytest.mark.parametrize("T,dtype,Fs,path", [(1, "bf16", 512, ds.PATH_STREAM), (3, "bf16", 512, ds.PATH_DECODE3),
+                                             (8, "bf16", 1024, ds.PATH_BATCHED_DECODE),
+                                             (33, "f32", 1024, ds.PATH_GROUPED_GEMV),
+                                             (300, "bf16", 1024, ds.PATH_TENSOR_CORE)])
+def test_more_than_256_experts(E, T, dtype, Fs, path):
+    """Expert counts above 256 (the library takes up to 1024): every lane of a
+    selecting warp holds more than eight logits, so each selection
+    implementation takes its general scan instead of the sorted eight-per-lane
+    lists; 300 is not a multiple of 32 (ragged last lanes)."""
+    cfg = replace(_tie_cfg(T, dtype, Fs, 6, E), name=f"E={E} T={T} {dtype}", seed=29)
+    parity(cfg, path=path, tol=DECODE_TOL if path != ds.PATH_TENSOR_CORE else 5e-3)
