@@ -161,7 +161,9 @@ int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *ou
               const Work &wk, const ds_moe_debug *dbg, cudaStream_t s, char *err, size_t errlen,
               const Residency *res = nullptr) {
   cudaError_t e;
-  if (fused_decode_supported(sh, wk.T)) {
+  // the batched kernels take precedence over the chain where both apply
+  const bool mt = !res && wk.mt && aligned(x, 16) && decode_mt_supported(sh, wk.T);
+  if (!mt && fused_decode_supported(sh, wk.T)) {
     if ((e = launch_decode_fused(sh, W, x, wk, out, accumulate, s, nullptr, res)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "fused decode layer");
   } else if (res) {  // residency: the kernels that address each expert by pointer
@@ -170,7 +172,7 @@ int run_layer(const Shape &sh, const ds_moe_weights &W, const void *x, float *ou
     if ((e = launch_route(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "route");
     if ((e = launch_decode_ffn(sh, W, x, wk, s, res)) != cudaSuccess) return cuda_fail(err, errlen, e, "expert FFN");
     if ((e = launch_combine(sh, wk, out, accumulate, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "combine");
-  } else if (wk.mt && aligned(x, 16) && decode_mt_supported(sh, wk.T)) {
+  } else if (mt) {
     if ((e = launch_router_logits(sh, W, x, wk, s)) != cudaSuccess) return cuda_fail(err, errlen, e, "router");
     if ((e = launch_decode_mt(sh, W, x, wk, out, accumulate, wk.mt, s)) != cudaSuccess)
       return cuda_fail(err, errlen, e, "batched decode layer");
@@ -510,8 +512,8 @@ int ds_moe_layer_path(const ds_moe_shape *shape, int64_t T, const void *x) {
   Shape sh;
   if (check_shape(shape, nullptr, 0, &sh) != DS_OK || T < 0) return DS_ERR_INVALID_ARG;
   if (T == 0) return DS_PATH_NONE;
-  if (fused_decode_supported(sh, T)) return stream_decode_supported(sh, T) ? DS_PATH_STREAM : DS_PATH_DECODE3;
   if (aligned(x, 16) && decode_mt_supported(sh, T)) return DS_PATH_BATCHED_DECODE;
+  if (fused_decode_supported(sh, T)) return stream_decode_supported(sh, T) ? DS_PATH_STREAM : DS_PATH_DECODE3;
   if (aligned(x, 16) && prefill_tc_supported(sh, T)) return DS_PATH_TENSOR_CORE;
   return DS_PATH_GROUPED_GEMV;
 }

@@ -127,8 +127,9 @@ cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const voi
                              cudaStream_t s);
 // Batched decode (MT_MIN_T..MT_MAX_T tokens): the router logits alone, then
 // selection, route, expert FFNs and combine in the batched decode kernels.
-// (The kernels hold up to 32 tokens; above 16 the tensor-core path is faster.)
-constexpr int64_t MT_MIN_T = 5, MT_MAX_T = 16;
+// (The kernels hold up to 32 tokens; above 16 the tensor-core path is faster,
+// below 4 the three-kernel chain.)
+constexpr int64_t MT_MIN_T = 4, MT_MAX_T = 16;
 cudaError_t launch_router_logits(const Shape &sh, const ds_moe_weights &W, const void *x, const Work &wk,
                                  cudaStream_t s);
 bool decode_mt_supported(const Shape &sh, int64_t T);

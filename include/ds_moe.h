@@ -180,12 +180,12 @@ int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, 
  * T == 0 is a no-op.  The kernels that run depend on T and the shape (see
  * ds_moe_layer_path): one token at the instantiated widths with top_k <= 8
  * streams the whole layer through one cooperative kernel; up to four tokens
- * (and one token otherwise) use a three-kernel decode chain; both compute
- * the routed rows as exact integer dots on 16-bit fixed-point activations.
- * 5..16 tokens with Q2_K experts, bf16 x and router and n_embd, n_ff,
- * n_ff_shared multiples of 1024 run the batched decode kernels (the same
- * integer dots; the shared expert on the tensor cores with exact bf16
- * products).  Larger batches with bf16 x and router and n_embd, n_ff
+ * (and one token otherwise) use a three-kernel decode chain, except where
+ * the batched kernels below apply; both compute the routed rows as exact
+ * integer dots on 16-bit fixed-point activations.  4..16 tokens with Q2_K
+ * experts, bf16 x and router and n_embd, n_ff, n_ff_shared multiples of
+ * 1024 run the batched decode kernels (the same integer dots; the shared
+ * expert on the tensor cores with exact bf16 products).  Larger batches with bf16 x and router and n_embd, n_ff
  * multiples of 1024 (Q4_K experts: from five tokens) run the expert FFNs as
  * grouped tcgen05 GEMMs with fp16 operands (dequantised weights and
  * activations rounded once to fp16; an |x| or intermediate above 65504 is
@@ -337,10 +337,11 @@ int ds_moe_cache_stats(const ds_moe_cache *cache, int64_t *hits, int64_t *misses
 enum {
   DS_PATH_NONE = 0,          /* T == 0 */
   DS_PATH_STREAM = 1,        /* one token: router kernel + one cooperative streaming kernel */
-  DS_PATH_DECODE3 = 2,       /* T <= 4: router, gate/up and down kernels chained */
+  DS_PATH_DECODE3 = 2,       /* T <= 4 (2..3, or 4 where the batched kernels do not apply): router,
+                                gate/up and down kernels chained */
   DS_PATH_GROUPED_GEMV = 3,  /* route kernels + grouped dequantising GEMVs + combine */
   DS_PATH_TENSOR_CORE = 4,   /* route kernels + grouped tcgen05 GEMMs + combine */
-  DS_PATH_BATCHED_DECODE = 5 /* 5..16 tokens: router kernel + batched decode kernels (integer
+  DS_PATH_BATCHED_DECODE = 5 /* 4..16 tokens: router kernel + batched decode kernels (integer
                                 routed dots, shared expert on the tensor cores) */
 };
 int ds_moe_layer_path(const ds_moe_shape *shape, int64_t T, const void *x);

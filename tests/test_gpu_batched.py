@@ -1,8 +1,8 @@
-"""Parity of the batched decode path (5..16 tokens), of every selection
+"""Parity of the batched decode path (4..16 tokens), of every selection
 implementation on exact ties and of every path with more than 256 experts,
 through the C ABI, against the fp64 oracle.
 
-Batched decode: routed experts as exact integer dots on 16-bit fixed-point
+Batched decode (4..16 tokens): routed experts as exact integer dots on 16-bit fixed-point
 activations, the shared expert on the tensor cores with exact bf16 products;
 outputs within the decode tolerance 2e-3 * rms(out_oracle), ids, counts,
 offsets and the permutation bit-exact.
@@ -95,11 +95,11 @@ def _w1024(T, Fs, k, E, zipf=0.0, seed=11):
                    router_dtype="bf16", router_sigma=0.02, zipf_s=zipf, seed=seed)
 
 
-@pytest.mark.parametrize("T,Fs,k,E,zipf", [(5, 1024, 2, 16, 0.0), (13, 0, 6, 40, 0.0),
+@pytest.mark.parametrize("T,Fs,k,E,zipf", [(4, 1024, 2, 16, 0.0), (5, 1024, 2, 16, 0.0), (13, 0, 6, 40, 0.0),
                                             (16, 1024, 4, 8, 0.0), (16, 2048, 6, 64, 1.1),
                                             (15, 1024, 16, 16, 0.0), (9, 1024, 1, 3, 0.0)])
 def test_batched_decode_width_1024(T, Fs, k, E, zipf):
-    """At width 1024: the smallest batch of the path, no shared expert, every
+    """At width 1024: the smallest batches of the path (4, 5), no shared expert, every
     expert with many tokens (E = 8, k = 4, 16 tokens), a Zipf-skewed route,
     k = E, one expert per token with an odd expert count."""
     parity(_w1024(T, Fs, k, E, zipf))
@@ -111,7 +111,7 @@ def flash_layer():
     return cfg, synthetic.build_layer(cfg)
 
 
-@pytest.mark.parametrize("T", [5, 8, 12, 16])
+@pytest.mark.parametrize("T", [4, 5, 8, 12, 16])
 def test_batched_decode_flash(flash_layer, T):
     """The Flash layer at the batch sizes of the path: one K slice of n_embd
     per block up to 8 tokens, then two (partial sums in a fixed order)."""

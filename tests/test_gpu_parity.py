@@ -268,7 +268,8 @@ def test_layer_path_selection():
     sh = synthetic.shape_of(dsgen.DECODE1)
     assert ds.layer_path(sh, 0) == ds.PATH_NONE
     assert ds.layer_path(sh, 1) == ds.PATH_STREAM
-    assert ds.layer_path(sh, 4) == ds.PATH_DECODE3
+    assert ds.layer_path(sh, 3) == ds.PATH_DECODE3
+    assert ds.layer_path(sh, 4) == ds.PATH_BATCHED_DECODE
     assert ds.layer_path(sh, 5) == ds.PATH_BATCHED_DECODE
     assert ds.layer_path(sh, 8) == ds.PATH_BATCHED_DECODE
     assert ds.layer_path(sh, 16) == ds.PATH_BATCHED_DECODE
