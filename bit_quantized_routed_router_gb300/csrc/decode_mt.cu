@@ -1,4 +1,4 @@
-// Batched decode: the layer for 5..16 tokens with every used expert's weights
+// Batched decode: the layer for 4..16 tokens with every used expert's weights
 // read once.
 //
 // What it computes is the layer of "Understanding Dwarf Star" 5.3.2 / 5.3.7
