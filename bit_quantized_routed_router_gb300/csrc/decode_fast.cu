@@ -135,7 +135,17 @@ __device__ __forceinline__ void ld8<uint16_t>(const uint16_t *p, float v[8]) {
 // most 32 registers per thread, so that the CTA fits beside a streaming CTA).
 template <typename TX, typename TW>
 __global__ void __launch_bounds__(256, 8) route_kernel(const Args a) {
-  pdl_trigger();  // the gate/up kernel may start its route-free work now
+  // This grid may be launched while the previous kernel of the stream (the
+  // streaming kernel of the previous layer) still runs: its router rows do
+  // not depend on it and are started towards L2 at once; x and the workspace
+  // are touched only after that grid has completed.
+  if (threadIdx.x == 0 && 2 * blockIdx.x < a.E) {
+    const int rows = min(2, a.E - 2 * (int)blockIdx.x);
+    bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(a.router_w) + (int64_t)2 * blockIdx.x * a.D * sizeof(TW),
+                     (uint32_t)(rows * a.D * sizeof(TW)));
+  }
+  pdl_wait();
+  pdl_trigger();  // the next kernel may start its route-free work now
   // The dependent kernel touches this word only after its griddepcontrol.wait,
   // i.e. after this grid has completed.
   if (blockIdx.x == 0 && threadIdx.x == 0) a.ctrl[C_BAR] = 0u;
@@ -744,6 +754,9 @@ int stream_rows_b(int fmt, int D, int F, int Fs, int nslots) {
 // rows; STG: the ring stage size.
 template <class RD, class RF, uint32_t STG>
 __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Args a, int rb) {
+  // the next layer's router grid may launch now: it waits for this grid's
+  // completion before it reads x or writes the workspace
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *stages = smem;
   StreamShared &S = *reinterpret_cast<StreamShared *>(smem + (size_t)S_NS * STG);
@@ -1191,10 +1204,10 @@ cudaError_t launch_all(const Args &a, const Shape &sh, cudaStream_t s) {
   });
   if (e != cudaSuccess) return e;
   const dim3 g1((sh.E + 1) / 2);
-  if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16) route_kernel<uint16_t, uint16_t><<<g1, 256, 0, s>>>(a);
-  else if (sh.x_dtype == DS_F32 && sh.router_dtype == DS_F32) route_kernel<float, float><<<g1, 256, 0, s>>>(a);
+  if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16) e = launch_pdl(route_kernel<uint16_t, uint16_t>, g1, dim3(256), 0, s, a);
+  else if (sh.x_dtype == DS_F32 && sh.router_dtype == DS_F32) e = launch_pdl(route_kernel<float, float>, g1, dim3(256), 0, s, a);
   else return cudaErrorInvalidValue;
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   if ((e = launch_pdl(gateup_kernel<RD>, dim3(sms), dim3(NW2 * 32), k2_smem(sh.fmt, a.T, a.D), s, a)) != cudaSuccess)
     return e;
   return launch_pdl(down_kernel<RF>, dim3(sms), dim3(NW3 * 32), k3_smem(sh.fmt, a.T, a.k, a.F, a.Fs), s, a);
@@ -1242,10 +1255,10 @@ cudaError_t launch_stream(const Args &a, const Shape &sh, int rb, cudaStream_t s
     }
   }
   const dim3 g1((sh.E + 1) / 2);
-  if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16) route_kernel<uint16_t, uint16_t><<<g1, 256, 0, s>>>(a);
-  else if (sh.x_dtype == DS_F32 && sh.router_dtype == DS_F32) route_kernel<float, float><<<g1, 256, 0, s>>>(a);
+  cudaError_t e;
+  if (sh.x_dtype == DS_BF16 && sh.router_dtype == DS_BF16) e = launch_pdl(route_kernel<uint16_t, uint16_t>, g1, dim3(256), 0, s, a);
+  else if (sh.x_dtype == DS_F32 && sh.router_dtype == DS_F32) e = launch_pdl(route_kernel<float, float>, g1, dim3(256), 0, s, a);
   else return cudaErrorInvalidValue;
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
