@@ -375,6 +375,55 @@ def test_batch_invariance_decode(decode1):
                     "one-token kernel vs batched decode path")
 
 
+@pytest.mark.parametrize("T", [1, 3])
+def test_back_to_back_layers_read_the_previous_output(T):
+    """Layers enqueued back to back, each reading the previous layer's output
+    as its x (fp32 x and router, so that out feeds x directly): the router
+    grid of a layer may launch while the previous layer's kernels still run,
+    and must read x only after they have completed.  The outputs equal those
+    of the same calls with the stream synchronised between layers, bit for
+    bit, both eagerly and replayed from a CUDA graph."""
+    from dataclasses import replace
+    cfg = replace(dsgen.DECODE1, T=T, x_dtype="f32", router_dtype="f32", name=f"chain of layers T={T}")
+    sh = synthetic.shape_of(cfg)
+    assert ds.layer_path(sh, T) == (ds.PATH_STREAM if T == 1 else ds.PATH_DECODE3)
+    Ws = [synthetic.build_layer(cfg, layer=l) for l in range(4)]
+    x0 = synthetic.build_x(cfg)
+    ws = torch.empty(ds.workspace_bytes(sh, T), dtype=torch.uint8, device="cuda")
+    bufs = [torch.empty((T, cfg.D), dtype=torch.float32, device="cuda") for _ in range(4)]
+
+    def run(sync):
+        x = x0
+        for l in range(4):
+            ds.layer(sh, Ws[l], x, bufs[l], ws)
+            if sync:
+                torch.cuda.synchronize()
+            x = bufs[l]
+
+    run(True)
+    ref = [b.cpu().numpy().copy() for b in bufs]
+    assert all(np.isfinite(r).all() for r in ref)
+    for b in bufs:
+        b.fill_(float("nan"))
+    for _ in range(3):
+        run(False)
+    torch.cuda.synchronize()
+    ds.sync_status()
+    for l in range(4):
+        assert np.array_equal(bufs[l].cpu().numpy(), ref[l]), f"layer {l}"
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(False)
+    for b in bufs:
+        b.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ds.sync_status()
+    for l in range(4):
+        assert np.array_equal(bufs[l].cpu().numpy(), ref[l]), f"layer {l} (graph)"
+
+
 def test_batch_invariance_small_width():
     """At width 1024: tokens of a 2-token batch equal the same tokens in a
     3-token batch bit for bit (three-kernel path); a token alone (one-token
