@@ -18,8 +18,10 @@
  *   - Every pointer is a DEVICE pointer unless the argument says "host".
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call is asynchronous on that stream unless stated.
- *   - The library allocates no device memory: the caller owns every buffer,
- *     including the workspace, and nothing is retained after a call returns.
+ *   - The library allocates no device memory for a call: the caller owns
+ *     every buffer, including the workspace, and nothing is retained after a
+ *     call returns.  (Per device it keeps one status word, and
+ *     ds_moe_layer_noalloc's static scratch; ds_moe_cache keeps host state.)
  *   - Argument errors are detected on the host before any launch and return
  *     DS_ERR_INVALID_ARG (or DS_ERR_UNSUPPORTED) with a message in err.
  *     Errors a kernel detects (a non-finite weight given to the quantiser,
