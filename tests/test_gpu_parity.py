@@ -224,12 +224,12 @@ def _small(T, Fs, k=2, E=16, dtype="f32"):
                                             (1, 512, 6, 16, "bf16"), (1, 0, 16, 16, "f32"),
                                             (2, 1024, 4, 40, "bf16"), (1, 128, 1, 3, "f32"),
                                             (3, 256, 2, 16, "f32"), (4, 256, 4, 16, "f32"),
-                                            (8, 0, 16, 16, "f32")])
+                                            (1, 512, 8, 16, "bf16"), (8, 0, 16, 16, "f32")])
 def test_small_decode_variants(T, Fs, k, E, dtype):
-    """Decode-sized batches at a reduced width: the one-token kernel, the
-    three-kernel chain (up to four tokens here: fp32 inputs do not take the
-    batched kernels) and the grouped path, including k = E, one expert per
-    token, odd E and no shared expert."""
+    """Decode-sized batches at a reduced width: the one-token kernel (up to its
+    largest top-k, 8), the three-kernel chain (up to four tokens here: fp32
+    inputs do not take the batched kernels) and the grouped path, including
+    k = E, one expert per token, odd E and no shared expert."""
     layer_parity(_small(T, Fs, k, E, dtype), DECODE_TOL)
 
 

@@ -186,3 +186,42 @@ def test_cache_object_over_layers(n_slots):
             assert st["hits"] == 0
     finally:
         c.close()
+
+
+def test_zero_tokens_and_cache_gemv_path():
+    """T = 0 through the resident entry point and the cache object is a
+    no-op; an eight-token call through the cache (the GEMV path) matches the
+    oracle and fills slots like any other call."""
+    cfg = tiny(8)
+    sh = synthetic.shape_of(cfg)
+    W = synthetic.build_layer(cfg)
+    host = pinned_copy(W.experts)
+    eb = ds.expert_bytes(cfg.D, cfg.F, sh.expert_format)
+    slot = torch.full((cfg.E,), -1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(ds.workspace_bytes(sh, 8), dtype=torch.uint8, device="cuda")
+    x0 = torch.empty((0, cfg.D), dtype=torch.int16, device="cuda")
+    out0 = torch.empty((0, cfg.D), dtype=torch.float32, device="cuda")
+    ds.layer_resident(sh, replace(W, experts=None), slot, None, host, x0, out0, ws)
+    slots = torch.zeros((4, eb), dtype=torch.uint8, device="cuda")
+    tables = torch.zeros((1, cfg.E), dtype=torch.int32, device="cuda")
+    c = ds.ExpertCache(sh, [host], slots, 4, tables)
+    try:
+        c.layer(0, replace(W, experts=None), x0, out0, ws)
+        assert c.stats() == {"hits": 0, "misses": 0, "resident": 0}
+        lo = oracle.LayerOracle(cfg)
+        att = oracle.resample_attempts(cfg, lo)
+        x = synthetic.build_x(cfg, att)
+        out = torch.full((8, cfg.D), float("nan"), dtype=torch.float32, device="cuda")
+        c.layer(0, replace(W, experts=None), x, out, ws)
+        ds.sync_status()
+        assert c.stats()["resident"] == 4
+        lo_x = oracle.as_f64(dsgen.host_x(cfg, att), cfg.x_dtype)
+        rids, rw = oracle.select(lo.logits(lo_x), cfg.k)
+        ref = oracle.moe_layer(lo_x, lo.experts(rids), lo.shared, rids, rw, cfg.D, cfg.E, cfg.F, cfg.Fs,
+                               fmt=cfg.expert_fmt)
+        got = out.cpu().numpy().astype(np.float64)
+        rms = np.sqrt(np.mean(ref ** 2))
+        assert np.max(np.abs(got - ref)) <= DECODE_TOL * rms
+    finally:
+        c.close()
+
