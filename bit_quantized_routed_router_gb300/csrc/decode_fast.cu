@@ -697,6 +697,21 @@ __device__ bool s_wait(uint64_t *bar, uint32_t par, StreamShared &S, unsigned *s
   return true;
 }
 
+// One row of an expert that has no cache slot, copied by the calling warp
+// from host memory into its place in the stage (coalesced 16-byte loads; the
+// producer copied nothing into that place), so that the dot reads it like a
+// copied row.  One chunk per lane at a time keeps the registers of the
+// streaming path free.  The proxy fence orders these stores before the bulk
+// copies that later refill the stage.
+__device__ __forceinline__ void warp_copy_row(const uint8_t *g, uint8_t *s, int bytes) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int o = 16 * lane; o < bytes; o += 512)
+    *reinterpret_cast<uint4 *>(s + o) = __ldcs(reinterpret_cast<const uint4 *>(g + o));
+  fence_proxy_async();
+  __syncwarp();
+}
+
 // Bounded wait (one thread) for the route to be published.
 __device__ bool s_wait_ready(StreamShared &S, unsigned *status) {
   const uint64_t t0 = globaltimer_ns();
@@ -960,13 +975,12 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
         typename RD::Row gp, up;
         bool far;
         const uint8_t *hrow = expert_at(a, S.rt_used[u], far) + (int64_t)f * rowb_d;
-        if (far) {  // the expert's rows are read from host memory
-          RD::load_g(hrow, gp);
-          RD::load_g(hrow + a.gate_bytes, up);
-        } else {
-          RD::load_s(src + (size_t)warp * rowb_d, gp);
-          RD::load_s(src + (size_t)(S_GU + warp) * rowb_d, up);
+        if (far) {  // the expert's rows, from host memory into their place in the stage
+          warp_copy_row(hrow, const_cast<uint8_t *>(src) + (size_t)warp * rowb_d, rowb_d);
+          warp_copy_row(hrow + a.gate_bytes, const_cast<uint8_t *>(src) + (size_t)(S_GU + warp) * rowb_d, rowb_d);
         }
+        RD::load_s(src + (size_t)warp * rowb_d, gp);
+        RD::load_s(src + (size_t)(S_GU + warp) * rowb_d, up);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[st]);
         const float gu[2] = {RD::dot_reg(gp, xr), RD::dot_reg(up, xr)};
@@ -1092,8 +1106,10 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
     auto load_down_row = [&](int p, typename RF::Row &row) {
       bool far;
       const uint8_t *hp = expert_at(a, S.rt_used[p / rb], far);
-      if (far) RF::load_g(hp + 2 * a.gate_bytes + (int64_t)((bid + G * m) * rb + p % rb) * rowb_f, row);
-      else RF::load_s(routed + (size_t)p * rowb_f, row);
+      if (far)
+        warp_copy_row(hp + 2 * a.gate_bytes + (int64_t)((bid + G * m) * rb + p % rb) * rowb_f,
+                      const_cast<uint8_t *>(routed) + (size_t)p * rowb_f, rowb_f);
+      RF::load_s(routed + (size_t)p * rowb_f, row);
     };
     float y[2] = {0.f, 0.f};
     if (two) {
