@@ -244,11 +244,11 @@ def gpu_arm(args, rank, world, local_rank):
 
 LAUNCHES_PER_DECODE_STEP = 2  # router logits; the one-token streaming kernel
 # DRAM bytes read + written by one decode step, from one ncu capture of these
-# kernels as they stand (route_kernel 2,118,144 read; stream_kernel
-# 100,034,304 read + 2,914,816 written; the commands are in the decode profile
+# kernels as they stand (route_kernel 2,118,912 read; stream_kernel
+# 100,035,840 read + 2,830,080 written; the commands are in the decode profile
 # summary).  Set to None whenever either kernel changes until it is captured
 # again.
-DECODE_STEP_DRAM_BYTES = None
+DECODE_STEP_DRAM_BYTES = 104_984_832
 
 PREFILL_FLOPS = 1.4517e12  # 4096 x (6*3*2*D*F + 3*2*D*F + 2*D*E) at the Flash shape
 
@@ -421,16 +421,22 @@ def time_resident(cfg, R, budgets, n_tokens, dev):
         ds.sync_status()
         st0 = c.stats()
         torch.cuda.synchronize(dev)
+        calls = []
         t0 = time.perf_counter()
         for t in range(n_tokens):
             for r in range(R):
-                c.layer(r, Ws[r], xs[t], out, ws)
+                t1 = time.perf_counter()
+                c.layer(r, Ws[r], xs[t], out, ws)  # synchronous: it reads back the route
+                calls.append(time.perf_counter() - t1)
         torch.cuda.synchronize(dev)
         ms = (time.perf_counter() - t0) * 1e3 / (n_tokens * R)
         ds.sync_status()
         st1 = c.stats()
         hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
+        calls.sort()
         res[f"{frac:g}"] = {"slots": n_slots, "cache_gb": n_slots * eb / 1e9, "ms_per_layer": ms,
+                            "median_ms_per_call": calls[len(calls) // 2] * 1e3,
+                            "max_ms_per_call": calls[-1] * 1e3,
                             "tokens_per_s_per_layer": 1e3 / ms, "hit_rate": hits / max(1, hits + misses),
                             "host_expert_bytes_per_call": misses * eb / (n_tokens * R)}
         c.close()

@@ -32,6 +32,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -68,15 +69,17 @@ enum { MODE_GU = 0, MODE_DN = 1, MODE_ROUTER = 2 };
 
 // Pipeline shape per contraction: a stage holds A_TILES weight tiles (gate
 // and up, or one) and a token tile of NMAX rows; RAW slots of raw blocks
-// (one per 256-wide K block) feed the dequant warps.  Q4_K blocks are 144
-// bytes: two raw slots (one block ahead) keep the pipeline within the
-// shared memory of a block.
+// (one per 256-wide K block) feed the dequant warps.  A Q2_K raw slot is
+// free again as soon as the dequant warps hold its rows in registers, so
+// one slot keeps a block in flight and the room goes to a fourth stage;
+// Q4_K blocks (144 bytes) are read from the slot stage by stage, so Q4_K
+// keeps two raw slots and three stages within the shared memory of a block.
 template <int MODE, int FMT = DS_Q2_K>
 struct TcCfg {
   static constexpr int A_TILES = MODE == MODE_ROUTER ? 1 : 2;  // gate + up, or two 128-row down blocks
   static constexpr int NMAX = MODE == MODE_GU ? TC_NGU : MODE == MODE_DN ? TC_NDN : TC_NRT;
-  static constexpr int STAGES = MODE == MODE_ROUTER ? 4 : 3;
-  static constexpr int RAW = MODE == MODE_ROUTER ? 1 : FMT == DS_Q4_K ? 2 : 3;
+  static constexpr int STAGES = MODE == MODE_ROUTER ? 4 : FMT == DS_Q4_K ? 3 : 4;
+  static constexpr int RAW = MODE == MODE_ROUTER ? 1 : FMT == DS_Q4_K ? 2 : 1;
   static constexpr uint32_t RAW_ROW = FMT == DS_Q4_K ? TC_RAW_ROW_Q4 : TC_RAW_ROW;
   static constexpr uint32_t STAGE_BYTES = (A_TILES + NMAX / 128) * TC_TILE_BYTES;
   static constexpr uint32_t RAW_BYTES = A_TILES * TC_BM * RAW_ROW;
@@ -361,8 +364,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // Raw blocks (one copy per weight row and 256-wide K block: a 96-byte
     // window holding the Q2_K block, or the 144-byte Q4_K block) of the
     // routed tiles run ahead of the stages: when the stages of the routed
-    // block c begin, blocks up to c + RAW - 1 are issued.  (ri, rkb) walks
-    // the routed blocks in the order the dequant warps consume them.
+    // block c begin, blocks up to c + RAW - 1 are issued (waiting for their
+    // slots), and block c + RAW as soon as its slot is free (checked before
+    // every stage, never waited for).  (ri, rkb) walks the routed blocks in
+    // the order the dequant warps consume them.
     if (lane == 0) {  // descriptors into the TMA unit's cache before the first copies
       const CUtensorMap *maps[8] = {&tm_raw, &tm_b_r32, &tm_b_r64, &tm_b_r96, &tm_b_routed, &tm_b_shared, &tm_a0, &tm_a1};
       for (int m = 0; m < 8; ++m)
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     int st_it = 0, rawq = 0, rawpos = 0, ri = 0, rkb = 0;
     bool ok = true;
-    auto issue_raw = [&]() -> int {  // 1 issued, 0 none left, -1 failed wait
+    auto issue_raw = [&](bool wait) -> int {  // 1 issued, 0 none left (or slot busy), -1 failed wait
       for (;;) {
         if (bid + G * ri >= n_tiles) return 0;
         const TcTile t = tile_of(ri);
@@ -382,8 +387,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int slot = rawq % TC_RAW_SLOTS;
       if (rawq >= TC_RAW_SLOTS) {
         int w = 1;
-        if (lane == 0) w = tc_wait(&S.raw_empty[slot], ((rawq / TC_RAW_SLOTS) & 1) ^ 1, S, a.status);
-        if (!__shfl_sync(0xffffffffu, w, 0)) return -1;
+        if (!wait) {
+          if (lane == 0) w = mbar_test_wait(&S.raw_empty[slot], ((rawq / TC_RAW_SLOTS) & 1) ^ 1);
+          if (!__shfl_sync(0xffffffffu, w, 0)) return 0;
+        } else {
+          if (lane == 0) w = tc_wait(&S.raw_empty[slot], ((rawq / TC_RAW_SLOTS) & 1) ^ 1, S, a.status);
+          if (!__shfl_sync(0xffffffffu, w, 0)) return -1;
+        }
       }
       const int rows = 2 * TC_BM;
       if (lane == 0) {
@@ -410,12 +420,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (routed && (kc & 3) == 0) {
           ++rawpos;
           while (rawq < rawpos + TC_RAW_SLOTS - 1) {
-            const int r = issue_raw();
+            const int r = issue_raw(true);
             if (r < 0) ok = false;
             if (r <= 0) break;
           }
           if (!ok) break;
         }
+        if (rawq < rawpos + TC_RAW_SLOTS) issue_raw(false);  // one block further once its slot is free
         const int s = st_it % TC_STAGES;
         if (st_it >= TC_STAGES) {
           int w = 1;
@@ -469,73 +480,101 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // Thread dt owns one weight row of every stage, all four of its
     // sub-blocks: gate/up: row dt (gate rows 0-127, then up rows); down: row
     // dt of the two 128-row blocks.  Its raw and destination offsets are fixed.
-    constexpr int NSUB = 4;
     const int dt = threadIdx.x - TC_DQ0 * 32;  // 0 .. 255
     const int r = dt;
-    const int jb = 0;
     const uint32_t raw_row = (uint32_t)r * C::RAW_ROW;
     const uint32_t dst_row = (uint32_t)((r / TC_BM) * TC_TILE_BYTES + (r % TC_BM) * 128);
     const int x7 = r & 7;
     int st_it = 0, raw_it = 0;
     bool ok = true;
+    // the next stage's slot, once the MMAs have released it (false: abort)
+    auto stage_begin = [&](int &s) -> bool {
+      s = st_it % TC_STAGES;
+      return st_it < TC_STAGES || tc_wait(&S.empty[s], ((st_it / TC_STAGES) & 1) ^ 1, S, a.status);
+    };
+    auto stage_end = [&](int s) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.full[s]);
+      ++st_it;
+    };
     for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
       const TcTile t = tile_of(i);
-      const int K = tile_k<MODE>(a, t), nk = K / TC_BK;
-      const bool routed = t.kind == 0;
-      for (int kc = 0; ok && kc < nk; ++kc) {
+      const int nk = tile_k<MODE>(a, t) / TC_BK;
+      if (t.kind != 0) {  // dense shared-expert tile: its weights come by copy
+        for (int kc = 0; ok && kc < nk; ++kc) {
+          int s;
+          if (!stage_begin(s)) { ok = false; break; }
+          stage_end(s);
+        }
+        continue;
+      }
+      for (int kb = 0; ok && kb < nk / 4; ++kb) {  // one 256-wide block: four stages
         const int slot = raw_it % TC_RAW_SLOTS;
-        if (routed && (kc & 3) == 0 && !tc_wait(&S.raw_full[slot], (raw_it / TC_RAW_SLOTS) & 1, S, a.status)) {
-          ok = false;
-          break;
-        }
-        const int s = st_it % TC_STAGES;
-        if (st_it >= TC_STAGES && !tc_wait(&S.empty[s], ((st_it / TC_STAGES) & 1) ^ 1, S, a.status)) {
-          ok = false;
-          break;
-        }
-        if (routed && FMT == DS_Q4_K) {
-          // sub-blocks 2 q4 and 2 q4 + 1 of the block: eight chunks of the row
-          uint8_t *dst = stages + (size_t)s * TC_STAGE_BYTES + dst_row;
-          const uint8_t *blk = raw + (size_t)slot * TC_RAW_BYTES + raw_row;
-          const int q4 = kc & 3;
-          const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+        if (!tc_wait(&S.raw_full[slot], (raw_it / TC_RAW_SLOTS) & 1, S, a.status)) { ok = false; break; }
+        const uint8_t *rb = raw + (size_t)slot * TC_RAW_BYTES + raw_row;
+        if (FMT == DS_Q4_K) {
+          const uint4 hdr = *reinterpret_cast<const uint4 *>(rb);
           const float d = fp16_to_f32((uint16_t)(hdr.x & 0xFFFFu)), dmin = fp16_to_f32((uint16_t)(hdr.x >> 16));
+          for (int q4 = 0; q4 < 4; ++q4) {  // sub-blocks 2 q4 and 2 q4 + 1: eight chunks of the row
+            int s;
+            if (!stage_begin(s)) { ok = false; break; }
+            uint8_t *dst = stages + (size_t)s * TC_STAGE_BYTES + dst_row;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int sb = 2 * q4 + j;
-            const float dsc = d * (float)q4k_field(hdr, sb), dmm = dmin * (float)q4k_field(hdr, 8 + sb);  // exact
-            uint4 c4[4];
-            dequant_q4_sub(*reinterpret_cast<const uint4 *>(blk + 16 + 16 * sb), dsc, dmm, c4);
+            for (int j = 0; j < 2; ++j) {
+              const int sb = 2 * q4 + j;
+              const float dsc = d * (float)q4k_field(hdr, sb), dmm = dmin * (float)q4k_field(hdr, 8 + sb);  // exact
+              uint4 c4[4];
+              dequant_q4_sub(*reinterpret_cast<const uint4 *>(rb + 16 + 16 * sb), dsc, dmm, c4);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(dst + (((4 * j + c) ^ x7) << 4)) = c4[c];
+              for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(dst + (((4 * j + c) ^ x7) << 4)) = c4[c];
+            }
+            fence_proxy_async();
+            stage_end(s);
           }
-          fence_proxy_async();
-        } else if (routed) {
-          uint8_t *dst = stages + (size_t)s * TC_STAGE_BYTES + dst_row;
-          // the block's bytes start (84 kb) mod 16 into its 96-byte copy
-          const uint8_t *blk = raw + (size_t)slot * TC_RAW_BYTES + raw_row + ((uint32_t)(QB * (kc >> 2)) & 15u);
-          const int q4 = kc & 3;  // quarter of the block in this stage: sub-blocks 4 q4 ..
-          const uint32_t scw = *reinterpret_cast<const uint32_t *>(blk + 4 * q4);
-          const uint32_t dd = *reinterpret_cast<const uint32_t *>(blk + 80);
-          const float d = fp16_to_f32((uint16_t)(dd & 0xFFFFu)), dmin = fp16_to_f32((uint16_t)(dd >> 16));
-#pragma unroll
-          for (int jj = 0; jj < NSUB; ++jj) {
-            const int j = jb + jj;
-            const uint32_t codes = *reinterpret_cast<const uint32_t *>(blk + 16 + 4 * (4 * q4 + j));
-            uint4 c0, c1;
-            dequant_codes(codes, (scw >> (8 * j)) & 0xFFu, d, dmin, c0, c1);
-            *reinterpret_cast<uint4 *>(dst + (((2 * j) ^ x7) << 4)) = c0;
-            *reinterpret_cast<uint4 *>(dst + (((2 * j + 1) ^ x7) << 4)) = c1;
-          }
-          fence_proxy_async();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.full[s]);
-        if (routed && (kc & 3) == 3) {
+          __syncwarp();
           if (lane == 0) mbar_arrive(&S.raw_empty[slot]);
-          ++raw_it;
+        } else {
+          // The row's 96-byte window in registers with six 16-byte loads (at
+          // the 96-byte row pitch these conflict two ways, where word loads
+          // conflict eight ways); the raw slot is free once they are done.
+          uint32_t W[24];
+#pragma unroll
+          for (int c = 0; c < 6; ++c) {
+            const uint4 v = reinterpret_cast<const uint4 *>(rb)[c];
+            W[4 * c] = v.x; W[4 * c + 1] = v.y; W[4 * c + 2] = v.z; W[4 * c + 3] = v.w;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.raw_empty[slot]);
+          // the block starts (84 kb) mod 16 bytes = word kb mod 4 into the window
+          auto block = [&](auto oc) -> bool {
+            constexpr int O = decltype(oc)::value;
+            const float d = fp16_to_f32((uint16_t)(W[O + 20] & 0xFFFFu)), dmin = fp16_to_f32((uint16_t)(W[O + 20] >> 16));
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {  // quarter of the block in this stage: sub-blocks 4 q4 ..
+              int s;
+              if (!stage_begin(s)) return false;
+              uint8_t *dst = stages + (size_t)s * TC_STAGE_BYTES + dst_row;
+              const uint32_t scw = W[O + q4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint4 c0, c1;
+                dequant_codes(W[O + 4 + 4 * q4 + j], (scw >> (8 * j)) & 0xFFu, d, dmin, c0, c1);
+                *reinterpret_cast<uint4 *>(dst + (((2 * j) ^ x7) << 4)) = c0;
+                *reinterpret_cast<uint4 *>(dst + (((2 * j + 1) ^ x7) << 4)) = c1;
+              }
+              fence_proxy_async();
+              stage_end(s);
+            }
+            return true;
+          };
+          switch (kb & 3) {
+            case 0: ok = block(std::integral_constant<int, 0>()); break;
+            case 1: ok = block(std::integral_constant<int, 1>()); break;
+            case 2: ok = block(std::integral_constant<int, 2>()); break;
+            default: ok = block(std::integral_constant<int, 3>()); break;
+          }
         }
-        ++st_it;
+        ++raw_it;
       }
     }
   } else if (warp == TC_MMA_WARP) {
