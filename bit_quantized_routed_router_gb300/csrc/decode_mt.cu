@@ -84,6 +84,8 @@ constexpr int MT_DN_R = 8;                                 // routed down rows p
 constexpr int MT_DN_NR = MT_CONS * MT_DN_R;                // rows per down tile (64)
 static_assert(2 * MT_GU_NR * MT_CB <= (int)MT_STAGE && MT_DN_NR * MT_CB <= (int)MT_STAGE, "routed tile");
 static_assert(MT_SH_BOX + 2 * MT_MAXT * 128 <= MT_STAGE, "shared tile");
+static_assert(2 * MT_GU_RP <= 8 && 32 % (2 * MT_GU_RP) == 0 && MT_DN_R <= 8 && 32 % MT_DN_R == 0,
+              "values per warp: at most eight, spread evenly over the lanes");
 
 struct MtArgs {
   int D, E, F, Fs, k, T, T8, P;
@@ -499,16 +501,18 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
     const int u = d.y, g = d.z, cl = d.w;
     const int e = s_used[u], base = s_off[e], n = s_cnt[e];
     const uint8_t *tile = stages + (size_t)st * MT_STAGE;
-    const int vi = lane >> 2;  // lane 4 i holds value i: gate rows 0-3, up rows 0-3
-    const int f = g * MT_GU_NR + warp * MT_GU_RP + (vi & 3);
+    // lane LV i holds value i: the warp's gate rows, then its up rows
+    constexpr int LV = 32 / (2 * MT_GU_RP);
+    const int vi = lane / LV;
+    const int f = g * MT_GU_NR + warp * MT_GU_RP + vi % MT_GU_RP;
     auto emit = [&](int j, float tot) {
-      if ((lane & 3) == 0) {
+      if (lane % LV == 0) {
         if (NCq > 1) {
           float *acc = s_acc + ((size_t)warp * T + j) * 8 + vi;
           tot = cl == 0 ? tot : *acc + tot;
           *acc = tot;
         }
-        if (cl == NCq - 1) (vi < 4 ? a.gp : a.up)[((int64_t)q * P + base + j) * F + f] = tot;
+        if (cl == NCq - 1) (vi < MT_GU_RP ? a.gp : a.up)[((int64_t)q * P + base + j) * F + f] = tot;
       }
     };
     auto row_of = [&](int i) {
@@ -754,10 +758,11 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
     const int u = d.y, g = d.z, cl = d.w & 255;
     const int base = s_base[u], n = s_cnt[u];
     const uint8_t *tile = stages + (size_t)st * MT_STAGE;
-    const int vi = lane >> 2;  // lane 4 i holds row i's value
+    constexpr int LV = 32 / MT_DN_R;  // lane LV i holds row i's value
+    const int vi = lane / LV;
     const int drow = g * MT_DN_NR + warp * MT_DN_R + vi;
     auto emit = [&](int j, float tot) {
-      if ((lane & 3) == 0) {
+      if (lane % LV == 0) {
         if (NCqd > 1) {
           float *acc = s_acc + ((size_t)warp * T + j) * 8 + vi;
           tot = cl == 0 ? tot : *acc + tot;
