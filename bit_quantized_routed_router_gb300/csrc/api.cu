@@ -500,7 +500,9 @@ int ds_moe_sync_status(void *stream, char *err, size_t errlen) {
   if (v & ST_TIMEOUT) return fail(err, errlen, DS_ERR_TIMEOUT, "a device wait timed out (status 0x%x)", v);
   if (v & ST_QUANT_INPUT)
     return fail(err, errlen, DS_ERR_DEVICE_CHECK, "quantiser input not finite or |w| > 65504 (status 0x%x)", v);
-  if (v & ST_BAD_ID) return fail(err, errlen, DS_ERR_DEVICE_CHECK, "expert id out of range (status 0x%x)", v);
+  if (v & ST_BAD_ID)
+    return fail(err, errlen, DS_ERR_DEVICE_CHECK,
+                "a token with fewer than top_k non-NaN router logits, or an expert id out of range (status 0x%x)", v);
   if (v & ST_RANGE)
     return fail(err, errlen, DS_ERR_DEVICE_CHECK,
                 "a value beyond the fp16 range reached the tensor-core path and was saturated (status 0x%x)", v);

@@ -17,7 +17,7 @@ constexpr int NUM_SMS = 152; // GB300
 // Sticky status bits (per device, read by ds_moe_sync_status).
 enum : unsigned {
   ST_QUANT_INPUT = 1u << 0,   // non-finite / out-of-range quantiser input
-  ST_BAD_ID = 1u << 1,        // expert id outside [0, E)
+  ST_BAD_ID = 1u << 1,        // expert id outside [0, E), or a pick with no candidate (NaN logits)
   ST_TIMEOUT = 1u << 2,       // a bounded device wait expired
   ST_BAD_COUNT = 1u << 3,     // route counts inconsistent
   ST_RANGE = 1u << 4,         // a value beyond the fp16 range met the tensor-core path (saturated)

@@ -179,6 +179,10 @@ int ds_moe_workspace_bytes(const ds_moe_shape *shape, int64_t T, size_t *bytes, 
  *        its contents need no initialisation and are scratch after return
  *   dbg  optional debug outputs (NULL to skip)
  * Tokens are independent: row t of out depends only on row t of x.
+ * A NaN router logit is never selected.  When fewer than top_k of a token's
+ * logits are numbers (a NaN in its x, say), its remaining picks take expert
+ * 0, its row of out is not meaningful, and ds_moe_sync_status reports
+ * DS_ERR_DEVICE_CHECK; nothing of such a call carries over into later calls.
  * T == 0 is a no-op.  The kernels that run depend on T and the shape (see
  * ds_moe_layer_path): one token at the instantiated widths with top_k <= 8
  * streams the whole layer through one cooperative kernel; up to four tokens
