@@ -43,8 +43,9 @@ namespace {
 
 constexpr int TC_BM = 128;                 // weight rows per tile (MMA M)
 constexpr int TC_BK = 64;                  // K per stage: one 128-byte swizzle row
-constexpr int TC_NGU = 128;                // tokens per gate/up tile at most
-constexpr int TC_NDN = 128;                // tokens per down tile at most
+constexpr int TC_NGU = 128;                // tokens per gate/up or down tile at most, Q4_K
+constexpr int TC_NDN = 128;                //   (and the chunk the workspace is sized for)
+constexpr int TC_NWIDE = 256;              // tokens per gate/up or down tile at most, Q2_K
 constexpr int TC_NRT = 256;                // tokens per router tile at most
 constexpr uint32_t TC_TILE_BYTES = TC_BM * 128;       // one 128 x 64 operand tile (16 KB)
 constexpr uint32_t TC_RAW_ROW = 96;        // bytes copied per weight row and 256-weight block (Q2_K)
@@ -70,19 +71,29 @@ enum { MODE_GU = 0, MODE_DN = 1, MODE_ROUTER = 2 };
 // Pipeline shape per contraction: a stage holds A_TILES weight tiles (gate
 // and up, or one) and a token tile of NMAX rows; RAW slots of raw blocks
 // (one per 256-wide K block) feed the dequant warps.  A Q2_K raw slot is
-// free again as soon as the dequant warps hold its rows in registers, so
-// one slot keeps a block in flight and the room goes to a fourth stage;
-// Q4_K blocks (144 bytes) are read from the slot stage by stage, so Q4_K
-// keeps two raw slots and three stages within the shared memory of a block.
+// free again as soon as the dequant warps hold its rows in registers, so one
+// slot keeps a block in flight, and the ring has one of two layouts, which
+// the tile plan chooses per launch: four stages of up to 128 tokens, or
+// (when experts with more than 128 tokens make it worth it) three stages of
+// up to 256 tokens, so that such an expert is dequantised once per 256 of
+// its tokens instead of per 128.  Q4_K blocks (144 bytes) are read from the
+// slot stage by stage, so Q4_K keeps two raw slots and three stages of 128
+// tokens within the shared memory of a block.
 template <int MODE, int FMT = DS_Q2_K>
 struct TcCfg {
   static constexpr int A_TILES = MODE == MODE_ROUTER ? 1 : 2;  // gate + up, or two 128-row down blocks
-  static constexpr int NMAX = MODE == MODE_GU ? TC_NGU : MODE == MODE_DN ? TC_NDN : TC_NRT;
+  static constexpr int NMAX = MODE == MODE_ROUTER ? TC_NRT : TC_NGU;
   static constexpr int STAGES = MODE == MODE_ROUTER ? 4 : FMT == DS_Q4_K ? 3 : 4;
   static constexpr int RAW = MODE == MODE_ROUTER ? 1 : FMT == DS_Q4_K ? 2 : 1;
   static constexpr uint32_t RAW_ROW = FMT == DS_Q4_K ? TC_RAW_ROW_Q4 : TC_RAW_ROW;
   static constexpr uint32_t STAGE_BYTES = (A_TILES + NMAX / 128) * TC_TILE_BYTES;
   static constexpr uint32_t RAW_BYTES = A_TILES * TC_BM * RAW_ROW;
+  // the wide layout
+  static constexpr bool WIDE = MODE != MODE_ROUTER && FMT == DS_Q2_K;
+  static constexpr int NMAX_W = TC_NWIDE, STAGES_W = 3;
+  static constexpr uint32_t STAGE_BYTES_W = (A_TILES + NMAX_W / 128) * TC_TILE_BYTES;
+  static constexpr uint32_t RING_BYTES =
+      WIDE && STAGES_W * STAGE_BYTES_W > STAGES * STAGE_BYTES ? STAGES_W * STAGE_BYTES_W : STAGES * STAGE_BYTES;
 };
 
 struct TcArgs {
@@ -94,6 +105,7 @@ struct TcArgs {
   int64_t expert_bytes, gate_bytes;
   const int4 *tiles;
   const int *n_tiles;
+  const int *wide;         // non-zero: the plan chose the wide layout (Q2_K gate/up and down)
   uint16_t *h16;  // fp16: routed rows [P][F] (K order permuted), then shared rows [T][Fs]
   float *y;       // [P][D] routed outputs, perm order
   float *ys;      // [T][D] shared output
@@ -305,8 +317,9 @@ template <int MODE, int FMT = DS_Q2_K>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tm_raw,
                    const __grid_constant__ CUtensorMap tm_b_r32, const __grid_constant__ CUtensorMap tm_b_r64,
-                   const __grid_constant__ CUtensorMap tm_b_r96, const __grid_constant__ CUtensorMap tm_b_routed,
-                   const __grid_constant__ CUtensorMap tm_b_shared, const __grid_constant__ CUtensorMap tm_a0,
+                   const __grid_constant__ CUtensorMap tm_b_r96, const __grid_constant__ CUtensorMap tm_b_r128,
+                   const __grid_constant__ CUtensorMap tm_b_routed, const __grid_constant__ CUtensorMap tm_b_shared,
+                   const __grid_constant__ CUtensorMap tm_b_shared_w, const __grid_constant__ CUtensorMap tm_a0,
                    const __grid_constant__ CUtensorMap tm_a1) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base (the swizzle pattern repeats every 1024 bytes);
@@ -314,9 +327,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *stages = smem;
   using C = TcCfg<MODE, FMT>;
-  constexpr int TC_STAGES = C::STAGES, TC_RAW_SLOTS = C::RAW;
-  constexpr uint32_t TC_STAGE_BYTES = C::STAGE_BYTES, TC_RAW_BYTES = C::RAW_BYTES;
-  uint8_t *raw = smem + TC_STAGES * TC_STAGE_BYTES;
+  constexpr int TC_RAW_SLOTS = C::RAW;
+  constexpr uint32_t TC_RAW_BYTES = C::RAW_BYTES;
+  // the ring layout of this launch (every role reads the same word)
+  const bool wl = C::WIDE && *a.wide != 0;
+  const int TC_STAGES = wl ? C::STAGES_W : C::STAGES, NMAX = wl ? C::NMAX_W : C::NMAX;
+  const uint32_t TC_STAGE_BYTES = wl ? C::STAGE_BYTES_W : C::STAGE_BYTES;
+  uint8_t *raw = smem + C::RING_BYTES;
   TcShared &S = *reinterpret_cast<TcShared *>(raw + TC_RAW_SLOTS * TC_RAW_BYTES);
   constexpr bool GU = MODE == MODE_GU;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -369,11 +386,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // every stage, never waited for).  (ri, rkb) walks the routed blocks in
     // the order the dequant warps consume them.
     if (lane == 0) {  // descriptors into the TMA unit's cache before the first copies
-      const CUtensorMap *maps[8] = {&tm_raw, &tm_b_r32, &tm_b_r64, &tm_b_r96, &tm_b_routed, &tm_b_shared, &tm_a0, &tm_a1};
-      for (int m = 0; m < 8; ++m)
+      const CUtensorMap *maps[10] = {&tm_raw,      &tm_b_r32,    &tm_b_r64,      &tm_b_r96, &tm_b_r128,
+                                     &tm_b_routed, &tm_b_shared, &tm_b_shared_w, &tm_a0,    &tm_a1};
+      for (int m = 0; m < 10; ++m)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(maps[m])) : "memory");
     }
     int st_it = 0, rawq = 0, rawpos = 0, ri = 0, rkb = 0;
+    int sl = 0, ph = 0;  // slot and phase of stage st_it (no division by the runtime stage count)
     bool ok = true;
     auto issue_raw = [&](bool wait) -> int {  // 1 issued, 0 none left (or slot busy), -1 failed wait
       for (;;) {
@@ -427,21 +446,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (!ok) break;
         }
         if (rawq < rawpos + TC_RAW_SLOTS) issue_raw(false);  // one block further once its slot is free
-        const int s = st_it % TC_STAGES;
+        const int s = sl;
         if (st_it >= TC_STAGES) {
           int w = 1;
-          if (lane == 0) w = tc_wait(&S.empty[s], ((st_it / TC_STAGES) & 1) ^ 1, S, a.status);
+          if (lane == 0) w = tc_wait(&S.empty[s], ph ^ 1, S, a.status);
           if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
         }
         uint8_t *stage = stages + (size_t)s * TC_STAGE_BYTES;
         if (lane == 0) {
-          // one box of token rows: the tile's width rounded up to 32 (routed
-          // tiles) or NMAX (shared ones); rows past the tile's tokens only
-          // feed accumulator columns that are never read
-          const int bsel = routed && MODE != MODE_ROUTER ? min((t.n - 1) >> 5, 3) : 3;
-          const CUtensorMap *bm = !routed ? &tm_b_shared
-                                  : bsel == 0 ? &tm_b_r32 : bsel == 1 ? &tm_b_r64 : bsel == 2 ? &tm_b_r96 : &tm_b_routed;
-          uint32_t bytes = routed ? (uint32_t)(bsel + 1) * 32 * 128 : (uint32_t)C::NMAX * 128;
+          // one box of token rows: a routed tile's width rounded up to 32
+          // (up to 128 tokens) or NMAX (wider routed tiles, and shared ones);
+          // rows past the tile's tokens only feed accumulator columns that
+          // are never read
+          const int bsel = routed && MODE != MODE_ROUTER ? (t.n > 128 ? 4 : (t.n - 1) >> 5) : 4;
+          const CUtensorMap *bm = !routed       ? (wl ? &tm_b_shared_w : &tm_b_shared)
+                                  : bsel == 0 ? &tm_b_r32
+                                  : bsel == 1 ? &tm_b_r64
+                                  : bsel == 2 ? &tm_b_r96
+                                  : bsel == 3 ? &tm_b_r128
+                                              : &tm_b_routed;
+          uint32_t bytes = (uint32_t)(bsel < 4 ? 32 * (bsel + 1) : NMAX) * 128;
           if (!routed) bytes += C::A_TILES * TC_TILE_BYTES;
           mbar_arrive_expect_tx(&S.full[s], bytes);
           uint8_t *bdst = stage + C::A_TILES * TC_TILE_BYTES;
@@ -460,6 +484,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         __syncwarp();
         ++st_it;
+        if (++sl == TC_STAGES) sl = 0, ph ^= 1;
       }
     }
     // every copy issued has landed before the block may end
@@ -485,17 +510,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t raw_row = (uint32_t)r * C::RAW_ROW;
     const uint32_t dst_row = (uint32_t)((r / TC_BM) * TC_TILE_BYTES + (r % TC_BM) * 128);
     const int x7 = r & 7;
-    int st_it = 0, raw_it = 0;
+    int st_it = 0, raw_it = 0, sl = 0, ph = 0;  // sl, ph: slot and phase of stage st_it
     bool ok = true;
     // the next stage's slot, once the MMAs have released it (false: abort)
     auto stage_begin = [&](int &s) -> bool {
-      s = st_it % TC_STAGES;
-      return st_it < TC_STAGES || tc_wait(&S.empty[s], ((st_it / TC_STAGES) & 1) ^ 1, S, a.status);
+      s = sl;
+      return st_it < TC_STAGES || tc_wait(&S.empty[s], ph ^ 1, S, a.status);
     };
     auto stage_end = [&](int s) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.full[s]);
       ++st_it;
+      if (++sl == TC_STAGES) sl = 0, ph ^= 1;
     };
     for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
       const TcTile t = tile_of(i);
@@ -580,20 +606,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == TC_MMA_WARP) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      int st_it = 0;
+      // Accumulators: a tile up to 128 tokens wide takes one of the two
+      // 256-column buffers in turn (first accumulator at +0, second at +128);
+      // a wider one takes both (at 0 and 256).  The epilogue warps walk the
+      // same tiles and take the same buffers; fill0 and fill1 count the
+      // tiles that each buffer has held, which gives every wait its parity.
+      int st_it = 0, sl = 0, ph = 0, nnar = 0, fill0 = 0, fill1 = 0;  // sl, ph: slot and phase of stage st_it
       bool ok = true;
       for (int i = 0; ok && bid + G * i < n_tiles; ++i) {
         const TcTile t = tile_of(i);
         const int K = tile_k<MODE>(a, t), nk = K / TC_BK;
         const int nb = (t.n + 15) & ~15;
-        const int buf = i & 1;
-        if (i >= 2 && !tc_wait(&S.acc_empty[buf], ((i >> 1) & 1) ^ 1, S, a.status)) break;
+        const bool wide = C::A_TILES == 2 && nb > 128;
+        const int buf = wide ? 0 : (nnar++ & 1), blast = wide ? 1 : buf;
+        bool got = true;
+        for (int b = buf; b <= blast; ++b) {
+          const int f = b ? fill1 : fill0;
+          if (f > 0 && !tc_wait(&S.acc_empty[b], (f & 1) ^ 1, S, a.status)) got = false;
+        }
+        if (!got) break;
         tc_fence_after();
         const uint32_t idesc = f16_idesc(nb, (GU && t.kind == 1) || MODE == MODE_ROUTER);
-        const uint32_t d0 = tmem + (uint32_t)(buf * 256);
+        const uint32_t d0 = tmem + (uint32_t)(buf * 256), d1 = d0 + (wide ? 256u : 128u);
         for (int kc = 0; kc < nk; ++kc) {
-          const int s = st_it % TC_STAGES;
-          if (!tc_wait(&S.full[s], (st_it / TC_STAGES) & 1, S, a.status)) { ok = false; break; }
+          const int s = sl;
+          if (!tc_wait(&S.full[s], ph, S, a.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sbase = smem_u32(stages + (size_t)s * TC_STAGE_BYTES);
           const uint32_t bbase = sbase + C::A_TILES * TC_TILE_BYTES;
@@ -603,16 +640,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (C::A_TILES == 2) {  // gate and up, or two down blocks: two accumulators
               const bool acc = kc > 0 || kk > 0;
               mma_f16(d0, sw128_desc(sbase + 32 * kk), bd, idesc, acc);
-              mma_f16(d0 + 128, sw128_desc(sbase + TC_TILE_BYTES + 32 * kk), bd, idesc, acc);
+              mma_f16(d1, sw128_desc(sbase + TC_TILE_BYTES + 32 * kk), bd, idesc, acc);
             } else {
               mma_f16(d0, sw128_desc(sbase + 32 * kk), bd, idesc, kc > 0 || kk > 0);
             }
           }
           mma_commit(&S.empty[s]);  // the stage is free once these MMAs have read it
           ++st_it;
+          if (++sl == TC_STAGES) sl = 0, ph ^= 1;
         }
         if (!ok) break;
-        mma_commit(&S.acc_full[buf]);
+        for (int b = buf; b <= blast; ++b) {
+          mma_commit(&S.acc_full[b]);
+          (b ? fill1 : fill0) += 1;
+        }
       }
       // nothing of this thread may still run when the accumulators are freed
       mma_commit(&S.drain);
@@ -625,12 +666,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ------------------------------------------------------ epilogue warps --
     const int q = warp;  // TMEM lanes 32 q .. 32 q + 31
     const int r = 32 * q + lane;
+    int nnar = 0, fill0 = 0, fill1 = 0;  // the MMA thread's buffer choice, tile by tile
     for (int i = 0; bid + G * i < n_tiles; ++i) {
       const TcTile t = tile_of(i);
-      const int buf = i & 1;
-      if (!tc_wait(&S.acc_full[buf], (i >> 1) & 1, S, a.status)) break;
+      const bool wide = C::A_TILES == 2 && ((t.n + 15) & ~15) > 128;
+      const int buf = wide ? 0 : (nnar++ & 1), blast = wide ? 1 : buf;
+      bool got = true;
+      for (int b = buf; b <= blast; ++b)
+        if (!tc_wait(&S.acc_full[b], (b ? fill1 : fill0) & 1, S, a.status)) got = false;
+      if (!got) break;
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 256);
+      const uint32_t off2 = wide ? 256u : 128u;  // the second accumulator
       if (GU) {
         const int f = t.blk * TC_BM + r;
         const int ld = t.kind == 0 ? a.F : a.Fs;
@@ -640,7 +687,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int j0 = 0; j0 < t.n; j0 += 16) {
           float g[16], u[16];
           tmem_ld16(tl + j0, g);
-          tmem_ld16(tl + 128 + j0, u);
+          tmem_ld16(tl + off2 + j0, u);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (j0 + j < t.n) {
@@ -665,7 +712,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int j0 = 0; j0 < t.n; j0 += 16) {
           float v[16], w[16];
           tmem_ld16(tl + j0, v);
-          tmem_ld16(tl + 128 + j0, w);
+          tmem_ld16(tl + off2 + j0, w);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (j0 + j < t.n) {
@@ -676,7 +723,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acc_empty[buf]);
+      for (int b = buf; b <= blast; ++b) {
+        if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+        (b ? fill1 : fill0) += 1;
+      }
     }
   }
 
@@ -754,16 +804,31 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint16_t *__rest
 // Tile lists of both contractions from the route: shared-expert tiles
 // first (full token chunks), then per expert its token chunks times the
 // weight-row blocks (chunk-major, so neighbouring tiles share token rows).
-// One block of 1024 threads, one thread per expert.
+// Tokens per tile at most: 128, or with allow_wide 256 when that cuts the
+// routed chunks by more than a tenth (experts with more than 128 tokens);
+// *wide records the choice for the two GEMM launches, whose ring layout
+// follows it.  One block of 1024 threads, one thread per expert.
 __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict__ counts,
                                                        const int32_t *__restrict__ offsets, int E, int64_t T,
-                                                       int64_t P, int D, int F, int Fs, int4 *__restrict__ gu,
-                                                       int4 *__restrict__ dn, int *__restrict__ n_gu,
-                                                       int *__restrict__ n_dn) {
+                                                       int64_t P, int D, int F, int Fs, int allow_wide,
+                                                       int4 *__restrict__ gu, int4 *__restrict__ dn,
+                                                       int *__restrict__ n_gu, int *__restrict__ n_dn,
+                                                       int *__restrict__ wide) {
   __shared__ int scan_gu[1024], scan_dn[1024];
+  __shared__ int n128, n256;
   const int e = threadIdx.x;
   const int ne = e < E ? counts[e] : 0;
-  const int cg = (ne + TC_NGU - 1) / TC_NGU, cd = (ne + TC_NDN - 1) / TC_NDN;
+  if (e == 0) n128 = n256 = 0;
+  __syncthreads();
+  if (allow_wide && ne > 0) {
+    atomicAdd(&n128, (ne + TC_NGU - 1) / TC_NGU);
+    atomicAdd(&n256, (ne + TC_NWIDE - 1) / TC_NWIDE);
+  }
+  __syncthreads();
+  const bool w = allow_wide && 10 * n256 < 9 * n128;
+  const int chunk = w ? TC_NWIDE : TC_NGU;
+  if (e == 0) *wide = w ? 1 : 0;
+  const int cg = (ne + chunk - 1) / chunk, cd = (ne + chunk - 1) / chunk;
   const int tg = cg * (F / TC_BM), td = cd * (D / (2 * TC_BM));
   scan_gu[e] = tg;
   scan_dn[e] = td;
@@ -775,18 +840,18 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict
     scan_dn[e] += b;
     __syncthreads();
   }
-  const int sg_chunks = Fs > 0 ? (int)((T + TC_NGU - 1) / TC_NGU) : 0;
-  const int sd_chunks = Fs > 0 ? (int)((T + TC_NDN - 1) / TC_NDN) : 0;
+  const int sg_chunks = Fs > 0 ? (int)((T + chunk - 1) / chunk) : 0;
+  const int sd_chunks = Fs > 0 ? (int)((T + chunk - 1) / chunk) : 0;
   const int n_sg = sg_chunks * (Fs / TC_BM), n_sd = sd_chunks * (D / (2 * TC_BM));
   // shared tiles
   for (int i = e; i < n_sg; i += 1024) {
     const int c = i / (Fs / TC_BM), b = i % (Fs / TC_BM);
-    const int t0 = c * TC_NGU, n = (int)min((int64_t)TC_NGU, T - t0);
+    const int t0 = c * chunk, n = (int)min((int64_t)chunk, T - t0);
     gu[i] = make_int4(1, 0, t0, n | (b << 16));
   }
   for (int i = e; i < n_sd; i += 1024) {
     const int c = i / (D / (2 * TC_BM)), b = i % (D / (2 * TC_BM));
-    const int t0 = c * TC_NDN, n = (int)min((int64_t)TC_NDN, T - t0);
+    const int t0 = c * chunk, n = (int)min((int64_t)chunk, T - t0);
     dn[i] = make_int4(1, 0, t0, n | (b << 16));
   }
   if (e < E && ne > 0) {
@@ -794,14 +859,14 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict
     int o = n_sg + scan_gu[e] - tg;
     for (int c = 0; c < cg; ++c)
       for (int b = 0; b < F / TC_BM; ++b) {
-        const int n = min(TC_NGU, ne - c * TC_NGU);
-        gu[o++] = make_int4(0, e, base + c * TC_NGU, n | (b << 16));
+        const int n = min(chunk, ne - c * chunk);
+        gu[o++] = make_int4(0, e, base + c * chunk, n | (b << 16));
       }
     o = n_sd + scan_dn[e] - td;
     for (int c = 0; c < cd; ++c)
       for (int b = 0; b < D / (2 * TC_BM); ++b) {
-        const int n = min(TC_NDN, ne - c * TC_NDN);
-        dn[o++] = make_int4(0, e, base + c * TC_NDN, n | (b << 16));
+        const int n = min(chunk, ne - c * chunk);
+        dn[o++] = make_int4(0, e, base + c * chunk, n | (b << 16));
       }
   }
   if (e == 1023) {
@@ -813,7 +878,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t *__restrict
 template <int MODE, int FMT = DS_Q2_K>
 constexpr size_t tc_smem() {
   using C = TcCfg<MODE, FMT>;
-  return 1024 + C::STAGES * C::STAGE_BYTES + C::RAW * C::RAW_BYTES + sizeof(TcShared);
+  return 1024 + C::RING_BYTES + C::RAW * C::RAW_BYTES + sizeof(TcShared);
 }
 static_assert(tc_smem<MODE_GU>() <= 227 * 1024 && tc_smem<MODE_DN>() <= 227 * 1024 &&
                   tc_smem<MODE_ROUTER>() <= 227 * 1024 && tc_smem<MODE_GU, DS_Q4_K>() <= 227 * 1024 &&
@@ -888,8 +953,8 @@ cudaError_t launch_router_tc(const Shape &sh, const ds_moe_weights &W, const voi
   CUtensorMap m_wr, m_x;
   if (!make_map(&m_wr, W.router_w, sh.E, sh.D, TC_BM, true) || !make_map(&m_x, x, T, sh.D, TC_NRT, true))
     return cudaErrorInvalidValue;
-  tc_gemm_kernel<MODE_ROUTER><<<std::min<int>(sms, a.router_tiles), TC_THREADS, tc_smem<MODE_ROUTER>(), s>>>(a, m_wr, m_x, m_x, m_x, m_x,
-                                                                                              m_x, m_wr, m_wr);
+  tc_gemm_kernel<MODE_ROUTER><<<std::min<int>(sms, a.router_tiles), TC_THREADS, tc_smem<MODE_ROUTER>(), s>>>(
+      a, m_wr, m_x, m_x, m_x, m_x, m_x, m_x, m_x, m_wr, m_wr);
   return cudaGetLastError();
 }
 
@@ -964,8 +1029,8 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
         (const uint16_t *)W.shared_down, n8, sd16, st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  tc_plan_kernel<<<1, 1024, 0, s>>>(wk.counts, wk.offsets, sh.E, T, P, sh.D, sh.F, sh.Fs, tiles_gu, tiles_dn, cnt,
-                                    cnt + 1);
+  tc_plan_kernel<<<1, 1024, 0, s>>>(wk.counts, wk.offsets, sh.E, T, P, sh.D, sh.F, sh.Fs, q4 ? 0 : 1, tiles_gu,
+                                    tiles_dn, cnt, cnt + 1, cnt + 2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   TcArgs a{};
@@ -977,13 +1042,17 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
   a.y = wk.y;
   a.ys = wk.ys;
   a.status = st;
+  a.wide = cnt + 2;
 
-  CUtensorMap m_xp, m_x, m_sg, m_su, m_h, m_sd;
+  // token boxes of the wide layout (Q2_K): 256 rows; Q4_K has none
+  const int wrows = q4 ? TC_NGU : TC_NWIDE;
+  CUtensorMap m_xp, m_x, m_xw, m_sg, m_su, m_h, m_sd;
   const int fs1 = std::max(sh.Fs, TC_BM);
-  if (!make_map(&m_xp, xp, P, sh.D, TC_NGU, false) || !make_map(&m_x, x, T, sh.D, TC_NGU, true) ||
+  if (!make_map(&m_xp, xp, P, sh.D, wrows, false) || !make_map(&m_x, x, T, sh.D, TC_NGU, true) ||
+      !make_map(&m_xw, x, T, sh.D, wrows, true) ||
       !make_map(&m_sg, sh.Fs > 0 ? (const void *)W.shared_gate : (const void *)W.experts, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
       !make_map(&m_su, sh.Fs > 0 ? (const void *)W.shared_up : (const void *)W.experts, sh.Fs > 0 ? sh.Fs : 1, sh.D, TC_BM, true) ||
-      !make_map(&m_h, h16, P, sh.F, TC_NDN, false) ||
+      !make_map(&m_h, h16, P, sh.F, wrows, false) ||
       !make_map(&m_sd, sd16, sh.D, fs1, TC_BM, false))
     return cudaErrorInvalidValue;
   CUtensorMap m_rgu, m_rdn;
@@ -993,33 +1062,35 @@ cudaError_t launch_prefill_tc(const Shape &sh, const ds_moe_weights &W, const vo
     return cudaErrorInvalidValue;
   a.tiles = tiles_gu;
   a.n_tiles = cnt;
-  // routed token rows with boxes of 32, 64, 96 and 128 rows
-  CUtensorMap m_xp32, m_xp64, m_xp96;
+  // routed token rows with boxes of 32, 64, 96, 128 and chunk rows
+  CUtensorMap m_xp32, m_xp64, m_xp96, m_xp128;
   if (!make_map(&m_xp32, xp, P, sh.D, 32, false) || !make_map(&m_xp64, xp, P, sh.D, 64, false) ||
-      !make_map(&m_xp96, xp, P, sh.D, 96, false))
+      !make_map(&m_xp96, xp, P, sh.D, 96, false) || !make_map(&m_xp128, xp, P, sh.D, 128, false))
     return cudaErrorInvalidValue;
   if (q4)
     tc_gemm_kernel<MODE_GU, DS_Q4_K><<<sms, TC_THREADS, tc_smem<MODE_GU, DS_Q4_K>(), s>>>(
-        a, m_rgu, m_xp32, m_xp64, m_xp96, m_xp, m_x, m_sg, m_su);
+        a, m_rgu, m_xp32, m_xp64, m_xp96, m_xp128, m_xp, m_x, m_xw, m_sg, m_su);
   else
-    tc_gemm_kernel<MODE_GU><<<sms, TC_THREADS, tc_smem<MODE_GU>(), s>>>(a, m_rgu, m_xp32, m_xp64, m_xp96, m_xp, m_x, m_sg,
-                                                                        m_su);
+    tc_gemm_kernel<MODE_GU><<<sms, TC_THREADS, tc_smem<MODE_GU>(), s>>>(a, m_rgu, m_xp32, m_xp64, m_xp96, m_xp128, m_xp,
+                                                                        m_x, m_xw, m_sg, m_su);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the shared rows of h have n_ff_shared columns: their own map
-  CUtensorMap m_hs;
-  if (!make_map(&m_hs, h16 + (size_t)P * sh.F, T, std::max(sh.Fs, 64), TC_NDN, false)) return cudaErrorInvalidValue;
+  CUtensorMap m_hs, m_hsw;
+  if (!make_map(&m_hs, h16 + (size_t)P * sh.F, T, std::max(sh.Fs, 64), TC_NGU, false) ||
+      !make_map(&m_hsw, h16 + (size_t)P * sh.F, T, std::max(sh.Fs, 64), wrows, false))
+    return cudaErrorInvalidValue;
   a.tiles = tiles_dn;
   a.n_tiles = cnt + 1;
-  CUtensorMap m_h32, m_h64, m_h96;
+  CUtensorMap m_h32, m_h64, m_h96, m_h128;
   if (!make_map(&m_h32, h16, P, sh.F, 32, false) || !make_map(&m_h64, h16, P, sh.F, 64, false) ||
-      !make_map(&m_h96, h16, P, sh.F, 96, false))
+      !make_map(&m_h96, h16, P, sh.F, 96, false) || !make_map(&m_h128, h16, P, sh.F, 128, false))
     return cudaErrorInvalidValue;
   if (q4)
     tc_gemm_kernel<MODE_DN, DS_Q4_K><<<sms, TC_THREADS, tc_smem<MODE_DN, DS_Q4_K>(), s>>>(
-        a, m_rdn, m_h32, m_h64, m_h96, m_h, m_hs, m_sd, m_sd);
+        a, m_rdn, m_h32, m_h64, m_h96, m_h128, m_h, m_hs, m_hsw, m_sd, m_sd);
   else
-    tc_gemm_kernel<MODE_DN><<<sms, TC_THREADS, tc_smem<MODE_DN>(), s>>>(a, m_rdn, m_h32, m_h64, m_h96, m_h, m_hs, m_sd,
-                                                                        m_sd);
+    tc_gemm_kernel<MODE_DN><<<sms, TC_THREADS, tc_smem<MODE_DN>(), s>>>(a, m_rdn, m_h32, m_h64, m_h96, m_h128, m_h, m_hs,
+                                                                        m_hsw, m_sd, m_sd);
   return cudaGetLastError();
 }
 
