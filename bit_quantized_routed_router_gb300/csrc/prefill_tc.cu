@@ -9,18 +9,20 @@
 //
 // Both contractions run "weights as M": a tile is 128 weight rows (the f
 // rows of gate and up, or the d rows of down) times up to N tokens of one
-// expert (N rounded up to a multiple of 16), so an expert with 96 tokens
-// wastes no more than 15 columns.  Per tile and 64-wide K step:
+// expert (N rounded up to a multiple of 16; at most 128, or 256 when the
+// tile plan picks the wide layout for a launch), so an expert with 96
+// tokens wastes no more than 15 columns.  Per tile and 64-wide K step:
 //
 //   dequant warps  Q2_K rows -> fp16 in the 128-byte swizzled K-major layout
 //                  of the MMA, from raw copies (96 bytes per row holding one
 //                  84-byte block, 128 rows per tensor copy) that the copy
-//                  warp stages in shared memory two blocks ahead;
+//                  warp stages in shared memory ahead of them;
 //   copy warp      bulk-tensor (TMA) loads of the token rows (fp16) and, for
 //                  the dense shared expert, of its weight rows;
 //   MMA thread     tcgen05.mma kind::f16, fp32 accumulators in tensor memory
 //                  (two accumulator buffers, so the epilogue of one tile
-//                  overlaps the main loop of the next);
+//                  overlaps the main loop of the next; a tile wider than 128
+//                  tokens takes both);
 //   epilogue warps tcgen05.ld of the accumulators: SiLU(g) * u -> h (fp16),
 //                  or y (fp32).
 //
