@@ -250,17 +250,31 @@ def _tc(T, Fs, k, E, zipf=0.0, seed=7):
                    router_dtype="bf16", router_sigma=0.02, zipf_s=zipf, seed=seed)
 
 
-@pytest.mark.parametrize("T,Fs,k,E,zipf", [(300, 1024, 4, 16, 0.0), (64, 1024, 2, 8, 0.0),
-                                            (200, 0, 6, 40, 0.0), (520, 1024, 6, 32, 1.1)])
-def test_prefill_tensor_core_path(T, Fs, k, E, zipf):
+def wide_layout(counts):
+    """Whether the tile plan takes token chunks of up to 256 (Q2_K): when they
+    cut the routed chunks of up to 128 by more than a tenth."""
+    used = counts[counts > 0]
+    n128, n256 = int(np.sum((used + 127) // 128)), int(np.sum((used + 255) // 256))
+    return 10 * n256 < 9 * n128
+
+
+@pytest.mark.parametrize("T,Fs,k,E,zipf,wide", [(300, 1024, 4, 16, 0.0, False), (64, 1024, 2, 8, 0.0, False),
+                                                 (200, 0, 6, 40, 0.0, False), (520, 1024, 6, 32, 1.1, True),
+                                                 (600, 1024, 6, 8, 0.0, True)])
+def test_prefill_tensor_core_path(T, Fs, k, E, zipf, wide):
     """Batches of 64 tokens or more with bf16 inputs and widths that are
     multiples of 1024 run the expert FFNs as grouped tcgen05 GEMMs: the whole
     output against the oracle at the prefill tolerance.  The cases cover the
     smallest batch of the path, several 128-token chunks per expert (ragged
-    last chunks), no shared expert, an odd expert count, and a Zipf-skewed
-    route whose hottest experts exceed one 256-token down chunk."""
+    last chunks), no shared expert, an odd expert count, and, in the wide
+    layout (tiles of up to 256 tokens), a Zipf-skewed route whose hottest
+    experts exceed one 256-token chunk and a route of about 450 tokens per
+    expert (ragged 256-token chunks)."""
     cfg = _tc(T, Fs, k, E, zipf)
     assert ds.layer_path(synthetic.shape_of(cfg), T) == ds.PATH_TENSOR_CORE
+    lo, att, x64 = oracle_case(cfg)
+    ids, _ = oracle.select(lo.logits(x64), cfg.k)
+    assert wide_layout(np.bincount(ids.ravel(), minlength=cfg.E)) == wide
     layer_parity(cfg, PREFILL_TOL)
 
 
