@@ -673,7 +673,7 @@ struct StreamShared {
   int ready;           // the route above is published
   int abort_;          // a wait expired
   int go;              // consumers continue past the grid barrier
-  int tile[S_NS];                  // phase-A tile in each stage: shared i >= 0, routed -1 - r
+  int tile[S_NS];                  // phase-A tile in each stage: shared i >= 0, routed -1 - (slot << 16 | row group)
   float reda[S_MAXT][S_CONS][4];   // per shared tile: partial gate/up sums of each warp
   float redb[S_MAXT][S_CONS][4];   // per phase-B tile: partial shared-down sums of each warp
   float yrb[S_MAXT][S_MAXP];       // per phase-B tile: routed down results [slot * rb + row]
@@ -785,6 +785,7 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
   const int ngrp = (F + S_GU - 1) / S_GU;       // routed gate/up tiles per slot
   const int nslots = a.n_slots;
   const int nB = D / rb;
+  const int lrb = 31 - __clz(rb);  // rb is 1, 2 or 4: pair p is (slot p >> lrb, row p & (rb - 1))
   // this block's phase-A tiles; routed tiles are dealt from the last block
   // down, so the blocks with one shared tile fewer get one routed tile more
   const int rbid = G - 1 - bid;
@@ -856,7 +857,7 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
       } else {
         if (!have_route && !(have_route = s_wait_ready(S, a.status))) { ok = false; break; }
         const int r = rbid + G * jr++, u = r / ngrp, g = r % ngrp;
-        S.tile[st] = -1 - r;
+        S.tile[st] = -1 - ((u << 16) | g);  // the consumers take u and g without a division
         const int rows = min(S_GU, F - g * S_GU);
         bool far = false;
         const uint8_t *gr = u < S.rt_nu ? expert_at(a, S.rt_used[u], far) + (int64_t)g * S_GU * rowb_d : nullptr;
@@ -969,7 +970,7 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
         nu = rdy ? S.rt_nu : 0;
         have_route = true;
       }
-      const int r = -1 - td, u = r / ngrp, g = r % ngrp;
+      const int ug = -1 - td, u = ug >> 16, g = ug & 0xFFFF;
       const int f = g * S_GU + warp;
       if (got && u < nu && f < F) {
         typename RD::Row gp, up;
@@ -1105,9 +1106,9 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
     // host memory for an expert that has no cache slot
     auto load_down_row = [&](int p, typename RF::Row &row) {
       bool far;
-      const uint8_t *hp = expert_at(a, S.rt_used[p / rb], far);
+      const uint8_t *hp = expert_at(a, S.rt_used[p >> lrb], far);
       if (far)
-        warp_copy_row(hp + 2 * a.gate_bytes + (int64_t)((bid + G * m) * rb + p % rb) * rowb_f,
+        warp_copy_row(hp + 2 * a.gate_bytes + (int64_t)((bid + G * m) * rb + (p & (rb - 1))) * rowb_f,
                       const_cast<uint8_t *>(routed) + (size_t)p * rowb_f, rowb_f);
       RF::load_s(routed + (size_t)p * rowb_f, row);
     };
@@ -1123,7 +1124,7 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
       if (lane == 0) mbar_arrive(&S.empty[st]);
       if (got && 2 * warp < np) {
         if ((rb & 1) == 0) {  // one slot: its planes in registers, two dots
-          const uint32_t *pl = hpl + (2 * warp / rb) * hw;
+          const uint32_t *pl = hpl + ((2 * warp) >> lrb) * hw;
           typename RF::XR hr;
           RF::load_x(pl, reinterpret_cast<const float *>(pl + RF::NPL * nsb_f), nsb_f, hr);
           y[0] = RF::dot_reg(rp[0], hr);
@@ -1133,7 +1134,7 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
           for (int h = 0; h < 2; ++h) {
             const int p = 2 * warp + h;
             if (p < np) {
-              const uint32_t *pl = hpl + (p / rb) * hw;
+              const uint32_t *pl = hpl + (p >> lrb) * hw;
               y[h] = RF::dot(rp[h], pl, reinterpret_cast<const float *>(pl + RF::NPL * nsb_f), nsb_f);
             }
           }
@@ -1158,7 +1159,7 @@ __global__ void __maxnreg__(RD::BB == QB ? S_REGS : 128) stream_kernel(const Arg
         if (got) {
           typename RF::Row rp;
           load_down_row(p, rp);
-          const uint32_t *pl = hpl + (p / rb) * hw;
+          const uint32_t *pl = hpl + (p >> lrb) * hw;
           yy = RF::dot(rp, pl, reinterpret_cast<const float *>(pl + RF::NPL * nsb_f), nsb_f);
         }
         yy = warp_sum(yy);

@@ -342,12 +342,23 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
   // was there.  Shared-expert tiles (no route needed) come first.
   const bool producer = warp == MT_CONS - 1 && lane == 0;
   int n_tiles = n_sh * NB;  // routed tiles are added once the route is known
+  // the tiles are issued in order: their coordinates advance without divisions
+  int p_kb = 0, p_c = b % NCd, p_sg = b / NCd;                   // shared: item b + G m, box kb
+  const int p_gd = G / NCd, p_gm = G % NCd;
+  int p_cl = 0, p_u = rr0 / max(NG, 1), p_g = rr0 % max(NG, 1);  // routed: item rr0 + Gq r, chunk cl
+  const int p_qd = Gq / max(NG, 1), p_qm = Gq % max(NG, 1);
   auto issue = [&](int i) -> bool {
     const int st = i % MT_NS;
     if (i >= MT_NS && !mt_wait(&S.empty[st], ((i / MT_NS) & 1) ^ 1, S, a.status)) return false;
     uint8_t *dst = stages + (size_t)st * MT_STAGE;
     if (i < n_sh * NB) {
-      const int it = b + G * (i / NB), kb = i % NB, c = it % NCd, sg = it / NCd;
+      const int kb = p_kb, c = p_c, sg = p_sg;
+      if (++p_kb == NB) {
+        p_kb = 0;
+        p_c += p_gm;
+        p_sg += p_gd;
+        if (p_c >= NCd) p_c -= NCd, ++p_sg;
+      }
       const bool gate = sg < n_sh_groups / 2;
       const int row0 = (gate ? sg : sg - n_sh_groups / 2) * MT_SH_ROWS;
       S.desc[st] = make_int4(0, sg, kb, c);
@@ -356,8 +367,13 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
       tma2d(dst, gate ? &m_sg : &m_su, kx, row0, &S.full[st]);
       tma2d(dst + MT_SH_BOX, &m_x, kx, 0, &S.full[st]);
     } else {
-      const int r = i - n_sh * NB, it = rr0 + Gq * (r / NCq), cl = r % NCq;
-      const int u = it / NG, g = it % NG, e = s_used[u];
+      const int cl = p_cl, u = p_u, g = p_g, e = s_used[u];
+      if (++p_cl == NCq) {
+        p_cl = 0;
+        p_g += p_qm;
+        p_u += p_qd;
+        if (p_g >= NG) p_g -= NG, ++p_u;
+      }
       S.desc[st] = make_int4(1, u, g, cl);
       mbar_arrive_expect_tx(&S.full[st], 2u * MT_GU_NR * MT_CB);
       const int xw = (q * NCq + cl) * (MT_CB / 4);
@@ -694,21 +710,36 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
   // previous expert's planes.
   const bool producer = warp == MT_CONS - 1 && lane == 0;
   bool h_ready = false;  // (producer lane) the h kernel has completed
+  // the tiles are issued in order: their coordinates advance without divisions
+  int p_it = r0, p_cl = 0, p_u = r0 / NG, p_g = r0 % NG;         // routed: item it, chunk cl
+  int p_kb = 0, p_cc = NCs > 0 ? b % NCs : 0, p_rs = NCs > 0 ? b / NCs : 0;  // shared: item b + G m, box kb
+  const int p_gd = NCs > 0 ? G / NCs : 0, p_gm = NCs > 0 ? G % NCs : 0;
   auto issue = [&](int i) -> bool {
     const int st = i % MT_NS;
     if (i >= MT_NS && !mt_wait(&S.empty[st], ((i / MT_NS) & 1) ^ 1, S, a.status)) return false;
     uint8_t *dst = stages + (size_t)st * MT_STAGE;
     if (i < n_rt) {
-      const int it = r0 + i / NCqd, cl = i % NCqd, u = it / NG, g = it % NG;
-      const bool first = cl == 0 && (it == r0 || (it - 1) / NG != u);
-      const bool last = cl == NCqd - 1 && (it == r1 - 1 || (it + 1) / NG != u);
+      const int it = p_it, cl = p_cl, u = p_u, g = p_g;
+      if (++p_cl == NCqd) {
+        p_cl = 0;
+        ++p_it;
+        if (++p_g == NG) p_g = 0, ++p_u;
+      }
+      // an expert's first and last tiles: row group 0 or NG - 1, or the ends of this block's range
+      const bool first = cl == 0 && (it == r0 || g == 0);
+      const bool last = cl == NCqd - 1 && (it == r1 - 1 || g == NG - 1);
       S.desc[st] = make_int4(1, u, g, cl | (first ? 256 : 0) | (last ? 512 : 0));
       mbar_arrive_expect_tx(&S.full[st], (uint32_t)MT_DN_NR * MT_CB);
       tma3d(dst, &m_rdn, (q * NCqd + cl) * (MT_CB / 4), g * MT_DN_NR, s_used[u], &S.full[st]);
     } else {
       if (!h_ready) { pdl_wait(); h_ready = true; }  // hs is written by the h kernel
-      const int m = (i - n_rt) / NB, kb = (i - n_rt) % NB;
-      const int it = b + G * m, cc = it % NCs, rs = it / NCs;
+      const int kb = p_kb, cc = p_cc, rs = p_rs;
+      if (++p_kb == NB) {
+        p_kb = 0;
+        p_cc += p_gm;
+        p_rs += p_gd;
+        if (p_cc >= NCs) p_cc -= NCs, ++p_rs;
+      }
       S.desc[st] = make_int4(0, rs, kb, cc);
       mbar_arrive_expect_tx(&S.full[st], MT_SH_BOX + 2u * a.T8 * 128);
       const int kx = cc * MT_CHUNK + kb * MT_BOX_K;
