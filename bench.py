@@ -248,7 +248,7 @@ LAUNCHES_PER_DECODE_STEP = 2  # router logits; the one-token streaming kernel
 # 100,035,840 read + 2,830,080 written; the commands are in the decode profile
 # summary).  Set to None whenever either kernel changes until it is captured
 # again.
-DECODE_STEP_DRAM_BYTES = 104_984_832
+DECODE_STEP_DRAM_BYTES = None
 
 PREFILL_FLOPS = 1.4517e12  # 4096 x (6*3*2*D*F + 3*2*D*F + 2*D*E) at the Flash shape
 
