@@ -245,10 +245,10 @@ def gpu_arm(args, rank, world, local_rank):
 LAUNCHES_PER_DECODE_STEP = 2  # router logits; the one-token streaming kernel
 # DRAM bytes read + written by one decode step, from one ncu capture of these
 # kernels as they stand (route_kernel 2,118,912 read; stream_kernel
-# 100,035,840 read + 2,830,080 written; the commands are in the decode profile
+# 100,054,016 read + 3,266,816 written; the commands are in the decode profile
 # summary).  Set to None whenever either kernel changes until it is captured
 # again.
-DECODE_STEP_DRAM_BYTES = None
+DECODE_STEP_DRAM_BYTES = 105_439_744
 
 PREFILL_FLOPS = 1.4517e12  # 4096 x (6*3*2*D*F + 3*2*D*F + 2*D*E) at the Flash shape
 
